@@ -1,0 +1,471 @@
+"""Pins for the fp64 oracle. CPU only.
+
+Each test ties an oracle function to something the oracle does not compute
+itself: a number printed on a page, a closed form, a library routine
+(torch's scaled_dot_product_attention), an invariant of the mathematics, or a
+brute-force construction. ``test_planted_mistakes_are_caught`` then plants
+plausible bugs in the oracle and checks that these pins catch them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+GiB = 1 << 30
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Printed numbers: cache bytes, capacity, parameters, operation counts
+# ---------------------------------------------------------------------------
+
+
+def test_cache_bytes_printed_table():
+    g = gold("p1_cache_bytes.json")
+    for shape in g["shapes"].values():
+        L, H, D = shape["layers"], shape["heads"], shape["head_dim"]
+        mha = O.kv_cache_bytes(L, H, D, 1, shape["dtype_bytes"])
+        gqa = O.kv_cache_bytes(L, 8, D, 1, shape["dtype_bytes"])
+        mla = O.mla_cache_bytes(L, shape["d_c"], shape["d_rope"], 1, shape["dtype_bytes"])
+        assert (mha, gqa, mla) == (shape["mha"], shape["gqa8"], shape["mla"])
+        assert f"{mha / gqa:.1f}" == shape["gqa8_ratio"]
+        assert f"{mha / mla:.1f}" == shape["mla_ratio"]
+        assert f"{gqa / mla:.1f}" == shape["mla_vs_gqa8"]
+
+
+def test_decoupled_rope_cost_printed():
+    g = gold("p1_cache_bytes.json")["decoupled_rope_deepseek_v2"]
+    latent = O.mla_cache_bytes(60, 512, 0, 1)
+    full = O.mla_cache_bytes(60, 512, 64, 1)
+    assert (latent, full, full - latent) == (g["latent_only"], g["with_rope"], g["added"])
+    assert f"{100 * (full - latent) / latent:.1f}" == g["added_percent"]
+    assert f"{O.kv_cache_bytes(60, 128, 128, 1) / full:.1f}" == g["vs_mha"]
+
+
+def test_per_layer_elements_and_unverifiable_quote():
+    g = gold("p1_cache_bytes.json")
+    e = g["per_layer_elements"]
+    assert O.mla_cache_bytes(1, 512, 64, 1, dtype_bytes=1) == e["mla"]
+    assert O.kv_cache_bytes(1, 128, 128, 1, dtype_bytes=1) == e["mha"]
+    # The quoted 93.3% is not what the pages' formulas give; record what they do give.
+    red = 1 - O.mla_cache_bytes(60, 512, 64, 1) / O.kv_cache_bytes(60, 128, 128, 1)
+    assert f"{100 * red:.2f}" == "98.24"
+    assert g["quoted_not_derivable"]["reduction_vs_mha_percent_quoted"] == "93.3"
+
+
+def test_capacity_in_80_gib_printed():
+    g = gold("p1_capacity_80gib.json")
+    s = g["shape"]
+    budget = g["budget_gib"] * GiB
+    for row in g["rows"]:
+        n = row["context"]
+        mha = O.kv_cache_bytes(s["layers"], s["heads"], s["head_dim"], n)
+        gqa = O.kv_cache_bytes(s["layers"], s["gqa_groups"], s["head_dim"], n)
+        mla = O.mla_cache_bytes(s["layers"], s["d_c"], s["d_rope"], n)
+        assert f"{mha / GiB:.2f}" == row["mha_gib"]
+        assert f"{gqa / GiB:.2f}" == row["gqa8_gib"]
+        assert f"{mla / GiB:.2f}" == row["mla_gib"]
+        assert O.sequences_in_budget(budget, mla) == row["mla_seqs"]
+    n = 32768
+    got = {
+        "mha": O.sequences_in_budget(budget, O.kv_cache_bytes(60, 128, 128, n)),
+        "gqa8": O.sequences_in_budget(budget, O.kv_cache_bytes(60, 8, 128, n)),
+        "mla": O.sequences_in_budget(budget, O.mla_cache_bytes(60, 512, 64, n)),
+    }
+    assert got == g["seqs_at_32k"]
+
+
+def test_params_per_layer_printed():
+    p = gold("p1_params_macs.json")["params"]
+    kw = dict(d_model=p["d_model"], n_heads=p["heads"], head_dim=p["head_dim"])
+    mha = O.attention_params_per_layer("mha", **kw)
+    gqa = O.attention_params_per_layer("gqa", kv_groups=p["gqa_groups"], **kw)
+    mla = O.attention_params_per_layer("mla", d_c=p["d_c"], d_rope=p["d_rope"], **kw)
+    assert (mha, gqa, mla) == (p["mha"], p["gqa8"], p["mla"])
+    assert f"{mla / mha:.2f}" == p["mla_vs_mha"]
+    assert f"{mla / gqa:.2f}" == p["mla_vs_gqa8"]
+
+
+def test_operation_counts_printed():
+    g = gold("p1_params_macs.json")
+    m = g["macs"]
+    for row in m["rows"]:
+        e, a = O.macs_per_head_per_step(row["n"], m["d_model"], m["d_c"], m["head_dim"])
+        assert (e, a) == (row["expanded"], row["absorbed"])
+        assert f"{e / a:.2f}" == row["saving"]
+    r = g["rebuild"]
+    assert O.rebuild_absorbed_macs(r["steps"], r["heads"], r["d_model"], r["head_dim"],
+                                   r["d_c"]) == r["extra_macs"]
+
+
+def test_operation_counts_by_brute_force():
+    """Count the multiplies of each path on a tiny case by running it."""
+    d_model, d_c, d_h, n = 5, 4, 3, 7
+    # expanded: keys c@W_uk (n*d_c*d_h), query x@W_q (d_model*d_h), scores K@q (n*d_h)
+    # absorbed: x@W_abs (d_model*d_c), scores C@q_lat (n*d_c)
+    count = {"e": 0, "a": 0}
+
+    def mm(a_shape, b_shape, key):
+        count[key] += a_shape[0] * a_shape[1] * b_shape[1]
+
+    mm((n, d_c), (d_c, d_h), "e")
+    mm((1, d_model), (d_model, d_h), "e")
+    mm((n, d_h), (d_h, 1), "e")
+    mm((1, d_model), (d_model, d_c), "a")
+    mm((n, d_c), (d_c, 1), "a")
+    assert O.macs_per_head_per_step(n, d_model, d_c, d_h) == (count["e"], count["a"])
+
+
+# ---------------------------------------------------------------------------
+# Softmax and RoPE
+# ---------------------------------------------------------------------------
+
+
+def test_softmax_rows_sum_to_one_and_match_library():
+    g = np.random.default_rng(11)
+    s = g.normal(0, 5, (64, 37))
+    s[:, 5] = -np.inf
+    p = O.softmax(s)
+    assert np.max(np.abs(p.sum(-1) - 1)) < 1e-12
+    assert np.all(p[:, 5] == 0)
+    ref = torch.softmax(torch.tensor(s, dtype=torch.float64), dim=-1).numpy()
+    assert np.max(np.abs(p - ref)) < 1e-14
+    # shift invariance; huge values do not overflow
+    assert np.max(np.abs(O.softmax(s + 1e4) - p)) < 1e-12
+
+
+def _rotation_matrix(pos, d_r, base):
+    """Explicit block rotation: plane (i, i + d_r/2) turned by pos*base^(-2i/d_r)."""
+    half = d_r // 2
+    M = np.zeros((d_r, d_r))
+    for i in range(half):
+        th = pos * base ** (-2.0 * i / d_r)
+        c, s = math.cos(th), math.sin(th)
+        M[i, i], M[i, i + half] = c, -s
+        M[i + half, i], M[i + half, i + half] = s, c
+    return M
+
+
+def test_rope_matches_explicit_rotation_and_preserves_norm():
+    g = np.random.default_rng(12)
+    for d_r in (2, 8, 64):
+        x = g.normal(size=(5, d_r))
+        pos = np.array([0, 1, 17, 4095, 131071])
+        y = O.apply_rope(x, pos, 10000.0)
+        for k in range(5):
+            ref = _rotation_matrix(int(pos[k]), d_r, 10000.0) @ x[k]
+            assert np.max(np.abs(y[k] - ref)) < 1e-9
+        assert np.max(np.abs(np.linalg.norm(y, axis=-1) - np.linalg.norm(x, axis=-1))) < 1e-12
+        assert np.array_equal(O.apply_rope(x[:1], np.array([0]), 10000.0), x[:1])
+
+
+def test_rope_d2_is_complex_multiplication():
+    g = np.random.default_rng(13)
+    x = g.normal(size=(9, 2))
+    pos = np.arange(9) * 3
+    y = O.apply_rope(x, pos, 10000.0)
+    z = (x[:, 0] + 1j * x[:, 1]) * np.exp(1j * pos)   # theta_0 = 1 for i = 0
+    assert np.max(np.abs(y[:, 0] - z.real)) < 1e-12
+    assert np.max(np.abs(y[:, 1] - z.imag)) < 1e-12
+
+
+def test_rope_relative_position_invariance():
+    g = np.random.default_rng(14)
+    a, b = g.normal(size=64), g.normal(size=64)
+    base = 10000.0
+    for m, n in [(0, 5), (100, 105), (131066, 131071), (7, 2), (50007, 50002)]:
+        d1 = O.apply_rope(a, m, base) @ O.apply_rope(b, n, base)
+        d0 = O.apply_rope(a, 0, base) @ O.apply_rope(b, n - m, base) if n >= m else \
+            O.apply_rope(a, m - n, base) @ O.apply_rope(b, 0, base)
+        assert abs(d1 - d0) < 1e-9
+    # and it does change with the offset
+    assert abs(O.apply_rope(a, 0, base) @ O.apply_rope(b, 3, base)
+               - O.apply_rope(a, 0, base) @ O.apply_rope(b, 4, base)) > 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Attention: absorbed == materialised == textbook
+# ---------------------------------------------------------------------------
+
+
+def _tiny(seed=0, n_h=4, d_model=32, d_c=16, d_r=8, d_nope=8, d_v=8, L=37):
+    g = np.random.default_rng(seed)
+    W_dkv = g.normal(0, d_model ** -0.5, (d_model, d_c))
+    W_kr = g.normal(0, d_model ** -0.5, (d_model, d_r))
+    W_uk = g.normal(0, d_c ** -0.5, (d_c, n_h * d_nope))
+    W_uv = g.normal(0, d_c ** -0.5, (d_c, n_h * d_v))
+    X = g.normal(size=(L, d_model))
+    rows = O.latent_rows(X, W_dkv, W_kr, np.arange(L), 10000.0)
+    q = g.normal(size=(1, 2, n_h, d_nope + d_r))
+    return dict(W_dkv=W_dkv, W_kr=W_kr, W_uk=W_uk, W_uv=W_uv, X=X, rows=rows, q=q,
+                n_h=n_h, d_c=d_c, d_r=d_r, d_nope=d_nope, d_v=d_v, L=L)
+
+
+def _sdpa_reference(t, n_q):
+    """Textbook attention via torch's scaled_dot_product_attention.
+
+    Keys and values are built explicitly per head: k = [c W_uk_h | k_rope],
+    v = c W_uv_h; the query is [q_nope | RoPE(q_rope, pos)].
+    """
+    d_c, d_nope, d_v, n_h, L = t["d_c"], t["d_nope"], t["d_v"], t["n_h"], t["L"]
+    C, KR = t["rows"][:, :d_c], t["rows"][:, d_c:]
+    out = np.zeros((n_q, n_h, d_v))
+    for h in range(n_h):
+        K = np.concatenate([C @ t["W_uk"][:, h * d_nope:(h + 1) * d_nope], KR], axis=1)
+        V = C @ t["W_uv"][:, h * d_v:(h + 1) * d_v]
+        Q = []
+        for i in range(n_q):
+            pos = L - n_q + i
+            qh = t["q"][0, i, h]
+            Q.append(np.concatenate([qh[:d_nope], O.apply_rope(qh[d_nope:], pos, 10000.0)]))
+        Q = torch.tensor(np.array(Q))[None, None]
+        mask = torch.tensor(np.arange(L)[None, :] <= (L - n_q + np.arange(n_q))[:, None])
+        o = torch.nn.functional.scaled_dot_product_attention(
+            Q, torch.tensor(K)[None, None], torch.tensor(V)[None, None],
+            attn_mask=mask[None, None], scale=O.default_scale(d_nope, t["d_r"]))
+        out[:, h] = o[0, 0].numpy()
+    return out
+
+
+def _oracle_out(t, n_q):
+    return O.decode_materialised(t["q"][:, :n_q], [t["rows"]], [t["L"]], t["W_uk"], t["W_uv"],
+                                 t["d_c"], t["d_nope"], t["d_v"],
+                                 O.default_scale(t["d_nope"], t["d_r"]), 10000.0)[0]
+
+
+@pytest.mark.parametrize("n_q", [1, 2])
+def test_materialised_matches_library_attention(n_q):
+    t = _tiny(seed=1)
+    got = _oracle_out(t, n_q)
+    ref = _sdpa_reference(t, n_q)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_absorbed_equals_materialised():
+    t = _tiny(seed=2, L=64)
+    scale = O.default_scale(t["d_nope"], t["d_r"])
+    worst = 0.0
+    for h in range(t["n_h"]):
+        wuk = O.head_slice(t["W_uk"], h, t["d_nope"])
+        wuv = O.head_slice(t["W_uv"], h, t["d_v"])
+        for pos in (63, 40):
+            a = O.decode_head_absorbed(t["q"][0, 0, h], t["rows"], pos, wuk, wuv, t["d_c"], scale, 1e4)
+            m = O.decode_head_materialised(t["q"][0, 0, h], t["rows"], pos, wuk, wuv, t["d_c"], scale, 1e4)
+            worst = max(worst, np.max(np.abs(a - m)))
+    assert worst <= gold("p1_params_macs.json")["float_noise_bound"]
+
+
+def test_full_fold_scores_equal_expanded():
+    """P1's fold: (x W_q)(c W_uk)^T == (x (W_q W_uk^T)) c^T; and the reversed fold."""
+    g = np.random.default_rng(3)
+    d_model, d_c, d_h, n = 32, 16, 8, 64
+    W_q = g.normal(size=(d_model, d_h))
+    W_uk = g.normal(size=(d_c, d_h))
+    W_uv = g.normal(size=(d_c, d_h))
+    x = g.normal(size=(1, d_model))
+    C = g.normal(size=(n, d_c))
+    expanded = (x @ W_q) @ (C @ W_uk).T
+    W_abs = O.absorb_q_full(W_q, W_uk)
+    assert W_abs.shape == (d_model, d_c)
+    got = O.scores_absorbed(x, W_abs, C)
+    assert np.max(np.abs(got - expanded)) <= 1e-10
+    # absorbing the wrong matrix keeps the shape but changes the answer
+    wrong = O.scores_absorbed(x, O.absorb_q_full(W_q, W_uv), C)
+    assert wrong.shape == got.shape and np.max(np.abs(wrong - expanded)) > 1e-3
+    # the transposed order is the same matrix, transposed: harmless
+    assert np.max(np.abs((W_uk @ W_q.T).T - W_abs)) == 0.0
+
+
+def test_rotating_after_absorbing_is_wrong():
+    """Rotating the absorbed query does not give the decoupled score."""
+    t = _tiny(seed=4, L=16)
+    d_c, d_nope, h = t["d_c"], t["d_nope"], 0
+    wuk = O.head_slice(t["W_uk"], h, d_nope)
+    q = t["q"][0, 0, h]
+    C, KR = t["rows"][:, :d_c], t["rows"][:, d_c:]
+    correct = C @ (wuk @ q[:d_nope]) + KR @ O.apply_rope(q[d_nope:], 15, 1e4)
+    # the broken variant: one rotation applied to the absorbed latent query
+    q_lat = wuk @ q[:d_nope]
+    broken = C @ O.apply_rope(q_lat, 15, 1e4)
+    assert np.max(np.abs(correct - broken)) > 1e-2
+
+
+def test_full_rank_mla_is_exactly_mha():
+    """P1's full-rank check: factor [W_k | W_v] at full rank, run MLA (no RoPE
+    block), compare with textbook multi-head attention over X W_k and X W_v."""
+    g = np.random.default_rng(5)
+    d_model, n_h, d_h, L = 32, 4, 8, 24
+    W_k = g.normal(0, 0.4, (d_model, n_h * d_h))
+    W_v = g.normal(0, 0.4, (d_model, n_h * d_h))
+    W_q = g.normal(0, 0.4, (d_model, n_h * d_h))
+    U, S, Vt = np.linalg.svd(np.concatenate([W_k, W_v], axis=1), full_matrices=False)
+    d_c = d_model
+    W_dkv, W_ukv = U[:, :d_c] * S[:d_c], Vt[:d_c]
+    W_uk, W_uv = W_ukv[:, :n_h * d_h], W_ukv[:, n_h * d_h:]
+    X = g.normal(size=(L, d_model))
+    rows = O.latent_rows(X, W_dkv, np.zeros((d_model, 0)), np.arange(L), 1e4)
+    q = (X[-1:] @ W_q).reshape(1, 1, n_h, d_h)
+    got = O.decode_materialised(q, [rows], [L], W_uk, W_uv, d_c, d_h, d_h,
+                                1 / math.sqrt(d_h), 1e4)[0, 0]
+    K = torch.tensor((X @ W_k).reshape(L, n_h, d_h).transpose(1, 0, 2))
+    V = torch.tensor((X @ W_v).reshape(L, n_h, d_h).transpose(1, 0, 2))
+    Q = torch.tensor(q[0].transpose(1, 0, 2))
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V)[:, 0].numpy()
+    assert np.max(np.abs(got - ref)) <= gold("p1_params_macs.json")["float_noise_bound"]
+
+
+def test_single_token_and_identical_rows():
+    t = _tiny(seed=6, L=1)
+    scale = O.default_scale(t["d_nope"], t["d_r"])
+    for h in range(t["n_h"]):
+        wuk = O.head_slice(t["W_uk"], h, t["d_nope"])
+        wuv = O.head_slice(t["W_uv"], h, t["d_v"])
+        o = O.decode_head_materialised(t["q"][0, 0, h], t["rows"], 0, wuk, wuv, t["d_c"], scale, 1e4)
+        assert np.max(np.abs(o - t["rows"][0, :t["d_c"]] @ wuv)) < 1e-13
+    # identical latent parts with zero rope parts: the scores are all equal,
+    # so the output is the mean of the values, which is the one value
+    rows = np.repeat(t["rows"][:1], 50, axis=0)
+    rows[:, t["d_c"]:] = 0.0
+    wuk = O.head_slice(t["W_uk"], 1, t["d_nope"])
+    wuv = O.head_slice(t["W_uv"], 1, t["d_v"])
+    o = O.decode_head_materialised(t["q"][0, 0, 1], rows, 49, wuk, wuv, t["d_c"], scale, 1e4)
+    assert np.max(np.abs(o - rows[0, :t["d_c"]] @ wuv)) < 1e-13
+
+
+def test_two_queries_are_causal():
+    """With n_q = 2 the first query must ignore the newest token entirely."""
+    t = _tiny(seed=7, L=20)
+    both = _oracle_out(t, 2)
+    first_alone = O.decode_materialised(t["q"][:, :1], [t["rows"][:19]], [19], t["W_uk"], t["W_uv"],
+                                        t["d_c"], t["d_nope"], t["d_v"],
+                                        O.default_scale(t["d_nope"], t["d_r"]), 1e4)[0, 0]
+    assert np.max(np.abs(both[0] - first_alone)) < 1e-13
+    # perturb the last row: query 0 unchanged, query 1 changes
+    t2 = dict(t)
+    t2["rows"] = t["rows"].copy()
+    t2["rows"][-1] += 1.0
+    both2 = _oracle_out(t2, 2)
+    assert np.max(np.abs(both2[0] - both[0])) == 0.0
+    assert np.max(np.abs(both2[1] - both[1])) > 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Paged layout and append
+# ---------------------------------------------------------------------------
+
+
+def test_append_places_rows_by_page_table():
+    g = np.random.default_rng(8)
+    bs, R, B = 4, 6, 3
+    d_model, d_c, d_r = 5, 4, 2
+    pt = np.array([[5, 2, -1], [0, 7, 3], [6, 1, 4]], dtype=np.int32)
+    cache = g.normal(size=(8, bs, R))
+    seq_idx = np.array([0, 1, 1, 2, 0])
+    pos = np.array([5, 0, 11, 6, 2])
+    x = g.normal(size=(5, d_model))
+    W_dkv, W_kr = g.normal(size=(d_model, d_c)), g.normal(size=(d_model, d_r))
+    out = O.append_to_paged_cache(cache, x, seq_idx, pos, pt, W_dkv, W_kr, 1e4, bs)
+    # brute force: block and slot written out by hand
+    where = {0: (2, 1), 1: (0, 0), 2: (3, 3), 3: (1, 2), 4: (5, 2)}
+    touched = set()
+    for t, (blk, slot) in where.items():
+        c = x[t] @ W_dkv
+        kr = O.apply_rope(x[t] @ W_kr, pos[t], 1e4)
+        assert np.max(np.abs(out[blk, slot] - np.concatenate([c, kr]))) < 1e-12
+        touched.add((blk, slot))
+    for blk in range(8):
+        for slot in range(bs):
+            if (blk, slot) not in touched:
+                assert np.array_equal(out[blk, slot], cache[blk, slot])
+    # gather reads the same rows back in logical order
+    seq1 = O.gather_sequence(out, pt, 1, 12, bs)
+    assert np.array_equal(seq1[0], out[0, 0]) and np.array_equal(seq1[11], out[3, 3])
+    assert np.array_equal(seq1[5], out[7, 1])
+
+
+# ---------------------------------------------------------------------------
+# The pins above must catch plausible mistakes in the oracle
+# ---------------------------------------------------------------------------
+
+
+def _mutants():
+    def rope_wrong_sign(x, pos, base):
+        x = np.asarray(x, dtype=np.float64)
+        half = x.shape[-1] // 2
+        if half == 0:
+            return x.copy()
+        a = O.rope_angles(pos, x.shape[-1], base)
+        c, s = np.cos(a), np.sin(a)
+        return np.concatenate([x[..., :half] * c + x[..., half:] * s,
+                               -x[..., :half] * s + x[..., half:] * c], -1)
+
+    def rope_interleaved(x, pos, base):
+        x = np.asarray(x, dtype=np.float64)
+        if x.shape[-1] == 0:
+            return x.copy()
+        a = O.rope_angles(pos, x.shape[-1], base)
+        c, s = np.cos(a), np.sin(a)
+        y = x.copy()
+        y[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+        y[..., 1::2] = x[..., 0::2] * s + x[..., 1::2] * c
+        return y
+
+    def no_rope_term(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
+        rows = np.array(rows, dtype=np.float64)
+        rows[:, d_c:] = 0.0
+        return ORIG_HEAD(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base)
+
+    def no_causal(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
+        return ORIG_HEAD(q_head, rows, rows.shape[0] - 1, W_uk_h, W_uv_h, d_c, scale, base)
+
+    def wrong_scale(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
+        return ORIG_HEAD(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c,
+                         1 / math.sqrt(W_uk_h.shape[1]), base)
+
+    def swapped_up(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
+        return ORIG_HEAD(q_head, rows, pos_q, W_uv_h, W_uk_h, d_c, scale, base)
+
+    def head_off_by_one(W, h, width):
+        W = np.asarray(W, dtype=np.float64)
+        n = W.shape[1] // width
+        h = (h + 1) % n
+        return W[:, h * width:(h + 1) * width]
+
+    def max_without_subtract(s, axis=-1):
+        e = np.exp(np.asarray(s, dtype=np.float64) * 1.0001)
+        return e / e.sum(axis=axis, keepdims=True)
+
+    return {
+        "apply_rope": [rope_wrong_sign, rope_interleaved],
+        "decode_head_materialised": [no_rope_term, no_causal, wrong_scale, swapped_up],
+        "head_slice": [head_off_by_one],
+        "softmax": [max_without_subtract],
+    }
+
+
+ORIG_HEAD = O.decode_head_materialised
+
+
+@pytest.mark.parametrize("target,idx", [(k, i) for k, v in _mutants().items() for i in range(len(v))])
+def test_planted_mistakes_are_caught(monkeypatch, target, idx):
+    mutant = _mutants()[target][idx]
+    monkeypatch.setattr(O, target, mutant)
+    failures = 0
+    for check in (lambda: test_materialised_matches_library_attention(2),
+                  test_rope_matches_explicit_rotation_and_preserves_norm,
+                  test_softmax_rows_sum_to_one_and_match_library):
+        try:
+            check()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"planted mistake in {target} went unnoticed"
