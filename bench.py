@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark the MLA latent-cache decode step on B300.
+
+A step is one pass of the whole hot path over one batch: compress-and-append
+the B*n_q new tokens (mla_append_kv), then decode (absorb q, split-KV
+attention over the paged latent cache, log-sum-exp combine, W_uv
+up-projection). It runs on the DeepSeek-V2-shaped workload: batch 16, 4096
+cached tokens per sequence, 1 query token, bf16 cache.
+
+L2 hygiene: the timed steps cycle through several layer-sized input sets
+(cache, page table, weights, queries, hidden states). Their total is more
+than 3x the L2 size, so no step finds its inputs in L2.
+
+Prints one JSON line. --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and latent-cache GB/s at 1 B300, % of roofline"
+DEFAULT_WORKLOAD = "dsv2_b16_l4096"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-heads", type=int, default=0,
+                    help="(b, h) pairs in the oracle sample (0: about 10 s worth)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value, dist, device="cpu"):
+    """Max of a float over all ranks (identity when not distributed)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, dist, device="cpu"):
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+
+def algorithmic(w, lens):
+    """Cache bytes and attention FLOPs of one decode call."""
+    rows = int(np.sum(lens))
+    cache_bytes = rows * w.R * w.elem_bytes
+    # per visible (row, query): 2*(R + d_c) FLOPs per head. Visible rows of query i
+    # are L - n_q + i + 1.
+    vis = sum(int(L) - w.n_q + i + 1 for L in lens for i in range(w.n_q))
+    attn_flops = 2.0 * w.n_h * (w.R + w.d_c) * vis
+    return cache_bytes, attn_flops
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def kernel_source_hash():
+    src = os.path.join(ROOT, "mla_latent_kv_73_b300", "csrc", "attend_tc.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "attend_tc_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t_start, t_end):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+    from mla_latent_kv_73_b300 import _lib, synth
+    from mla_latent_kv_73_b300.device_inputs import DeviceWeights, config_for, to_device
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    _lib.load()
+    w = synth.WORKLOADS[args.workload]
+    lens = synth.seq_lens(w)
+    B, n_q = w.batch, w.n_q
+    Tq = B * n_q
+    cfg = config_for(w)
+    impl = _lib.mla_decode_impl(cfg)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pt_np, num_blocks = synth.page_table(w, lens)
+    max_blocks = pt_np.shape[1]
+    cache_bytes, attn_flops = algorithmic(w, lens)
+
+    # input sets: one per simulated layer
+    wts = synth.weights(w)
+    set_bytes = cache_bytes + (w.R * w.d_model + 2 * w.n_h * w.d_c * w.d_nope) * w.elem_bytes
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    n_sets = max(2, math.ceil(3 * l2 / set_bytes))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1000 + rank)
+    sets = []
+    for k in range(n_sets):
+        s = {}
+        s["w"] = DeviceWeights(w, wts, cfg)
+        s["cache"] = torch.randn((num_blocks, w.block_size, w.R), generator=gen, device="cuda").to(dt)
+        s["pt"] = to_device(pt_np, "i32")
+        s["x"] = torch.randn((Tq, w.d_model), generator=gen, device="cuda").to(dt)
+        s["q"] = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen, device="cuda").to(dt)
+        sets.append(s)
+    seq_lens = to_device(lens, "i32")
+    seq_idx = to_device(np.repeat(np.arange(B), n_q).astype(np.int32), "i32")
+    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32), "i32")
+    out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
+    ws = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q, int(lens.sum())),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(s, ev_a=None, ev_b=None):
+        _lib.mla_append_kv(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], stream)
+        _lib.mla_decode_absorb_q(cfg, s["w"].handle, s["q"], seq_lens, max_blocks, ws, stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        _lib.mla_decode_attend(cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+        _lib.mla_decode_combine(cfg, s["w"].handle, seq_lens, B, n_q, out, ws, stream)
+
+    for i in range(args.warmup):
+        step(sets[i % n_sets])
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} after warm-up")
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record(stream)
+        for i in range(K):
+            step(sets[i % n_sets], ev_a[i], ev_b[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        wall1 = time.time()
+    clocks = clk.summary(wall0, wall1)
+    total_ms = t0.elapsed_time(t1)
+    attend_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(K)]
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+
+    total_ms_max = max_over_ranks(total_ms, dist, "cuda")
+    ms_per_step = total_ms_max / K
+    tokens = sum_over_ranks(Tq * K, dist, "cuda")
+    value = tokens / (total_ms_max / 1e3)
+
+    # end to end: host buffers in, host result out, through the same calls
+    pin_x = torch.empty((Tq, w.d_model), dtype=dt, pin_memory=True)
+    pin_q = torch.empty((B, n_q, w.n_h, w.d_nope + w.d_r), dtype=dt, pin_memory=True)
+    pin_lens = torch.from_numpy(lens.astype(np.int32)).pin_memory()
+    pin_out = torch.empty((B, n_q, w.n_h, w.d_v), pin_memory=True)
+    pin_x.copy_(sets[0]["x"].cpu())
+    pin_q.copy_(sets[0]["q"].cpu())
+    Ke = max(1, K // 4)
+    h2d = pin_x.numel() * pin_x.element_size() + pin_q.numel() * pin_q.element_size() + \
+        pin_lens.numel() * 4
+    d2h = pin_out.numel() * 4
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(Ke):
+        s = sets[i % n_sets]
+        s["x"].copy_(pin_x, non_blocking=True)
+        s["q"].copy_(pin_q, non_blocking=True)
+        seq_lens.copy_(pin_lens, non_blocking=True)
+        step(s)
+        pin_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+    e2e_value = sum_over_ranks(Tq * Ke, dist, "cuda") / (e2e_ms / 1e3)
+
+    # roofline of the dominant kernel (attention), per launch
+    hbm, tflops, tflops_sus, src = measured_peaks()
+    att_ms = statistics.mean(attend_ms)
+    achieved_gbs = cache_bytes / (att_ms / 1e3) / 1e9
+    tensor_tflops = attn_flops / (att_ms / 1e3) / 1e12
+    t_mem = cache_bytes / (hbm * 1e9)
+    t_ten = attn_flops / (tflops * 1e12)
+    bound = "hbm" if t_mem >= t_ten else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tensor_tflops, 1), "peak": tflops,
+                "unit": "TFLOP/s", "frac": round(tensor_tflops / tflops, 4)}
+    roof["traffic"] = profiled_traffic(args.workload)
+    roof["peak_source"] = src
+    roof["kernel"] = "attend_tc_kernel" if impl == 2 else "attend_simt_kernel"
+    roof["kernel_ms"] = round(att_ms, 5)
+    roof["roofline_ms"] = round(max(t_mem, t_ten) * 1e3, 5)
+    roof["frac_of_roofline_time"] = round(max(t_mem, t_ten) * 1e3 / att_ms, 4)
+    roof["tensor_tflops"] = round(tensor_tflops, 1)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) cache rows, hidden states and queries; "
+                "N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "batch": B, "seq_len": int(lens[0]) if w.len_lo == w.len_hi
+                   else [w.len_lo, w.len_hi], "n_q": n_q, "n_h": w.n_h, "d_model": w.d_model,
+                   "d_c": w.d_c, "d_r": w.d_r, "block_size": w.block_size,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"{n_sets} rotating layer-sized input sets, "
+                         f"{n_sets * set_bytes / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
+                   "decode_kernel": "tensor_core" if impl == 2 else "cuda_core"},
+        "cache_gbs": round(cache_bytes * K / (total_ms_max / 1e3) / 1e9, 1),
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, lens, args.cpu_sample_heads)
+    for s in sets:
+        s["w"].free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU) arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, lens, n_pairs):
+    """The (b, i, h) triples of a bounded oracle sample: whole sequences first."""
+    from mla_latent_kv_73_b300 import synth
+    trip = [(b, i, h) for b in range(w.batch) for i in range(w.n_q) for h in range(w.n_h)]
+    return trip[:n_pairs]
+
+
+def time_oracle(w, lens, n_pairs):
+    from mla_latent_kv_73_b300 import synth
+    from oracle import mla_oracle as O
+    wts = synth.weights(w)
+    qv, _ = synth.queries(w)
+    samples = oracle_sample(w, lens, n_pairs)
+    need = sorted({b for b, _, _ in samples})
+    rows = [None] * w.batch
+    for b in need:
+        rows[b] = synth.sequence_rows(w, b, lens[b])[0]
+    t0 = time.perf_counter()
+    O.decode_materialised(qv, rows, lens, wts.W_uk, wts.W_uv, w.d_c, w.d_nope, w.d_v, w.scale,
+                          w.rope_base, samples=samples)
+    dt = time.perf_counter() - t0
+    # a query token is done when all its heads are: tokens = (b,i,h) triples / n_h
+    return dt, len(samples) / w.n_h
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(w, lens, n_pairs):
+    if n_pairs <= 0:
+        # calibrate: time one head, then aim for about 10 s
+        dt1, _ = time_oracle(w, lens, 1)
+        n_pairs = int(min(w.batch * w.n_q * w.n_h, max(w.n_h, 10.0 / max(dt1, 1e-4))))
+    dt, toks = time_oracle(w, lens, n_pairs)
+    return {"value": round(toks / dt, 4), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{n_pairs} (sequence, query, head) triples of {w.name} "
+                      f"(= {toks:.3f} query tokens), fp64 NumPy, keys/values materialised"}
+
+
+def run_reference(args, world, rank):
+    from mla_latent_kv_73_b300 import synth
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    lens = synth.seq_lens(w)
+    dt1, _ = time_oracle(w, lens, 1)
+    # each step: a bounded sample sized so that warmup + steps stay within minutes
+    per_step_pairs = int(max(1, min(w.n_h, 8.0 / max(dt1, 1e-4))))
+    for _ in range(args.warmup):
+        time_oracle(w, lens, 1)
+    times, toks = [], 0.0
+    for _ in range(args.steps if args.steps <= 20 else 20):
+        dt, t = time_oracle(w, lens, per_step_pairs)
+        times.append(dt)
+        toks += t
+    total = sum(times)
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+        "n_gpus": world, "steps": len(times), "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "n_q": w.n_q, "n_h": w.n_h},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step_pairs} (sequence, query, head) triples per step"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * mla.h: C ABI of libmla, the decode hot path of Multi-head Latent Attention
+ * (MLA) over a paged latent KV cache, for NVIDIA B300 (sm_103a).
+ *
+ * What is computed. Each cached token keeps one row [c | k_rope] of
+ * d_c + d_r elements, shared by all heads. Here c = x W_dkv and
+ * k_rope = RoPE(x W_kr, pos). Sources: "Multi-head Latent Attention: the KV
+ * cache, compressed", sections "The one formula" and "RoPE, and why the
+ * explanations stop here"; "Multi-head Latent Attention and KV Cache
+ * Compression", section "Caching one latent vector".
+ *
+ * A decode step for head h and query token i of sequence b computes
+ *     q_lat  = W_uk[h] q_nope                      (absorbed query, d_c wide)
+ *     q_pe   = RoPE(q_rope, pos_i)
+ *     s_j    = (q_lat . c_j + q_pe . k_rope_j) * scale      for j <= pos_i
+ *     p      = softmax(s)
+ *     o_lat  = sum_j p_j c_j
+ *     out    = o_lat W_uv[h]                       (d_v wide)
+ * so no per-head key or value is ever materialised. Sources: "Multi-head
+ * Latent Attention and KV Cache Compression", section "The absorption trick
+ * and decoupled RoPE" (query- and value-side absorption); "Multi-head Latent
+ * Attention: the KV cache, compressed", sections "Absorption: the part that
+ * makes it free" and "RoPE, and why the explanations stop here" (the score
+ * has a content part and a decoupled RoPE part).
+ *
+ * Conventions. All of these are readings where the pages are silent.
+ *  - RoPE rotates the pair of dimensions (i, i + d_r/2) by the angle
+ *    pos * rope_base^(-2i/d_r).
+ *  - Positions are 0-based indices within a sequence. seq_lens[b] counts
+ *    every cached token, including the n_q new ones. Query i therefore sits
+ *    at pos_i = seq_lens[b] - n_q + i and attends to keys j <= pos_i.
+ *  - Paged cache: token j of sequence b lives in row
+ *    page_table[b * max_blocks + j / block_size] * block_size + j % block_size
+ *    of the cache, viewed as [num_blocks * block_size, d_c + d_r].
+ *  - The weights use the layouts below. Head h owns columns
+ *    [h*d, (h+1)*d) of W_uk and W_uv.
+ *
+ * Memory and streams. Every pointer argument is a DEVICE pointer to memory
+ * the caller owns and keeps alive until the work queued on `stream` has
+ * finished. The only exception is the out-parameters of the host-side query
+ * functions (mla_decode_workspace_size, mla_get_last_device_error), which
+ * are host pointers. All compute calls are asynchronous on `stream` and
+ * return once the work is queued. The library allocates device memory only
+ * inside mla_absorb_weights. It never allocates on the decode path.
+ *
+ * Errors. Each call checks its arguments on the host before queueing any
+ * work. A failed check returns a status other than MLA_OK and queues
+ * nothing. Problems that only the device can see (a page id out of range,
+ * a sequence shorter than n_q, a wait that timed out) set bits in a
+ * per-device error word. mla_get_last_device_error() reads and clears it.
+ * Nothing in the library traps or aborts.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, negative count, bad enum */
+  MLA_ERR_SHAPE = 2,         /* inconsistent or unsupported dimensions */
+  MLA_ERR_CAPACITY = 3,      /* page table / cache too small for the request */
+  MLA_ERR_UNSUPPORTED = 4,   /* valid request that this build or device cannot run */
+  MLA_ERR_WORKSPACE = 5,     /* workspace missing, misaligned or too small */
+  MLA_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+  MLA_ERR_DEVICE_CHECK = 7,  /* the device error word is non-zero */
+  MLA_ERR_TIMEOUT = 8        /* a bounded device-side wait gave up */
+} mla_status;
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Which decode kernel to run. MLA_IMPL_AUTO picks the tensor-core kernel
+ * when the shape and device allow it, and the CUDA-core kernel otherwise. */
+typedef enum {
+  MLA_IMPL_AUTO = 0,
+  MLA_IMPL_CUDA_CORE = 1,    /* fp32 FMA kernel, any supported shape */
+  MLA_IMPL_TENSOR_CORE = 2   /* tcgen05/TMEM kernel: bf16, d_c=512, d_r=64, block_size=64 */
+} mla_impl;
+
+/* Device error word bits (mla_get_last_device_error). */
+#define MLA_DEVERR_PAGE_RANGE   0x1u  /* a page-table entry outside [0, num_blocks) */
+#define MLA_DEVERR_SEQ_LEN      0x2u  /* seq_lens[b] < n_q or beyond the page table */
+#define MLA_DEVERR_APPEND_INDEX 0x4u  /* append: seq_idx or pos outside the page table */
+#define MLA_DEVERR_TIMEOUT      0x8u  /* a bounded mbarrier wait gave up */
+
+typedef struct {
+  int32_t n_h;            /* query heads */
+  int32_t d_model;        /* hidden width (input of W_dkv, W_kr) */
+  int32_t d_c;            /* latent width (cached) */
+  int32_t d_r;            /* decoupled RoPE width (cached, shared by heads); even */
+  int32_t d_nope;         /* per-head non-rotary query/key width */
+  int32_t d_v;            /* per-head value width */
+  int32_t block_size;     /* tokens per cache page */
+  float rope_base;        /* RoPE base, e.g. 10000 */
+  float softmax_scale;    /* 0 selects 1/sqrt(d_nope + d_r) */
+  mla_dtype dtype;        /* dtype of cache, weights, x and q; outputs are fp32 */
+  int32_t impl;           /* an mla_impl value */
+} mla_config;
+
+typedef struct mla_weights_s* mla_weights; /* opaque, library-owned */
+
+/* Fold the up-projections into the decode operands, once at load time.
+ * Source: "Multi-head Latent Attention: the KV cache, compressed", section
+ * "Store the archive, not the files" (build the fold once, at load);
+ * "Multi-head Latent Attention and KV Cache Compression", section "The
+ * absorption trick and decoupled RoPE" (W_uk goes to the query side and
+ * W_uv to the output side).
+ *   W_dkv [d_model, d_c], W_kr [d_model, d_r]       row-major, cfg->dtype
+ *   W_uk  [d_c, n_h*d_nope], W_uv [d_c, n_h*d_v]   row-major, cfg->dtype
+ * Allocates library-owned device buffers, queues the repacking kernels on
+ * `stream`, and returns the handle in *out. The caller's weight buffers may
+ * be freed once `stream` has passed this call. Release the handle with
+ * mla_weights_free. The handle is bound to the config it was built with and
+ * to the current device. */
+mla_status mla_absorb_weights(const mla_config* cfg, const void* W_dkv, const void* W_kr,
+                              const void* W_uk, const void* W_uv, cudaStream_t stream,
+                              mla_weights* out);
+
+/* Free a handle from mla_absorb_weights. Waits for the device to finish
+ * work that may still use it. NULL is accepted. */
+mla_status mla_weights_free(mla_weights w);
+
+/* Compress and append T new tokens to the paged latent cache.
+ * Source: "Multi-head Latent Attention: the KV cache, compressed", sections
+ * "The code" (latent) and "RoPE, and why the explanations stop here" (the
+ * decoupled key is rotated and cached, one copy for all heads); "DeepSeek V3
+ * Multi-Head Latent Attention (MLA): How It Slashes KV Cache Memory",
+ * section "Low-Rank Key-Value Joint Compression".
+ *   x          [T, d_model]               cfg->dtype
+ *   seq_idx    [T] int32                  sequence of each token, in [0, B)
+ *   pos        [T] int32                  position of each token in its sequence
+ *   page_table [B, max_blocks] int32
+ *   cache      [num_blocks, block_size, d_c + d_r] cfg->dtype, updated in place
+ * Row t is written to the cache row given by the paged-layout convention.
+ * Accumulation is fp32, and the result is rounded to nearest-even when
+ * stored. Tokens whose seq_idx, pos or page id fall outside the tables are
+ * skipped and set MLA_DEVERR_APPEND_INDEX or MLA_DEVERR_PAGE_RANGE. Two
+ * tokens that name the same row race. T = 0 is a no-op. */
+mla_status mla_append_kv(const mla_config* cfg, mla_weights w, const void* x,
+                         const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
+                         int32_t B, int32_t max_blocks, void* cache, int32_t num_blocks,
+                         int32_t T, cudaStream_t stream);
+
+/* Bytes of device workspace that mla_decode needs for B sequences with n_q
+ * query tokens each, on the current device. total_tokens (the sum of
+ * seq_lens, or an upper bound; 0 if unknown) is accepted for interface
+ * stability. The size does not depend on it. Writes the size to *bytes
+ * (a host pointer). */
+mla_status mla_decode_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                     int64_t total_tokens, size_t* bytes);
+
+/* Absorbed-query decode attention over the paged cache, with per-sequence
+ * lengths. Steps a2..a5 in one call: absorb q, split-KV latent attention,
+ * log-sum-exp combine, value up-projection.
+ *   q          [B, n_q, n_h, d_nope + d_r] cfg->dtype, RoPE not yet applied
+ *   cache      [num_blocks, block_size, d_c + d_r] cfg->dtype
+ *   page_table [B, max_blocks] int32
+ *   seq_lens   [B] int32, each in [n_q, max_blocks * block_size]
+ *   out        [B, n_q, n_h, d_v] fp32
+ *   workspace  device buffer of at least mla_decode_workspace_size() bytes,
+ *              256-byte aligned. Its contents on entry do not matter.
+ * Bad sequence lengths and page ids set the device error word. Their
+ * outputs are then zero (bad lengths) or unspecified (bad pages). */
+mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const void* cache,
+                      int32_t num_blocks, const int32_t* page_table, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t B, int32_t n_q, float* out,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* The three stages of mla_decode as separate calls, so that each kernel can
+ * be timed on its own. Called in this order with the same arguments and
+ * workspace, they produce exactly what mla_decode produces. Intermediate
+ * results live in the workspace, in a layout private to the library.
+ *   mla_decode_absorb_q   a2: q_lat = W_uk[h] q_nope, q_pe = RoPE(q_rope);
+ *                              also plans the split-KV partition.
+ *   mla_decode_attend     a3: split-KV attention over the latent cache.
+ *   mla_decode_combine    a4+a5: log-sum-exp combine of the splits, then
+ *                              out = o_lat W_uv[h]. */
+mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void* q,
+                               const int32_t* seq_lens, int32_t max_blocks, int32_t B,
+                               int32_t n_q, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream);
+mla_status mla_decode_attend(const mla_config* cfg, const void* cache, int32_t num_blocks,
+                             const int32_t* page_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t B, int32_t n_q, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream);
+mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_t* seq_lens,
+                              int32_t B, int32_t n_q, float* out, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream);
+
+/* Which decode kernel mla_decode would run for this config on the current
+ * device. Writes an mla_impl value other than MLA_IMPL_AUTO to *impl, a host
+ * pointer. */
+mla_status mla_decode_impl(const mla_config* cfg, int32_t* impl);
+
+/* Synchronise `stream`, then read and clear the current device's error word
+ * into *code (a host pointer). Returns MLA_ERR_DEVICE_CHECK if the word was
+ * non-zero. */
+mla_status mla_get_last_device_error(cudaStream_t stream, uint32_t* code);
+
+/* Static, human-readable name of a status code. */
+const char* mla_status_string(mla_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_H_ */

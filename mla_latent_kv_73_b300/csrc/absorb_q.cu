@@ -1,0 +1,136 @@
+// a2: fold each head's query into latent space, and plan the split-KV work.
+//
+//   qabs[t, h, 0:d_c]    = W_uk[h] q_nope[t, h]        (q_lat, d_c wide)
+//   qabs[t, h, d_c:d_c+d_r] = RoPE(q_rope[t, h], pos_t)
+//
+// Source: "Multi-head Latent Attention and KV Cache Compression", section
+// "The absorption trick and decoupled RoPE". The score q.k_j with
+// k_j = W_u c_j equals (W_u^T q).c_j, so the query is moved into latent
+// space once and dotted against cached latents directly. Only the position
+// block is rotated, per query position ("Multi-head Latent Attention: the
+// KV cache, compressed", section "RoPE, and why the explanations stop here").
+//
+// One CTA per (head, tile of 16 query tokens). It reads that head's
+// [d_c x d_nope] slice of W_uk once and reuses it for all 16 tokens.
+//
+// Block (0, 0) also writes the split-KV plan: the tiles of each sequence and
+// their prefix sum. The attention and combine kernels both read it.
+#include "device_common.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int AQ_TOK = 16, AQ_THREADS = 256;
+
+__device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks,
+                           int bs, int TS, int32_t* tiles, int32_t* prefix, uint32_t* err) {
+  __shared__ int32_t warp_sums[AQ_THREADS / 32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  for (int b0 = 0; b0 < B; b0 += AQ_THREADS) {
+    const int b = b0 + threadIdx.x;
+    int t = 0;
+    if (b < B) {
+      const long long L = seq_lens[b];
+      if (L < n_q || L > static_cast<long long>(max_blocks) * bs) {
+        set_error(err, MLA_DEVERR_SEQ_LEN);
+      } else {
+        t = static_cast<int>((L + TS - 1) / TS);
+      }
+      tiles[b] = t;
+    }
+    // inclusive warp scan
+    int v = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += warp_sums[w];
+    if (b < B) prefix[b] = before + v - t;
+    __syncthreads();
+    if (threadIdx.x == AQ_THREADS - 1) carry = before + v;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) prefix[B] = carry;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(AQ_THREADS)
+absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
+                const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
+                T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, uint32_t* err) {
+  extern __shared__ float qn[];  // [AQ_TOK][d_nope]
+  const int h = blockIdx.x;
+  const int tok0 = blockIdx.y * AQ_TOK;
+  const int Tq = B * n_q;
+  const int dq = s.d_nope + s.d_r, R = s.R();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    write_plan(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
+
+  const int ntok = min(AQ_TOK, Tq - tok0);
+  for (int i = threadIdx.x; i < AQ_TOK * s.d_nope; i += AQ_THREADS) {
+    const int t = i / s.d_nope, n = i % s.d_nope;
+    qn[i] = t < ntok ? to_f32<T>(q[(static_cast<size_t>(tok0 + t) * s.n_h + h) * dq + n]) : 0.f;
+  }
+  __syncthreads();
+
+  const T* W = w_uk + static_cast<size_t>(h) * s.d_c * s.d_nope;
+  for (int dc = threadIdx.x; dc < s.d_c; dc += AQ_THREADS) {
+    float acc[AQ_TOK];
+#pragma unroll
+    for (int t = 0; t < AQ_TOK; ++t) acc[t] = 0.f;
+    const T* wr = W + static_cast<size_t>(dc) * s.d_nope;
+    for (int n = 0; n < s.d_nope; ++n) {
+      const float wv = to_f32<T>(wr[n]);
+#pragma unroll
+      for (int t = 0; t < AQ_TOK; ++t) acc[t] = fmaf(wv, qn[t * s.d_nope + n], acc[t]);
+    }
+    for (int t = 0; t < ntok; ++t)
+      qabs[(static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc] = from_f32<T>(acc[t]);
+  }
+
+  // rotary block of the query, rotated at the query's own position
+  const int half = s.d_r / 2;
+  for (int i = threadIdx.x; i < ntok * half; i += AQ_THREADS) {
+    const int t = i / half, k = i % half;
+    const int tok = tok0 + t, b = tok / n_q, qi = tok % n_q;
+    const int pos = seq_lens[b] - n_q + qi;
+    const T* qr = q + (static_cast<size_t>(tok) * s.n_h + h) * dq + s.d_nope;
+    const float x1 = to_f32<T>(qr[k]), x2 = to_f32<T>(qr[k + half]);
+    float c, sn;
+    rope_cos_sin(pos, k, s.d_r, s.rope_base, &c, &sn);
+    T* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
+    o[k] = from_f32<T>(x1 * c - x2 * sn);
+    o[k + half] = from_f32<T>(x1 * sn + x2 * c);
+  }
+}
+
+template <typename T>
+cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const int32_t* seq_lens,
+                       int max_blocks, int B, int n_q, const Partition& p, const WsView& ws,
+                       uint32_t* err, cudaStream_t st) {
+  const int Tq = B * n_q;
+  dim3 grid(s.n_h, (Tq + AQ_TOK - 1) / AQ_TOK);
+  const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;
+  absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
+      s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), seq_lens, B, n_q, max_blocks,
+      p.TS, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
+                            const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                            const Partition& p, const WsView& ws, uint32_t* err, cudaStream_t st) {
+  if (dt == MLA_F32) return absorb_q_t<float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, err, st);
+  return absorb_q_t<__nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, err, st);
+}
+
+}  // namespace mla

@@ -1,0 +1,451 @@
+// C ABI of libmla: argument checks, workspace planning and kernel dispatch.
+// Every entry point checks its arguments before it queues anything. None of
+// them allocates device memory except mla_absorb_weights.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "mla_internal.h"
+
+// Per-device error word. Kernels OR MLA_DEVERR_* bits into it.
+__device__ uint32_t g_mla_device_error = 0;
+
+namespace mla {
+
+size_t attend_tc_smem_bytes();
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0, major = 0, minor = 0;
+  uint32_t* err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Queries (once per device) the SM count, compute capability and the device
+// address of the error word. Must run with the device current.
+const DeviceInfo* device_info() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[d];
+  if (!di.ready) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err), g_mla_device_error) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    di.ready = true;
+  }
+  return &di;
+}
+
+mla_status check_config(const mla_config* c) {
+  if (!c) return MLA_ERR_INVALID_ARG;
+  if (c->dtype != MLA_F32 && c->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (c->impl < MLA_IMPL_AUTO || c->impl > MLA_IMPL_TENSOR_CORE) return MLA_ERR_INVALID_ARG;
+  if (!(c->rope_base > 0.f) || !std::isfinite(c->rope_base)) return MLA_ERR_INVALID_ARG;
+  if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if (c->n_h < 1 || c->d_model < 1 || c->d_nope < 1 || c->d_v < 1 || c->block_size < 1)
+    return MLA_ERR_SHAPE;
+  if (c->d_c < 4 || c->d_c > 512 || c->d_c % 4 != 0) return MLA_ERR_SHAPE;
+  if (c->d_r < 2 || c->d_r % 2 != 0 || c->d_c + c->d_r > 1024) return MLA_ERR_SHAPE;
+  if (c->d_nope > 1024 || c->d_v > 4096) return MLA_ERR_SHAPE;
+  return MLA_OK;
+}
+
+Shape shape_of(const mla_config* c) {
+  Shape s;
+  s.n_h = c->n_h;
+  s.d_model = c->d_model;
+  s.d_c = c->d_c;
+  s.d_r = c->d_r;
+  s.d_nope = c->d_nope;
+  s.d_v = c->d_v;
+  s.bs = c->block_size;
+  s.rope_base = c->rope_base;
+  s.scale = c->softmax_scale > 0.f ? c->softmax_scale
+                                   : 1.0f / std::sqrt(static_cast<float>(c->d_nope + c->d_r));
+  return s;
+}
+
+int dtype_bytes(mla_dtype d) { return d == MLA_F32 ? 4 : 2; }
+
+bool tc_device(const DeviceInfo* di) { return di && di->major == 10 && di->minor == 3; }
+
+// Decode kernel for this config on this device, or -1 if the requested one cannot run.
+int resolve_impl(const mla_config* c, const DeviceInfo* di) {
+  const Shape s = shape_of(c);
+  const bool tc_ok = attend_tc_supported(s, c->dtype) && tc_device(di);
+  if (c->impl == MLA_IMPL_TENSOR_CORE) return tc_ok ? MLA_IMPL_TENSOR_CORE : -1;
+  if (c->impl == MLA_IMPL_CUDA_CORE) return MLA_IMPL_CUDA_CORE;
+  return tc_ok ? MLA_IMPL_TENSOR_CORE : MLA_IMPL_CUDA_CORE;
+}
+
+mla_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  cudaGetLastError();
+  return MLA_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+struct Plan {
+  Shape s;
+  int impl;
+  Partition part;
+  WsLayout lay;
+};
+
+mla_status make_plan(const mla_config* cfg, int B, int n_q, const DeviceInfo* di, int impl,
+                     Plan* out) {
+  out->s = shape_of(cfg);
+  out->impl = impl;
+  out->part = partition_for(impl, out->s, B, n_q, di->sms);
+  out->lay = ws_layout(out->s, dtype_bytes(cfg->dtype), B, n_q, out->part);
+  return MLA_OK;
+}
+
+mla_status check_decode_args(const mla_config* cfg, int B, int n_q) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (B < 1 || n_q < 1) return MLA_ERR_SHAPE;
+  const long long rows = static_cast<long long>(B) * n_q * cfg->n_h;
+  if (rows > (1LL << 30)) return MLA_ERR_SHAPE;
+  return MLA_OK;
+}
+
+}  // namespace
+
+Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms) {
+  Partition p;
+  const int rows = n_q * s.n_h;
+  if (impl == MLA_IMPL_TENSOR_CORE) {
+    p.RG = rows <= 64 ? ((rows + 15) / 16) * 16 : 64;
+    p.TS = 64;
+    p.C = num_sms;
+  } else {
+    p.RG = 16;
+    p.TS = 64;
+    p.C = num_sms * 3;
+  }
+  p.G = (rows + p.RG - 1) / p.RG;
+  p.slots = p.C + p.G * B;
+  return p;
+}
+
+WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p) {
+  WsLayout l;
+  size_t off = 0;
+  l.qabs = off;
+  off = align256(off + static_cast<size_t>(B) * n_q * s.n_h * s.R() * dtype_bytes);
+  l.tiles = off;
+  off = align256(off + sizeof(int32_t) * B);
+  l.prefix = off;
+  off = align256(off + sizeof(int32_t) * (B + 1));
+  l.part_o = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(p.slots) * p.RG * s.d_c);
+  l.part_lse = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(p.slots) * p.RG);
+  l.total = off;
+  return l;
+}
+
+WsView ws_view(void* base, const WsLayout& l) {
+  char* b = static_cast<char*>(base);
+  WsView v;
+  v.qabs = b + l.qabs;
+  v.tiles = reinterpret_cast<int32_t*>(b + l.tiles);
+  v.prefix = reinterpret_cast<int32_t*>(b + l.prefix);
+  v.part_o = reinterpret_cast<float*>(b + l.part_o);
+  v.part_lse = reinterpret_cast<float*>(b + l.part_lse);
+  return v;
+}
+
+}  // namespace mla
+
+struct mla_weights_s {
+  mla::Weights w;
+  mla_config cfg;
+};
+
+using namespace mla;
+
+namespace {
+
+bool same_shape(const mla_config* a, const mla_config* b) {
+  return a->n_h == b->n_h && a->d_model == b->d_model && a->d_c == b->d_c && a->d_r == b->d_r &&
+         a->d_nope == b->d_nope && a->d_v == b->d_v && a->dtype == b->dtype;
+}
+
+// Resolves the decode kernel and checks the workspace for one decode call.
+mla_status prepare_decode(const mla_config* cfg, int B, int n_q, const void* cache,
+                          const void* workspace, size_t ws_bytes, Plan* plan,
+                          const DeviceInfo** di_out) {
+  mla_status st = check_decode_args(cfg, B, n_q);
+  if (st != MLA_OK) return st;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  int impl = resolve_impl(cfg, di);
+  if (impl < 0) return MLA_ERR_UNSUPPORTED;
+  if (impl == MLA_IMPL_TENSOR_CORE && cache && !aligned16(cache)) {
+    if (cfg->impl == MLA_IMPL_TENSOR_CORE) return MLA_ERR_INVALID_ARG;
+    impl = MLA_IMPL_CUDA_CORE;
+  }
+  make_plan(cfg, B, n_q, di, impl, plan);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MLA_ERR_WORKSPACE;
+  if (ws_bytes < plan->lay.total) return MLA_ERR_WORKSPACE;
+  *di_out = di;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE";
+    case MLA_ERR_CAPACITY: return "MLA_ERR_CAPACITY";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_CHECK: return "MLA_ERR_DEVICE_CHECK";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+mla_status mla_absorb_weights(const mla_config* cfg, const void* W_dkv, const void* W_kr,
+                              const void* W_uk, const void* W_uv, cudaStream_t stream,
+                              mla_weights* out) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (!W_dkv || !W_kr || !W_uk || !W_uv) return MLA_ERR_INVALID_ARG;
+  const int dev = current_device();
+  if (dev < 0) return MLA_ERR_CUDA;
+  const Shape s = shape_of(cfg);
+  const size_t eb = dtype_bytes(cfg->dtype);
+  mla_weights_s* h = new (std::nothrow) mla_weights_s();
+  if (!h) return MLA_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->w.shape = s;
+  h->w.dtype = cfg->dtype;
+  h->w.device = dev;
+  const size_t n_dkvr = static_cast<size_t>(s.R()) * s.d_model * eb;
+  const size_t n_uk = static_cast<size_t>(s.n_h) * s.d_c * s.d_nope * eb;
+  const size_t n_uv = static_cast<size_t>(s.n_h) * s.d_c * s.d_v * eb;
+  if (cudaMalloc(&h->w.w_dkvr, n_dkvr) != cudaSuccess ||
+      cudaMalloc(&h->w.w_uk, n_uk) != cudaSuccess || cudaMalloc(&h->w.w_uv, n_uv) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->w.w_dkvr);
+    cudaFree(h->w.w_uk);
+    cudaFree(h->w.w_uv);
+    delete h;
+    return MLA_ERR_CUDA;
+  }
+  cudaError_t e = launch_pack_weights(s, cfg->dtype, W_dkv, W_kr, W_uk, W_uv, &h->w, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaStreamSynchronize(stream);
+    cudaFree(h->w.w_dkvr);
+    cudaFree(h->w.w_uk);
+    cudaFree(h->w.w_uv);
+    delete h;
+    return MLA_ERR_CUDA;
+  }
+  *out = h;
+  return MLA_OK;
+}
+
+mla_status mla_weights_free(mla_weights w) {
+  if (!w) return MLA_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(w->w.device);
+  cudaDeviceSynchronize();
+  cudaFree(w->w.w_dkvr);
+  cudaFree(w->w.w_uk);
+  cudaFree(w->w.w_uv);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete w;
+  return MLA_OK;
+}
+
+mla_status mla_append_kv(const mla_config* cfg, mla_weights w, const void* x,
+                         const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
+                         int32_t B, int32_t max_blocks, void* cache, int32_t num_blocks,
+                         int32_t T, cudaStream_t stream) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (!w) return MLA_ERR_INVALID_ARG;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (T < 0 || B < 1 || max_blocks < 1 || num_blocks < 1) return MLA_ERR_SHAPE;
+  if (T == 0) return MLA_OK;
+  if (!x || !seq_idx || !pos || !page_table || !cache) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  return from_cuda(launch_append(shape_of(cfg), cfg->dtype, &w->w, x, seq_idx, pos, page_table, B,
+                                 max_blocks, cache, num_blocks, T, di->err, stream));
+}
+
+mla_status mla_decode_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                     int64_t total_tokens, size_t* bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = 0;
+  mla_status st = check_decode_args(cfg, B, n_q);
+  if (st != MLA_OK) return st;
+  if (total_tokens < 0) return MLA_ERR_SHAPE;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  const int impl = resolve_impl(cfg, di);
+  if (impl < 0) return MLA_ERR_UNSUPPORTED;
+  Plan p;
+  make_plan(cfg, B, n_q, di, impl, &p);
+  size_t need = p.lay.total;
+  if (cfg->impl == MLA_IMPL_AUTO && impl == MLA_IMPL_TENSOR_CORE) {
+    // a misaligned cache falls back to the CUDA-core kernel: cover that too
+    Plan q;
+    make_plan(cfg, B, n_q, di, MLA_IMPL_CUDA_CORE, &q);
+    if (q.lay.total > need) need = q.lay.total;
+  }
+  *bytes = need;
+  return MLA_OK;
+}
+
+mla_status mla_decode_impl(const mla_config* cfg, int32_t* impl) {
+  if (!impl) return MLA_ERR_INVALID_ARG;
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  const int r = resolve_impl(cfg, di);
+  if (r < 0) return MLA_ERR_UNSUPPORTED;
+  *impl = r;
+  return MLA_OK;
+}
+
+mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void* q,
+                               const int32_t* seq_lens, int32_t max_blocks, int32_t B,
+                               int32_t n_q, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream) {
+  if (!w || !q || !seq_lens) return MLA_ERR_INVALID_ARG;
+  if (max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, nullptr, workspace, ws_bytes, &p, &di);
+  if (st != MLA_OK) return st;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  const WsView v = ws_view(workspace, p.lay);
+  return from_cuda(launch_absorb_q(p.s, cfg->dtype, &w->w, q, seq_lens, max_blocks, B, n_q,
+                                   p.part, v, di->err, stream));
+}
+
+mla_status mla_decode_attend(const mla_config* cfg, const void* cache, int32_t num_blocks,
+                             const int32_t* page_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t B, int32_t n_q, void* workspace,
+                             size_t ws_bytes, cudaStream_t stream) {
+  if (!cache || !page_table || !seq_lens) return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di);
+  if (st != MLA_OK) return st;
+  if (static_cast<long long>(num_blocks) * cfg->block_size > (1LL << 31) - 1) return MLA_ERR_SHAPE;
+  const WsView v = ws_view(workspace, p.lay);
+  cudaError_t e;
+  if (p.impl == MLA_IMPL_TENSOR_CORE)
+    e = launch_attend_tc(p.s, cache, num_blocks, page_table, max_blocks, B, n_q, p.part, v,
+                         seq_lens, di->err, stream);
+  else
+    e = launch_attend_simt(p.s, cfg->dtype, cache, num_blocks, page_table, max_blocks, B, n_q,
+                           p.part, v, seq_lens, di->err, stream);
+  return from_cuda(e);
+}
+
+mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_t* seq_lens,
+                              int32_t B, int32_t n_q, float* out, void* workspace,
+                              size_t ws_bytes, cudaStream_t stream) {
+  if (!w || !out || !seq_lens) return MLA_ERR_INVALID_ARG;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, nullptr, workspace, ws_bytes, &p, &di);
+  if (st != MLA_OK) return st;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  const WsView v = ws_view(workspace, p.lay);
+  return from_cuda(launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out,
+                                  stream));
+}
+
+mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const void* cache,
+                      int32_t num_blocks, const int32_t* page_table, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t B, int32_t n_q, float* out,
+                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!w || !q || !cache || !page_table || !seq_lens || !out) return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di);
+  if (st != MLA_OK) return st;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * cfg->block_size > (1LL << 31) - 1) return MLA_ERR_SHAPE;
+  // The three stages below see the same config, so they resolve the same
+  // kernel and partition as this call did.
+  mla_config c2 = *cfg;
+  c2.impl = p.impl;
+  st = mla_decode_absorb_q(&c2, w, q, seq_lens, max_blocks, B, n_q, workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode_attend(&c2, cache, num_blocks, page_table, max_blocks, seq_lens, B, n_q,
+                         workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  return mla_decode_combine(&c2, w, seq_lens, B, n_q, out, workspace, ws_bytes, stream);
+}
+
+mla_status mla_get_last_device_error(cudaStream_t stream, uint32_t* code) {
+  if (!code) return MLA_ERR_INVALID_ARG;
+  *code = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mla_device_error, sizeof(v)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (v) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_mla_device_error, &zero, sizeof(zero)) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  *code = v;
+  if (v & MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
+  return v ? MLA_ERR_DEVICE_CHECK : MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal declarations shared by the libmla translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Shape as the kernels see it.
+struct Shape {
+  int n_h, d_model, d_c, d_r, d_nope, d_v, bs;
+  float rope_base, scale;
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  int R() const { return d_c + d_r; }
+};
+
+// Split-KV partition of one decode call.
+//
+// The query rows of a sequence, r = i*n_h + h for query token i and head h,
+// are cut into G groups of RG rows. The cached tokens of sequence b form
+// tiles_b = ceil(L_b / TS) tiles. The attention grid of C CTAs splits the
+// flat list of work items (g, b, tile), ordered group-major, into C
+// contiguous ranges of near-equal length. One CTA's range therefore covers
+// pieces of several (g, b) pairs. The piece of CTA c on pair (g, b) writes
+// its partial result to slot c + g*B + b. The slots are unique, and
+// slots = C + G*B bound their number.
+struct Partition {
+  int RG, G, TS, C, slots;
+};
+
+// Pointers into the decode workspace.
+struct WsView {
+  void* qabs;         // [B*n_q*n_h, R] in the cache dtype: [q_lat | RoPE(q_rope)]
+  int32_t* tiles;     // [B]    tiles per sequence (0 for an invalid length)
+  int32_t* prefix;    // [B+1]  exclusive prefix sum of tiles
+  float* part_o;      // [slots, RG, d_c] normalised partial latent outputs
+  float* part_lse;    // [slots, RG]      natural-log sum-exp of each partial
+};
+
+struct WsLayout {
+  size_t qabs, tiles, prefix, part_o, part_lse, total;
+};
+
+WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p);
+WsView ws_view(void* base, const WsLayout& l);
+
+// Library-owned packed weights.
+struct Weights {
+  Shape shape;
+  mla_dtype dtype;
+  int device;
+  void* w_dkvr;   // [R][d_model]: column j of [W_dkv | W_kr] stored contiguously.
+                  // The d_r rotary columns are interleaved so that rotary
+                  // dims i and i + d_r/2 sit in adjacent packed columns.
+  void* w_uk;     // [n_h][d_c][d_nope]
+  void* w_uv;     // [n_h][d_c][d_v]
+};
+
+// ---------------------------------------------------------------- launchers
+// Each returns the cudaError_t of its launch.
+cudaError_t launch_pack_weights(const Shape& s, mla_dtype dt, const void* W_dkv, const void* W_kr,
+                                const void* W_uk, const void* W_uv, Weights* w, cudaStream_t st);
+
+cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const void* x,
+                          const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
+                          int B, int max_blocks, void* cache, int num_blocks, int T,
+                          uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
+                            const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                            const Partition& p, const WsView& ws, uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_attend_simt(const Shape& s, mla_dtype dt, const void* cache, int num_blocks,
+                               const int32_t* page_table, int max_blocks, int B, int n_q,
+                               const Partition& p, const WsView& ws, const int32_t* seq_lens,
+                               uint32_t* err, cudaStream_t st);
+
+// Tensor-core attention (bf16, d_c = 512, d_r = 64, block_size = 64).
+bool attend_tc_supported(const Shape& s, mla_dtype dt);
+cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
+                             const int32_t* page_table, int max_blocks, int B, int n_q,
+                             const Partition& p, const WsView& ws, const int32_t* seq_lens,
+                             uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
+                           const int32_t* seq_lens, int B, int n_q, const Partition& p,
+                           const WsView& ws, float* out, cudaStream_t st);
+
+// Partition parameters for each attention kernel.
+Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms);
+
+}  // namespace mla

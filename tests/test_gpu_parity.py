@@ -1,0 +1,322 @@
+"""GPU parity: libmla (through its C ABI) against the fp64 oracle.
+
+Tolerances:
+  * fp32 workloads: max-abs <= 1e-4.
+  * bf16 workloads: rel-L2 <= 5e-3 and max-abs <= 2e-2.
+  * Cache placement and page tables: bit-exact.
+
+Every input comes from the seeded generator. No expected value comes from
+the CUDA path.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+
+from mla_latent_kv_73_b300 import _lib, synth
+from mla_latent_kv_73_b300.device_inputs import (DeviceWeights, config_for, to_device,
+                                                to_host_f32)
+from oracle import mla_oracle as O
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+IMPLS = {"cuda_core": _lib.MLA_IMPL_CUDA_CORE, "tensor_core": _lib.MLA_IMPL_TENSOR_CORE}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0, f"device error word left set: {code:#x}"
+
+
+def check_bf16(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    mab = np.max(np.abs(got - ref))
+    assert rel <= 5e-3 and mab <= 2e-2, f"{what}: rel-L2 {rel:.3e} max-abs {mab:.3e}"
+    return rel, mab
+
+
+def check_f32(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    mab = np.max(np.abs(got - np.asarray(ref, dtype=np.float64)))
+    assert np.isfinite(mab) and mab <= 1e-4, f"{what}: max-abs {mab:.3e}"
+    return mab
+
+
+def check(dtype, got, ref, what=""):
+    return check_f32(got, ref, what) if dtype == "f32" else check_bf16(got, ref, what)
+
+
+def small_workload(n_h=128, d_model=64, lens=(1, 64, 65, 200), n_q=1, dtype="bf16", seed=11,
+                   d_c=512, d_r=64, d_nope=128, d_v=128):
+    w = synth.Workload(f"small_{n_h}_{n_q}_{seed}", n_h=n_h, d_model=d_model, d_c=d_c, d_r=d_r,
+                       d_nope=d_nope, d_v=d_v, batch=len(lens), n_q=n_q, len_lo=0, len_hi=0,
+                       dtype=dtype, seed=seed)
+    return w, np.asarray(lens, dtype=np.int32)
+
+
+class Run:
+    """One decode problem on the device: inputs, weights, workspace, output."""
+
+    def __init__(self, w, lens, impl, fill=float("nan"), spare_blocks=3):
+        self.w, self.lens = w, lens
+        self.cfg = config_for(w, impl)
+        self.wts = synth.weights(w)
+        self.dw = DeviceWeights(w, self.wts, self.cfg)
+        pt, nb = synth.page_table(w, lens, spare_blocks=spare_blocks)
+        self.pt_np, self.num_blocks = pt, nb
+        store, self.rows = synth.fill_paged_cache(w, lens, pt, nb, fill_value=fill)
+        self.cache = to_device(store, w.dtype)
+        self.pt = to_device(pt, "i32")
+        self.sl = to_device(lens.astype(np.int32), "i32")
+        qv, qs = synth.queries(w)
+        self.q_vals = qv
+        self.q = to_device(qs, w.dtype)
+        self.out = torch.full((w.batch, w.n_q, w.n_h, w.d_v), float("nan"), device="cuda")
+        nbytes = _lib.mla_decode_workspace_size(self.cfg, w.batch, w.n_q, int(lens.sum()))
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def decode(self):
+        _lib.mla_decode(self.cfg, self.dw.handle, self.q, self.cache, self.pt, self.sl, self.out,
+                        self.ws)
+        torch.cuda.synchronize()
+        return self.out.cpu().numpy()
+
+    def oracle(self, samples=None):
+        w = self.w
+        return O.decode_materialised(self.q_vals, self.rows, self.lens, self.wts.W_uk,
+                                     self.wts.W_uv, w.d_c, w.d_nope, w.d_v, w.scale,
+                                     w.rope_base, samples=samples)
+
+
+# ---------------------------------------------------------------------------
+# a1: compress and append
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("wname,T", [("tiny_fp32", 5), ("tiny_fp32", 77),
+                                     ("dsv2_b16_l4096", 16), ("dsv2_b16_l4096", 70),
+                                     ("nh16_b256_ragged", 3)])
+def test_append_places_rows_exactly(wname, T):
+    w = synth.WORKLOADS[wname]
+    B = 3
+    lens = np.array([130, 64, 200], dtype=np.int32)
+    pt, nb = synth.page_table(w, lens, spare_blocks=2)
+    g = np.random.default_rng(5)
+    # distinct (seq, pos) targets inside each sequence's pages
+    pairs = set()
+    while len(pairs) < T:
+        b = int(g.integers(0, B))
+        pairs.add((b, int(g.integers(0, lens[b]))))
+    pairs = sorted(pairs, key=lambda _: g.random())
+    seq_idx = np.array([p[0] for p in pairs], dtype=np.int32)
+    pos = np.array([p[1] for p in pairs], dtype=np.int32)
+    xv, xs = synth.hidden_states(w, T)
+    wts = synth.weights(w)
+    cfg = config_for(w)
+    dw = DeviceWeights(w, wts, cfg)
+    canary = 7.0
+    cache = torch.full((nb, w.block_size, w.R), canary, device="cuda",
+                       dtype=torch.float32 if w.dtype == "f32" else torch.bfloat16)
+    _lib.mla_append_kv(cfg, dw.handle, to_device(xs, w.dtype), to_device(seq_idx, "i32"),
+                       to_device(pos, "i32"), to_device(pt, "i32"), cache)
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0
+    got = to_host_f32(cache).reshape(-1, w.R)
+    rows = O.latent_rows(xv, wts.W_dkv, wts.W_kr, pos, w.rope_base)
+    written = np.zeros(got.shape[0], dtype=bool)
+    for t in range(T):
+        r = O.paged_row_index(pt, seq_idx[t], pos[t], w.block_size)
+        written[r] = True
+        check(w.dtype, got[r], rows[t], f"row {t}")
+    # every other row is bit-identical to the canary
+    assert np.all(got[~written] == canary)
+    dw.free()
+
+
+def test_append_bad_indices_are_flagged_and_skipped():
+    w = synth.WORKLOADS["tiny_fp32"]
+    lens = np.array([64, 64], dtype=np.int32)
+    pt, nb = synth.page_table(w, lens)
+    pt[1, 0] = nb + 5  # page id out of range
+    wts = synth.weights(w)
+    cfg = config_for(w)
+    dw = DeviceWeights(w, wts, cfg)
+    xv, xs = synth.hidden_states(w, 3)
+    cache = torch.zeros((nb, w.block_size, w.R), device="cuda")
+    seq_idx = np.array([0, 5, 1], dtype=np.int32)   # 5: no such sequence
+    pos = np.array([3, 0, 2], dtype=np.int32)       # token 2 hits the bad page
+    _lib.mla_append_kv(cfg, dw.handle, to_device(xs, "f32"), to_device(seq_idx, "i32"),
+                       to_device(pos, "i32"), to_device(pt, "i32"), cache)
+    st, code = _lib.mla_get_last_device_error()
+    assert code == (_lib.MLA_DEVERR_APPEND_INDEX | _lib.MLA_DEVERR_PAGE_RANGE)
+    assert st == 7  # MLA_ERR_DEVICE_CHECK
+    got = cache.cpu().numpy().reshape(-1, w.R)
+    r0 = O.paged_row_index(pt, 0, 3, w.block_size)
+    assert np.count_nonzero(np.any(got != 0, axis=1)) == 1 and np.any(got[r0] != 0)
+    dw.free()
+
+
+# ---------------------------------------------------------------------------
+# a2..a5: decode
+# ---------------------------------------------------------------------------
+
+
+def test_tiny_fp32_end_to_end():
+    """The fp32 workload: rows come from mla_append_kv, queries from the
+    generator; compare with the oracle's own rows and decode."""
+    w = synth.WORKLOADS["tiny_fp32"]
+    lens = synth.seq_lens(w)
+    cfg = config_for(w)
+    assert _lib.mla_decode_impl(cfg) == _lib.MLA_IMPL_CUDA_CORE
+    wts = synth.weights(w)
+    dw = DeviceWeights(w, wts, cfg)
+    pt, nb = synth.page_table(w, lens)
+    T = int(lens.sum())
+    xv, xs = synth.hidden_states(w, T)
+    seq_idx = np.repeat(np.arange(w.batch), lens).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    cache = torch.zeros((nb, w.block_size, w.R), device="cuda")
+    _lib.mla_append_kv(cfg, dw.handle, to_device(xs, "f32"), to_device(seq_idx, "i32"),
+                       to_device(pos, "i32"), to_device(pt, "i32"), cache)
+    qv, qs = synth.queries(w)
+    out = torch.zeros((w.batch, w.n_q, w.n_h, w.d_v), device="cuda")
+    ws = torch.empty(_lib.mla_decode_workspace_size(cfg, w.batch, w.n_q), dtype=torch.uint8,
+                     device="cuda")
+    _lib.mla_decode(cfg, dw.handle, to_device(qs, "f32"), cache, to_device(pt, "i32"),
+                    to_device(lens, "i32"), out, ws)
+    torch.cuda.synchronize()
+    rows_all = O.latent_rows(xv, wts.W_dkv, wts.W_kr, pos, w.rope_base)
+    seq_rows = [rows_all[seq_idx == b] for b in range(w.batch)]
+    ref = O.decode_materialised(qv, seq_rows, lens, wts.W_uk, wts.W_uv, w.d_c, w.d_nope, w.d_v,
+                                w.scale, w.rope_base)
+    check_f32(out.cpu().numpy(), ref, "tiny fp32 end to end")
+    # the tensor-core kernel does not take fp32
+    cfg_tc = config_for(w, _lib.MLA_IMPL_TENSOR_CORE)
+    with pytest.raises(_lib.MlaError) as ei:
+        _lib.mla_decode(cfg_tc, dw.handle, to_device(qs, "f32"), cache, to_device(pt, "i32"),
+                        to_device(lens, "i32"), out, ws)
+    assert ei.value.status == 4  # MLA_ERR_UNSUPPORTED
+    dw.free()
+
+
+SMALL_CASES = {
+    "ragged_nq1": dict(lens=(1, 64, 65, 200, 300)),
+    "causal_nq2": dict(lens=(2, 65, 129, 640), n_q=2),
+    "nh16": dict(n_h=16, lens=(1, 17, 64, 100, 129, 250, 333, 400, 3)),
+    "one_long_seq": dict(lens=(64 * 37 + 5,)),
+    "nh8_nq3": dict(n_h=8, n_q=3, lens=(3, 70, 191)),
+}
+
+
+@pytest.mark.parametrize("impl", list(IMPLS))
+@pytest.mark.parametrize("case", list(SMALL_CASES))
+def test_decode_small_bf16(impl, case):
+    w, lens = small_workload(**SMALL_CASES[case])
+    r = Run(w, lens, IMPLS[impl])
+    got = r.decode()
+    ref = r.oracle()
+    check_bf16(got, ref, f"{case}/{impl}")
+    r.dw.free()
+
+
+def test_decode_small_fp32_shapes():
+    w, lens = small_workload(n_h=4, d_model=32, d_c=32, d_r=8, d_nope=16, d_v=16,
+                             lens=(2, 5, 64, 65, 130), n_q=2, dtype="f32")
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO)
+    check_f32(r.decode(), r.oracle(), "small fp32")
+    r.dw.free()
+
+
+def test_kernels_agree_and_steps_equal_fused():
+    w, lens = small_workload(lens=(5, 128, 129, 700), n_q=2, seed=3)
+    a = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
+    out_tc = a.decode()
+    out_tc2 = a.decode()
+    assert np.array_equal(out_tc, out_tc2), "decode is not deterministic"
+    # the three stage calls reproduce the fused call bit for bit
+    out2 = torch.full_like(a.out, float("nan"))
+    _lib.mla_decode_absorb_q(a.cfg, a.dw.handle, a.q, a.sl, a.pt.shape[1], a.ws)
+    _lib.mla_decode_attend(a.cfg, a.cache, a.pt, a.sl, w.batch, w.n_q, a.ws)
+    _lib.mla_decode_combine(a.cfg, a.dw.handle, a.sl, w.batch, w.n_q, out2, a.ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(out2.cpu().numpy(), out_tc)
+    b = Run(w, lens, _lib.MLA_IMPL_CUDA_CORE)
+    check_bf16(b.decode(), out_tc, "cuda-core vs tensor-core")
+    a.dw.free()
+    b.dw.free()
+
+
+def test_bad_lengths_and_pages_are_flagged():
+    w, lens = small_workload(lens=(0, 70, 100))  # seq 0 shorter than n_q
+    r = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
+    got = r.decode()
+    st, code = _lib.mla_get_last_device_error()
+    assert code == _lib.MLA_DEVERR_SEQ_LEN
+    assert np.all(got[0] == 0.0)
+    ref = r.oracle(samples=[(b, 0, h) for b in (1, 2) for h in range(w.n_h)])
+    check_bf16(np.array([got[b, 0, h] for (b, _, h) in ref]), np.array(list(ref.values())))
+    # a page id outside the cache
+    pt = r.pt_np.copy()
+    pt[2, 0] = r.num_blocks + 1
+    r.pt = to_device(pt, "i32")
+    r.decode()
+    st, code = _lib.mla_get_last_device_error()
+    assert code & _lib.MLA_DEVERR_PAGE_RANGE
+    r.dw.free()
+
+
+def test_host_argument_checks():
+    w, lens = small_workload(lens=(10, 20))
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO)
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.MlaError) as ei:
+        _lib.mla_decode(r.cfg, r.dw.handle, r.q, r.cache, r.pt, r.sl, r.out, small)
+    assert ei.value.status == 5  # MLA_ERR_WORKSPACE
+    mis = r.ws[1:]
+    with pytest.raises(_lib.MlaError) as ei:
+        _lib.mla_decode(r.cfg, r.dw.handle, r.q, r.cache, r.pt, r.sl, r.out, mis)
+    assert ei.value.status == 5
+    bad = config_for(w)
+    bad.d_r = 3
+    with pytest.raises(_lib.MlaError) as ei:
+        _lib.mla_decode(bad, r.dw.handle, r.q, r.cache, r.pt, r.sl, r.out, r.ws)
+    assert ei.value.status == 2  # MLA_ERR_SHAPE
+    r.dw.free()
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled outputs against the oracle
+# ---------------------------------------------------------------------------
+
+
+def _samples(w, lens, g):
+    bs = {int(np.argmin(lens)), int(np.argmax(lens))} | {int(x) for x in g.integers(0, w.batch, 2)}
+    hs = {0, w.n_h - 1, int(g.integers(0, w.n_h))}
+    return [(b, i, h) for b in sorted(bs) for i in sorted({0, w.n_q - 1}) for h in sorted(hs)][:16]
+
+
+@pytest.mark.parametrize("wname", ["dsv2_b16_l4096", "dsv2_b64_ragged", "dsv2_b4_l131072_nq2",
+                                   "nh16_b256_ragged"])
+def test_full_size_sampled(wname):
+    w = synth.WORKLOADS[wname]
+    lens = synth.seq_lens(w)
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO, fill=0.0, spare_blocks=0)
+    assert _lib.mla_decode_impl(r.cfg) == _lib.MLA_IMPL_TENSOR_CORE
+    got = r.decode()
+    assert np.all(np.isfinite(got))
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0
+    samples = _samples(w, lens, np.random.default_rng(w.seed))
+    ref = r.oracle(samples=samples)
+    check_bf16(np.array([got[s] for s in samples]), np.array([ref[s] for s in samples]), wname)
+    r.dw.free()
