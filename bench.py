@@ -236,80 +236,114 @@ def run_ours(args, world, rank, local):
     out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
     ws = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q, int(lens.sum())),
                      dtype=torch.uint8, device="cuda")
+    def step(s, st):
+        _lib.mla_append_kv(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], st)
+        _lib.mla_decode_absorb_q(cfg, s["w"].handle, s["q"], seq_lens, max_blocks, ws, st)
+        _lib.mla_decode_attend(cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, st)
+        _lib.mla_decode_combine(cfg, s["w"].handle, seq_lens, B, n_q, out, ws, st)
+
     stream = torch.cuda.current_stream()
-
-    def step(s, ev_a=None, ev_b=None):
-        _lib.mla_append_kv(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], stream)
-        _lib.mla_decode_absorb_q(cfg, s["w"].handle, s["q"], seq_lens, max_blocks, ws, stream)
-        if ev_a is not None:
-            ev_a.record(stream)
-        _lib.mla_decode_attend(cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, stream)
-        if ev_b is not None:
-            ev_b.record(stream)
-        _lib.mla_decode_combine(cfg, s["w"].handle, seq_lens, B, n_q, out, ws, stream)
-
     for i in range(args.warmup):
-        step(sets[i % n_sets])
+        step(sets[i % n_sets], stream)
     torch.cuda.synchronize()
     st, code = _lib.mla_get_last_device_error(stream)
     if code:
         raise RuntimeError(f"device error word {code:#x} after warm-up")
 
-    K = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(dist)
-        torch.cuda.synchronize()
-        wall0 = time.time()
-        t0.record(stream)
-        for i in range(K):
-            step(sets[i % n_sets], ev_a[i], ev_b[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-        wall1 = time.time()
-    clocks = clk.summary(wall0, wall1)
-    total_ms = t0.elapsed_time(t1)
-    attend_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(K)]
-    st, code = _lib.mla_get_last_device_error(stream)
-    if code:
-        raise RuntimeError(f"device error word {code:#x} in the timed region")
-
-    total_ms_max = max_over_ranks(total_ms, dist, "cuda")
-    ms_per_step = total_ms_max / K
-    tokens = sum_over_ranks(Tq * K, dist, "cuda")
-    value = tokens / (total_ms_max / 1e3)
-
-    # end to end: host buffers in, host result out, through the same calls
+    # pinned host buffers for the end-to-end measurement
     pin_x = torch.empty((Tq, w.d_model), dtype=dt, pin_memory=True)
     pin_q = torch.empty((B, n_q, w.n_h, w.d_nope + w.d_r), dtype=dt, pin_memory=True)
     pin_lens = torch.from_numpy(lens.astype(np.int32)).pin_memory()
     pin_out = torch.empty((B, n_q, w.n_h, w.d_v), pin_memory=True)
     pin_x.copy_(sets[0]["x"].cpu())
     pin_q.copy_(sets[0]["q"].cpu())
-    Ke = max(1, K // 4)
-    h2d = pin_x.numel() * pin_x.element_size() + pin_q.numel() * pin_q.element_size() + \
-        pin_lens.numel() * 4
-    d2h = pin_out.numel() * 4
+
+    def e2e_step(s, st):
+        s["x"].copy_(pin_x, non_blocking=True)
+        s["q"].copy_(pin_q, non_blocking=True)
+        seq_lens.copy_(pin_lens, non_blocking=True)
+        step(s, st)
+        pin_out.copy_(out, non_blocking=True)
+
+    # One CUDA graph per input set: a whole step; the attention kernel alone;
+    # a whole step with its host<->device copies.
+    g_step, g_att, g_e2e = [], [], []
+    for s in sets:
+        for lst, fn in ((g_step, lambda st, s=s: step(s, st)),
+                        (g_att, lambda st, s=s: _lib.mla_decode_attend(
+                            cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, st)),
+                        (g_e2e, lambda st, s=s: e2e_step(s, st))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(torch.cuda.current_stream())
+            lst.append(g)
+    for i in range(3 * n_sets):
+        g_step[i % n_sets].replay()
+        g_att[i % n_sets].replay()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        t0.record()
+        h0 = time.perf_counter()
+        for i in range(K):
+            g_step[i % n_sets].replay()
+        host_us = (time.perf_counter() - h0) * 1e6 / K
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(dist)
+        wall1 = time.time()
+    clocks = clk.summary(wall0, wall1)
+    total_ms = t0.elapsed_time(t1)
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+    total_ms_max = max_over_ranks(total_ms, dist, "cuda")
+    ms_per_step = total_ms_max / K
+    tokens = sum_over_ranks(Tq * K, dist, "cuda")
+    value = tokens / (total_ms_max / 1e3)
+
+    # the attention kernel, launch by launch (each launch on a cold input set)
+    Ka = min(K, 2000)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(Ka)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(Ka)]
+    torch.cuda.synchronize()
+    for i in range(Ka):
+        ev_a[i].record()
+        g_att[i % n_sets].replay()
+        ev_b[i].record()
+    torch.cuda.synchronize()
+    attend_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(Ka)]
+
+    # end to end: pinned host inputs in, host result out, every step
+    Ke = max(n_sets, K // 2)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
-    e0.record(stream)
+    e0.record()
     for i in range(Ke):
-        s = sets[i % n_sets]
-        s["x"].copy_(pin_x, non_blocking=True)
-        s["q"].copy_(pin_q, non_blocking=True)
-        seq_lens.copy_(pin_lens, non_blocking=True)
-        step(s)
-        pin_out.copy_(out, non_blocking=True)
-    e1.record(stream)
+        g_e2e[i % n_sets].replay()
+    e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     e2e_value = sum_over_ranks(Tq * Ke, dist, "cuda") / (e2e_ms / 1e3)
+    h2d = pin_x.numel() * pin_x.element_size() + pin_q.numel() * pin_q.element_size() + \
+        pin_lens.numel() * 4
+    d2h = pin_out.numel() * 4
+    # the same, issuing every call from Python each step (no graph)
+    Kd = min(Ke, 500)
+    e0.record()
+    for i in range(Kd):
+        e2e_step(sets[i % n_sets], stream)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_direct = Tq * Kd / (e0.elapsed_time(e1) / 1e3)
 
     # roofline of the dominant kernel (attention), per launch
     hbm, tflops, tflops_sus, src = measured_peaks()
@@ -357,8 +391,10 @@ def run_ours(args, world, rank, local):
         "cache_gbs": round(cache_bytes * K / (total_ms_max / 1e3) / 1e9, 1),
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
+                "d2h_bytes_per_step": d2h, "steps": Ke, "graph": True,
+                "no_graph_value": round(e2e_direct, 1)},
         "gpu_launches": 4 * K,
+        "host_enqueue_us_per_step": round(host_us, 2),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -180,7 +180,11 @@ mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const
  *                              also plans the split-KV partition.
  *   mla_decode_attend     a3: split-KV attention over the latent cache.
  *   mla_decode_combine    a4+a5: log-sum-exp combine of the splits, then
- *                              out = o_lat W_uv[h]. */
+ *                              out = o_lat W_uv[h].
+ * The tensor-core kernel reads the cache with TMA, which needs a 16-byte
+ * aligned cache pointer. For a misaligned cache under MLA_IMPL_AUTO,
+ * mla_decode falls back to the CUDA-core kernel. The stage calls have to
+ * agree on one partition, so they return MLA_ERR_INVALID_ARG instead. */
 mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void* q,
                                const int32_t* seq_lens, int32_t max_blocks, int32_t B,
                                int32_t n_q, void* workspace, size_t ws_bytes,

@@ -10,8 +10,9 @@
 // block is rotated, per query position ("Multi-head Latent Attention: the
 // KV cache, compressed", section "RoPE, and why the explanations stop here").
 //
-// One CTA per (head, tile of 16 query tokens). It reads that head's
-// [d_c x d_nope] slice of W_uk once and reuses it for all 16 tokens.
+// One CTA per (head, tile of 16 query tokens). It streams that head's
+// [d_c x d_nope] slice of W_uk once with 16-byte loads. Each thread owns two
+// latent rows and all 16 tokens, so every weight element is read once.
 //
 // Block (0, 0) also writes the split-KV plan: the tiles of each sequence and
 // their prefix sum. The attention and combine kernels both read it.
@@ -63,9 +64,10 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
 template <typename T>
 __global__ void __launch_bounds__(AQ_THREADS)
 absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
-                const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
-                T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, uint32_t* err) {
-  extern __shared__ float qn[];  // [AQ_TOK][d_nope]
+                const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
+                int n_q, int max_blocks, int TS, T* __restrict__ qabs, int32_t* tiles,
+                int32_t* prefix, uint32_t* err) {
+  extern __shared__ __align__(16) float qn[];  // [d_nope][AQ_TOK], token fastest
   const int h = blockIdx.x;
   const int tok0 = blockIdx.y * AQ_TOK;
   const int Tq = B * n_q;
@@ -76,23 +78,61 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
   const int ntok = min(AQ_TOK, Tq - tok0);
   for (int i = threadIdx.x; i < AQ_TOK * s.d_nope; i += AQ_THREADS) {
     const int t = i / s.d_nope, n = i % s.d_nope;
-    qn[i] = t < ntok ? to_f32<T>(q[(static_cast<size_t>(tok0 + t) * s.n_h + h) * dq + n]) : 0.f;
+    qn[n * AQ_TOK + t] =
+        t < ntok ? to_f32<T>(q[(static_cast<size_t>(tok0 + t) * s.n_h + h) * dq + n]) : 0.f;
   }
   __syncthreads();
 
+  // Two latent rows per thread; the 16 token values of each n are one
+  // broadcast shared-memory read of 4 float4.
+  constexpr int V = Vec<T>::N;
   const T* W = w_uk + static_cast<size_t>(h) * s.d_c * s.d_nope;
-  for (int dc = threadIdx.x; dc < s.d_c; dc += AQ_THREADS) {
-    float acc[AQ_TOK];
+  const bool vec_ok = s.d_nope % V == 0;
+  for (int dc0 = 2 * threadIdx.x; dc0 < s.d_c; dc0 += 2 * AQ_THREADS) {
+    const bool two = dc0 + 1 < s.d_c;
+    float acc0[AQ_TOK], acc1[AQ_TOK];
 #pragma unroll
-    for (int t = 0; t < AQ_TOK; ++t) acc[t] = 0.f;
-    const T* wr = W + static_cast<size_t>(dc) * s.d_nope;
-    for (int n = 0; n < s.d_nope; ++n) {
-      const float wv = to_f32<T>(wr[n]);
+    for (int t = 0; t < AQ_TOK; ++t) acc0[t] = acc1[t] = 0.f;
+    const T* r0 = W + static_cast<size_t>(dc0) * s.d_nope;
+    const T* r1 = two ? r0 + s.d_nope : r0;
+    if (vec_ok) {
+#pragma unroll 2
+      for (int n0 = 0; n0 < s.d_nope; n0 += V) {
+        float w0[V], w1[V];
+        load_vec<T>(r0 + n0, w0);
+        load_vec<T>(r1 + n0, w1);
 #pragma unroll
-      for (int t = 0; t < AQ_TOK; ++t) acc[t] = fmaf(wv, qn[t * s.d_nope + n], acc[t]);
+        for (int j = 0; j < V; ++j) {
+          const float4* qv = reinterpret_cast<const float4*>(qn + (n0 + j) * AQ_TOK);
+#pragma unroll
+          for (int u = 0; u < AQ_TOK / 4; ++u) {
+            const float4 x = qv[u];
+            acc0[4 * u + 0] = fmaf(w0[j], x.x, acc0[4 * u + 0]);
+            acc0[4 * u + 1] = fmaf(w0[j], x.y, acc0[4 * u + 1]);
+            acc0[4 * u + 2] = fmaf(w0[j], x.z, acc0[4 * u + 2]);
+            acc0[4 * u + 3] = fmaf(w0[j], x.w, acc0[4 * u + 3]);
+            acc1[4 * u + 0] = fmaf(w1[j], x.x, acc1[4 * u + 0]);
+            acc1[4 * u + 1] = fmaf(w1[j], x.y, acc1[4 * u + 1]);
+            acc1[4 * u + 2] = fmaf(w1[j], x.z, acc1[4 * u + 2]);
+            acc1[4 * u + 3] = fmaf(w1[j], x.w, acc1[4 * u + 3]);
+          }
+        }
+      }
+    } else {
+      for (int n = 0; n < s.d_nope; ++n) {
+        const float w0 = to_f32<T>(r0[n]), w1 = to_f32<T>(r1[n]);
+#pragma unroll
+        for (int t = 0; t < AQ_TOK; ++t) {
+          acc0[t] = fmaf(w0, qn[n * AQ_TOK + t], acc0[t]);
+          acc1[t] = fmaf(w1, qn[n * AQ_TOK + t], acc1[t]);
+        }
+      }
     }
-    for (int t = 0; t < ntok; ++t)
-      qabs[(static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc] = from_f32<T>(acc[t]);
+    for (int t = 0; t < ntok; ++t) {
+      T* o = qabs + (static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc0;
+      o[0] = from_f32<T>(acc0[t]);
+      if (two) o[1] = from_f32<T>(acc1[t]);
+    }
   }
 
   // rotary block of the query, rotated at the query's own position
@@ -104,7 +144,7 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
     const T* qr = q + (static_cast<size_t>(tok) * s.n_h + h) * dq + s.d_nope;
     const float x1 = to_f32<T>(qr[k]), x2 = to_f32<T>(qr[k + half]);
     float c, sn;
-    rope_cos_sin(pos, k, s.d_r, s.rope_base, &c, &sn);
+    rope_cos_sin(pos, inv_freq[k], &c, &sn);
     T* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
     o[k] = from_f32<T>(x1 * c - x2 * sn);
     o[k + half] = from_f32<T>(x1 * sn + x2 * c);
@@ -119,8 +159,8 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
   dim3 grid(s.n_h, (Tq + AQ_TOK - 1) / AQ_TOK);
   const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;
   absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
-      s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), seq_lens, B, n_q, max_blocks,
-      p.TS, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
+      s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
+      max_blocks, p.TS, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
   return cudaGetLastError();
 }
 

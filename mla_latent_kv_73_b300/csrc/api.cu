@@ -197,9 +197,12 @@ bool same_shape(const mla_config* a, const mla_config* b) {
 }
 
 // Resolves the decode kernel and checks the workspace for one decode call.
+// Only the fused mla_decode may move from the tensor-core kernel to the
+// CUDA-core one for a misaligned cache: the stage calls must agree on one
+// partition, so they reject such a cache instead.
 mla_status prepare_decode(const mla_config* cfg, int B, int n_q, const void* cache,
                           const void* workspace, size_t ws_bytes, Plan* plan,
-                          const DeviceInfo** di_out) {
+                          const DeviceInfo** di_out, bool allow_fallback = false) {
   mla_status st = check_decode_args(cfg, B, n_q);
   if (st != MLA_OK) return st;
   const DeviceInfo* di = device_info();
@@ -207,7 +210,7 @@ mla_status prepare_decode(const mla_config* cfg, int B, int n_q, const void* cac
   int impl = resolve_impl(cfg, di);
   if (impl < 0) return MLA_ERR_UNSUPPORTED;
   if (impl == MLA_IMPL_TENSOR_CORE && cache && !aligned16(cache)) {
-    if (cfg->impl == MLA_IMPL_TENSOR_CORE) return MLA_ERR_INVALID_ARG;
+    if (!allow_fallback || cfg->impl == MLA_IMPL_TENSOR_CORE) return MLA_ERR_INVALID_ARG;
     impl = MLA_IMPL_CUDA_CORE;
   }
   make_plan(cfg, B, n_q, di, impl, plan);
@@ -257,23 +260,34 @@ mla_status mla_absorb_weights(const mla_config* cfg, const void* W_dkv, const vo
   const size_t n_dkvr = static_cast<size_t>(s.R()) * s.d_model * eb;
   const size_t n_uk = static_cast<size_t>(s.n_h) * s.d_c * s.d_nope * eb;
   const size_t n_uv = static_cast<size_t>(s.n_h) * s.d_c * s.d_v * eb;
-  if (cudaMalloc(&h->w.w_dkvr, n_dkvr) != cudaSuccess ||
-      cudaMalloc(&h->w.w_uk, n_uk) != cudaSuccess || cudaMalloc(&h->w.w_uv, n_uv) != cudaSuccess) {
-    cudaGetLastError();
+  const int half = s.d_r / 2;
+  auto release = [h]() {
     cudaFree(h->w.w_dkvr);
     cudaFree(h->w.w_uk);
     cudaFree(h->w.w_uv);
+    cudaFree(h->w.inv_freq);
     delete h;
+  };
+  if (cudaMalloc(&h->w.w_dkvr, n_dkvr) != cudaSuccess ||
+      cudaMalloc(&h->w.w_uk, n_uk) != cudaSuccess || cudaMalloc(&h->w.w_uv, n_uv) != cudaSuccess ||
+      cudaMalloc(&h->w.inv_freq, sizeof(double) * half) != cudaSuccess) {
+    cudaGetLastError();
+    release();
     return MLA_ERR_CUDA;
   }
-  cudaError_t e = launch_pack_weights(s, cfg->dtype, W_dkv, W_kr, W_uk, W_uv, &h->w, stream);
+  // RoPE inverse frequencies base^(-2i/d_r), in fp64 on the host.
+  double inv[512];
+  for (int i = 0; i < half; ++i)
+    inv[i] = std::pow(static_cast<double>(cfg->rope_base), -2.0 * i / s.d_r);
+  cudaError_t e = cudaMemcpyAsync(h->w.inv_freq, inv, sizeof(double) * half,
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess)
+    e = launch_pack_weights(s, cfg->dtype, W_dkv, W_kr, W_uk, W_uv, &h->w, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     cudaStreamSynchronize(stream);
-    cudaFree(h->w.w_dkvr);
-    cudaFree(h->w.w_uk);
-    cudaFree(h->w.w_uv);
-    delete h;
+    release();
     return MLA_ERR_CUDA;
   }
   *out = h;
@@ -289,6 +303,7 @@ mla_status mla_weights_free(mla_weights w) {
   cudaFree(w->w.w_dkvr);
   cudaFree(w->w.w_uk);
   cudaFree(w->w.w_uv);
+  cudaFree(w->w.inv_freq);
   if (prev >= 0) cudaSetDevice(prev);
   delete w;
   return MLA_OK;
@@ -410,7 +425,7 @@ mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const
   if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
   Plan p;
   const DeviceInfo* di = nullptr;
-  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di);
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di, true);
   if (st != MLA_OK) return st;
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;

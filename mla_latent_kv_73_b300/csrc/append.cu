@@ -23,6 +23,7 @@ namespace mla {
 namespace {
 
 struct AppendArgs {
+  const double* inv_freq;
   const int32_t* seq_idx;
   const int32_t* pos;
   const int32_t* page_table;
@@ -48,46 +49,18 @@ __device__ __forceinline__ long long append_row(const AppendArgs& a, const Shape
 // Value of packed column pc after RoPE, given the pre-rotation values of the
 // pair it belongs to (v_even: rotary dim i, v_odd: rotary dim i + d_r/2).
 // Returns the cache column it lands in.
-__device__ __forceinline__ int finish_column(const Shape& s, int pc, float v_self, float v_even,
-                                             float v_odd, int pos, float* out) {
+__device__ __forceinline__ int finish_column(const Shape& s, const double* inv_freq, int pc,
+                                             float v_self, float v_even, float v_odd, int pos,
+                                             float* out) {
   if (pc < s.d_c) {
     *out = v_self;
     return pc;
   }
   const int j = pc - s.d_c, i = j >> 1, e = j & 1, half = s.d_r / 2;
   float c, sn;
-  rope_cos_sin(pos, i, s.d_r, s.rope_base, &c, &sn);
+  rope_cos_sin(pos, inv_freq[i], &c, &sn);
   *out = e == 0 ? v_even * c - v_odd * sn : v_even * sn + v_odd * c;
   return s.d_c + i + e * half;
-}
-
-template <typename T>
-struct Vec;
-template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-};
-template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-};
-
-template <typename T>
-__device__ __forceinline__ void load_vec(const T* p, float (&v)[Vec<T>::N]) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(p);
-  if constexpr (sizeof(T) == 4) {
-    v[0] = __uint_as_float(raw.x);
-    v[1] = __uint_as_float(raw.y);
-    v[2] = __uint_as_float(raw.z);
-    v[3] = __uint_as_float(raw.w);
-  } else {
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
 }
 
 constexpr int GEMV_COLS = 4, GEMV_TOK = 8, GEMV_THREADS = 256;
@@ -156,8 +129,9 @@ append_gemv_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
         if (row >= 0) {
           const int ce = c & ~1;  // even member of the pair inside this CTA
           float out;
-          const int dst = finish_column(s, pc, res[c * GEMV_TOK + t], res[ce * GEMV_TOK + t],
-                                        res[(ce + 1) * GEMV_TOK + t], a.pos[tok], &out);
+          const int dst = finish_column(s, a.inv_freq, pc, res[c * GEMV_TOK + t],
+                                        res[ce * GEMV_TOK + t], res[(ce + 1) * GEMV_TOK + t],
+                                        a.pos[tok], &out);
           cache[row * R + dst] = from_f32<T>(out);
         }
       }
@@ -229,7 +203,7 @@ append_gemm_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
       const int je = j & ~1;
       float out;
       const int dst =
-          finish_column(s, pc, acc[i][j], acc[i][je], acc[i][je + 1], a.pos[tok], &out);
+          finish_column(s, a.inv_freq, pc, acc[i][j], acc[i][je], acc[i][je + 1], a.pos[tok], &out);
       cache[row * R + dst] = from_f32<T>(out);
     }
   }
@@ -258,7 +232,7 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st) {
-  AppendArgs a{seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err};
+  AppendArgs a{w->inv_freq, seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err};
   if (dt == MLA_F32) return append_t<float>(s, w, x, a, cache, st);
   return append_t<__nv_bfloat16>(s, w, x, a, cache, st);
 }

@@ -25,12 +25,15 @@
 // tile in shared memory, as an MN-major operand, so the tile is loaded once
 // and feeds both products.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer: Q rows once per piece, then 9 boxes of 64 x 64
 //               bf16 per 64-token page, 2-stage ring
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..5  softmax (query row r lives in TMEM lane 32*(r/16) + r%16),
-//               lazy rescale of O^T, and the epilogue of each piece
+//   warps 2..9  softmax, lazy rescale of O^T and the epilogue of each piece.
+//               Query row r lives in TMEM lane 32*(r/16) + r%16. Each lane
+//               quarter is read by two warps, one per 32-column half of the
+//               score tile. The halves meet once per tile, in shared memory,
+//               to agree on the row maximum.
 //
 // Lazy rescale: a row's running max is only raised when the new max exceeds
 // it by more than 8 (log2 units). Otherwise P is computed against the stale
@@ -58,7 +61,8 @@ constexpr int TC_ROWS = 64;                 // query rows per group (score MMA M
 constexpr int TC_TOK = 64;                  // tokens per tile = page size
 constexpr int TC_KCH = 9;                   // 576 / 64 column chunks
 constexpr int TC_STAGES = 2;
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 320;              // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int TC_SM_THREADS = 256;
 constexpr uint32_t CHUNK_BYTES = 64 * 128;  // 64 rows x 128 B (one 128B-swizzled box)
 constexpr uint32_t TILE_BYTES = TC_KCH * CHUNK_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
@@ -81,6 +85,8 @@ struct __align__(1024) TcSmem {
   int abort_flag;
   float row_alpha[TC_ROWS];
   float row_inv_l[TC_ROWS];
+  float xmax[2][TC_ROWS];  // partial row maxima of the two column halves
+  float xsum[TC_ROWS];     // row sum of the second column half
 };
 
 struct TcArgs {
@@ -116,6 +122,13 @@ __device__ __forceinline__ Piece locate_piece(long long it, long long end, long 
   const long long stop = min(end, static_cast<long long>(pc.g) * T_all + prefix[lo] + tiles[lo]);
   pc.n_tiles = static_cast<int>(stop - it);
   return pc;
+}
+
+// 2^x with the hardware ex2 unit (max relative error about 2^-22); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void note_timeout(TcSmem& sm, uint32_t* err) {
@@ -158,7 +171,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_init(&sm.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], 4);
+      mbar_init(&sm.s_empty[i], TC_SM_THREADS / 32);
     }
     mbar_init(&sm.p_full, 1);
     mbar_init(&sm.p_empty, 1);
@@ -226,6 +239,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(TC_ROWS, TC_TOK, false, false);
       const uint32_t idPV = idesc_bf16_f32(128, a.RG, true, false);
+      // Descriptor bases. Offsets inside the buffers are added to the
+      // start-address field (bits 0-13, in 16-byte units); shared addresses
+      // stay below 2^18 bytes, so the field never overflows.
+      const uint64_t dQ = desc_kmajor(sm.q[0], 0);
+      const uint64_t dP = desc_kmajor(sm.p, 0);
+      uint64_t dK[TC_STAGES], dC[TC_STAGES];
+      for (int s2 = 0; s2 < TC_STAGES; ++s2) {
+        dK[s2] = desc_kmajor(sm.kv[s2][0], 0);
+        dC[s2] = desc_ct(sm.kv[s2][0], 0);
+      }
       uint32_t kv_it = 0;
       int piece_idx = 0;
       bool pend = false, pend_first = false, pend_last = false;
@@ -238,17 +261,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         if (first && ppiece > 0 && !mbar_wait(&sm.o_empty, (ppiece - 1) & 1, WAIT_LIMIT))
           return false;
         tc_fence_after();
-        const int s = pit % TC_STAGES;
+        const int s2 = pit % TC_STAGES;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = desc_ct(sm.kv[s][2 * j], kk * 2048);
-            const uint64_t bd = desc_kmajor(sm.p, kk * 32);
+            const uint64_t ad = dC[s2] + ((2 * j * CHUNK_BYTES + kk * 2048) >> 4);
+            const uint64_t bd = dP + ((kk * 32) >> 4);
             mma_bf16_ss(tmem + TM_O + 64 * j, ad, bd, idPV, (first && kk == 0) ? 0u : 1u);
           }
         }
-        mma_commit(&sm.kv_empty[s]);
+        mma_commit(&sm.kv_empty[s2]);
         mma_commit(&sm.p_empty);
         if (last) mma_commit(&sm.o_full);
         return true;
@@ -264,18 +287,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             ok = false;
             break;
           }
-          const int s = kv_it % TC_STAGES;
-          if (!mbar_wait(&sm.kv_full[s], (kv_it / TC_STAGES) & 1, WAIT_LIMIT)) {
+          const int s2 = kv_it % TC_STAGES;
+          if (!mbar_wait(&sm.kv_full[s2], (kv_it / TC_STAGES) & 1, WAIT_LIMIT)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4 * TC_KCH; ++k) {
-            const int c = k >> 2;
-            const uint32_t off = (k & 3) * 32;
-            mma_bf16_ss(tmem + TM_S + 64 * sb, desc_kmajor(sm.q[c], off),
-                        desc_kmajor(sm.kv[s][c], off), idS, k > 0 ? 1u : 0u);
+            const uint32_t off = ((k >> 2) * CHUNK_BYTES + (k & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + TM_S + 64 * sb, dQ + off, dK[s2] + off, idS, k > 0 ? 1u : 0u);
           }
           mma_commit(&sm.s_full[sb]);
           if (i == pc.n_tiles - 1) mma_commit(&sm.q_empty);
@@ -300,96 +321,120 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       mbar_wait(&sm.drain, 0, WAIT_LIMIT);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 2..5
-    const int qd = warp & 3;                 // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ softmax warps 2..9
+    // A failed (timed-out) wait only sets `bad`. Every thread still passes
+    // every named barrier, and the group leaves the loop together at the
+    // end-of-tile barrier, so no barrier can be left half-filled.
+    const int qd = warp & 3;                   // TMEM lane quarter this warp may access
+    const int hf = (warp - 2) >> 2;            // score column half: [32*hf, 32*hf + 32)
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-    const int row = 16 * qd + lane;          // score row held by this lane (lane < 16)
+    const int row = 16 * qd + lane;            // score row held by this lane (lane < 16)
     const bool lane_has_row = lane < 16;
-    const int tid_sm = threadIdx.x - 64;     // 0..127
+    const int tid_sm = threadIdx.x - 64;       // 0..255
     uint32_t kv_it = 0;
     int piece_idx = 0;
-    bool ok = true;
-    for (long long it = it_begin; it < it_end && ok;) {
+    bool abort = false;
+    for (long long it = it_begin; it < it_end && !abort;) {
       const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
       const int L = a.seq_lens[pc.b];
       const int rg = pc.g * a.RG + row;
       const int rows_valid = min(a.RG, rows_total - pc.g * a.RG);
       const bool row_ok = lane_has_row && row < rows_valid;
       const int pos_q = L - a.n_q + (row_ok ? rg / a.n_h : 0);
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // m: running max (shared by both halves); l: this half
 
-      for (int i = 0; i < pc.n_tiles; ++i) {
+      for (int i = 0; i < pc.n_tiles && !abort; ++i) {
+        bool bad = false;
         const int t = pc.t_first + i;
         const int sb = kv_it & 1;
-        const int s = kv_it % TC_STAGES;
-        bool w_ok = mbar_wait(&sm.s_full[sb], (kv_it >> 1) & 1, WAIT_LIMIT);
-        if (named_bar_or(1, 128, !w_ok)) { ok = false; break; }
+        const int s2 = kv_it % TC_STAGES;
+        bad |= !mbar_wait(&sm.s_full[sb], (kv_it >> 1) & 1, WAIT_LIMIT);
         tc_fence_after();
-        float sc[TC_TOK];
-#pragma unroll
-        for (int c0 = 0; c0 < TC_TOK; c0 += 16) {
+        float sc[32];
+        {
           float v[16];
-          tmem_ld16(tmem + lane_base + TM_S + 64 * sb + c0, v);
+          tmem_ld16(tmem + lane_base + TM_S + 64 * sb + 32 * hf, v);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) sc[c0 + k] = v[k];
+          for (int k = 0; k < 16; ++k) sc[k] = v[k];
+          tmem_ld16(tmem + lane_base + TM_S + 64 * sb + 32 * hf + 16, v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) sc[16 + k] = v[k];
         }
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
 
-        const int j0 = t * TC_TOK;
-        float mx = -INFINITY;
+        const int j0 = t * TC_TOK + 32 * hf;  // token of sc[0]
+        if (row_ok && j0 + 31 <= L - a.n_q) {
 #pragma unroll
-        for (int c = 0; c < TC_TOK; ++c) {
-          const bool valid = row_ok && (j0 + c <= pos_q);
-          sc[c] = valid ? sc[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sc[c]);
+          for (int c = 0; c < 32; ++c) sc[c] *= a.scale_log2;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] * a.scale_log2 : -INFINITY;
         }
-        const float m_new = fmaxf(m, mx);
+        float pm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          pm[u] = fmaxf(fmaxf(sc[4 * u], sc[4 * u + 1]), fmaxf(sc[4 * u + 2], sc[4 * u + 3]));
+        const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
         const bool first = (i == 0);
-        const bool need = !first && (m_new > m + RESCALE_THRESHOLD);
+        if (lane_has_row) sm.xmax[hf][row] = pmax;
+        // One barrier: publishes both halves' maxima and tells everyone
+        // whether any row must rescale (or any wait failed).
+        const bool flag = bad || (!first && row_ok && pmax > m + RESCALE_THRESHOLD);
+        const bool any = named_bar_or(1, TC_SM_THREADS, flag);
+        const float m_new =
+            lane_has_row ? fmaxf(m, fmaxf(sm.xmax[0][row], sm.xmax[1][row])) : -INFINITY;
+        const bool need = !first && row_ok && (m_new > m + RESCALE_THRESHOLD);
         const float m_use = (first || need) ? m_new : m;
-        const float alpha = (m == -INFINITY || first) ? 0.f : exp2f(m - m_use);
+        const float alpha = (m == -INFINITY || first) ? 0.f : fast_exp2(m - m_use);
+        // A row with nothing visible yet keeps m_use = -inf; subtracting 0
+        // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
+        const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
 
         // P buffer free and O^T stable once the previous value MMA has finished.
-        w_ok = (kv_it == 0) || mbar_wait(&sm.p_empty, (kv_it - 1) & 1, WAIT_LIMIT);
-        if (named_bar_or(1, 128, !w_ok)) { ok = false; break; }
+        if (kv_it > 0) bad |= !mbar_wait(&sm.p_empty, (kv_it - 1) & 1, WAIT_LIMIT);
         tc_fence_after();
-        const bool any = named_bar_or(1, 128, need && row_ok);
         if (any) {
-          if (lane_has_row) sm.row_alpha[row] = need && row_ok ? alpha : 1.f;
-          named_bar_sync(1, 128);
-          for (int j = 0; j < 4; ++j) {
-            for (int c0 = 0; c0 < a.RG; c0 += 16) {
-              float v[16];
-              const uint32_t ta = tmem + lane_base + TM_O + 64 * j + c0;
-              tmem_ld16(ta, v);
-              tmem_wait_ld();
+          if (named_bar_or(1, TC_SM_THREADS, bad)) {
+            abort = true;
+          } else {
+            if (hf == 0 && lane_has_row) sm.row_alpha[row] = need ? alpha : 1.f;
+            named_bar_sync(1, TC_SM_THREADS);
+            for (int j = 2 * hf; j < 2 * hf + 2; ++j) {
+              for (int c0 = 0; c0 < a.RG; c0 += 16) {
+                float v[16];
+                const uint32_t ta = tmem + lane_base + TM_O + 64 * j + c0;
+                tmem_ld16(ta, v);
+                tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 16; ++k) v[k] *= sm.row_alpha[c0 + k];
-              tmem_st16(ta, v);
+                for (int k = 0; k < 16; ++k) v[k] *= sm.row_alpha[c0 + k];
+                tmem_st16(ta, v);
+              }
             }
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
-        // P row -> shared memory (bf16, 128B-swizzled K-major), row sums
-        if (lane_has_row) {
+        // P half-row -> shared memory (bf16, 128B-swizzled K-major)
+        if (lane_has_row && !abort) {
           float psum = 0.f;
           uint8_t* prow = sm.p + row * 128;
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
+          for (int ch = 0; ch < 4; ++ch) {
             uint32_t w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const float x0 = sc[ch * 8 + 2 * k], x1 = sc[ch * 8 + 2 * k + 1];
-              const float p0 = (x0 == -INFINITY) ? 0.f : exp2f(x0 - m_use);
-              const float p1 = (x1 == -INFINITY) ? 0.f : exp2f(x1 - m_use);
+              const float p0 = fast_exp2(x0 - m_sub), p1 = fast_exp2(x1 - m_sub);
               const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
               psum += __low2float(pb) + __high2float(pb);
               w[k] = *reinterpret_cast<const uint32_t*>(&pb);
             }
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) * 16)) =
+            const int unit = 4 * hf + ch;
+            *reinterpret_cast<uint4*>(prow + ((unit ^ (row & 7)) * 16)) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
           if (row_ok) {
@@ -399,36 +444,42 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         // Rows past the end of the sequence may hold anything; zero their
         // latent columns so that 0 * garbage cannot reach the accumulator.
-        if (j0 + TC_TOK > L) {
-          const int r0 = L - j0;  // first invalid row in this tile
+        const int jt = t * TC_TOK;
+        if (!abort && jt + TC_TOK > L) {
+          const int r0 = L - jt;  // first invalid row in this tile
           const int nrow = TC_TOK - r0;
-          for (int i2 = tid_sm; i2 < nrow * 8 * 8; i2 += 128) {
+          for (int i2 = tid_sm; i2 < nrow * 8 * 8; i2 += TC_SM_THREADS) {
             const int rr = r0 + i2 / 64, ch = (i2 / 8) % 8, u = i2 % 8;
-            *reinterpret_cast<uint4*>(sm.kv[s][ch] + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sm.kv[s2][ch] + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        named_bar_sync(1, 128);
-        if (tid_sm == 0) mbar_arrive(&sm.p_full);
+        if (named_bar_or(1, TC_SM_THREADS, bad)) abort = true;
+        if (tid_sm == 0 && !abort) mbar_arrive(&sm.p_full);
         ++kv_it;
       }
-      if (!ok) break;
+      if (abort) break;
 
       // ---- epilogue of the piece: O^T / l -> workspace slot
-      const bool w_ok = mbar_wait(&sm.o_full, piece_idx & 1, WAIT_LIMIT);
-      if (named_bar_or(1, 128, !w_ok)) { ok = false; break; }
+      bool bad = !mbar_wait(&sm.o_full, piece_idx & 1, WAIT_LIMIT);
       tc_fence_after();
+      if (hf == 1 && lane_has_row) sm.xsum[row] = l;
+      if (named_bar_or(1, TC_SM_THREADS, bad)) {
+        abort = true;
+        break;
+      }
       const int slot = blockIdx.x + pc.g * a.B + pc.b;
-      if (lane_has_row) {
-        sm.row_inv_l[row] = (row_ok && l > 0.f) ? 1.f / l : 0.f;
+      if (hf == 0 && lane_has_row) {
+        const float lt = l + sm.xsum[row];
+        sm.row_inv_l[row] = (row_ok && lt > 0.f) ? 1.f / lt : 0.f;
         if (row_ok)
           a.part_lse[static_cast<size_t>(slot) * a.RG + row] =
-              l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+              lt > 0.f ? (m + log2f(lt)) * 0.6931471805599453f : -INFINITY;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, TC_SM_THREADS);
       float* dst = a.part_o + static_cast<size_t>(slot) * a.RG * 512;
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 2 * hf; j < 2 * hf + 2; ++j) {
         for (int c0 = 0; c0 < a.RG; c0 += 16) {
           float v[16];
           tmem_ld16(tmem + lane_base + TM_O + 64 * j + c0, v);
@@ -442,14 +493,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
       }
       tc_fence_before();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, TC_SM_THREADS);
       if (tid_sm == 0) mbar_arrive(&sm.o_empty);
       ++piece_idx;
       it += pc.n_tiles;
     }
-    if (!ok && tid_sm == 0) note_timeout(sm, a.err);
+    if (abort && tid_sm == 0) note_timeout(sm, a.err);
   }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -473,7 +523,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
+bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {576, rows};
@@ -483,6 +533,36 @@ bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps depend only on (base address, rows), so recent ones are kept.
+struct MapCache {
+  static constexpr int kSlots = 32;
+  struct Entry {
+    const void* base = nullptr;
+    uint64_t rows = 0;
+    CUtensorMap map;
+  } e[kSlots];
+  int next = 0;
+  std::mutex mu;
+};
+
+bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  static MapCache cache;
+  std::lock_guard<std::mutex> lk(cache.mu);
+  for (auto& x : cache.e) {
+    if (x.base == base && x.rows == rows) {
+      *m = x.map;
+      return true;
+    }
+  }
+  if (!encode_rows_map(m, base, rows)) return false;
+  auto& slot = cache.e[cache.next];
+  cache.next = (cache.next + 1) % MapCache::kSlots;
+  slot.base = base;
+  slot.rows = rows;
+  slot.map = *m;
+  return true;
 }
 
 }  // namespace
@@ -520,10 +600,16 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   a.C = p.C;
   a.scale_log2 = s.scale * 1.4426950408889634f;
   const size_t smem = attend_tc_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
   attend_tc_kernel<<<p.C, TC_THREADS, smem, st>>>(tq, tkv, a);
   return cudaGetLastError();
 }

@@ -11,8 +11,9 @@
 // and decoupled RoPE" (the value up-projection is absorbed on the output
 // side the same way W_uk is on the query side).
 //
-// One CTA per (head, tile of 16 query tokens). It reads that head's
-// [d_c x d_v] slice of W_uv once and reuses it for all 16 tokens.
+// One CTA per (head, tile of 16 query tokens). It streams that head's
+// [d_v x d_c] slice of W_uv once with 16-byte loads and reuses each element
+// for all 16 tokens.
 #include <cmath>
 
 #include "device_common.cuh"
@@ -20,21 +21,30 @@
 namespace mla {
 namespace {
 
-constexpr int CB_TOK = 16, CB_THREADS = 128;
+constexpr int CB_TOK = 16, CB_THREADS = 256;
 
+// Dynamic shared memory: o_lat [d_c][CB_TOK] (token fastest), then the
+// partial outputs of the two d_c halves [2][CB_TOK][d_v], then the range
+// table rb[0..C] of the attention partition.
 template <typename T>
 __global__ void __launch_bounds__(CB_THREADS)
 combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ tiles,
                const int32_t* __restrict__ prefix, int B, int n_q, Partition p,
                const float* __restrict__ part_o, const float* __restrict__ part_lse,
                float* __restrict__ out) {
-  extern __shared__ float olat[];  // [CB_TOK][d_c]
+  extern __shared__ __align__(16) float sm[];
+  float* olat = sm;                                   // [d_c][CB_TOK]
+  float* half_out = olat + s.d_c * CB_TOK;            // [2][CB_TOK][d_v]
+  long long* rb = reinterpret_cast<long long*>(half_out + 2 * CB_TOK * s.d_v);  // [C+1]
   __shared__ int c_lo[CB_TOK], c_hi[CB_TOK], row_off[CB_TOK];
   __shared__ float m_max[CB_TOK], inv_den[CB_TOK];
   const int h = blockIdx.x, tok0 = blockIdx.y * CB_TOK;
   const int Tq = B * n_q, ntok = min(CB_TOK, Tq - tok0);
   const long long T_all = prefix[B];
   const long long N = T_all * p.G;
+
+  for (int c = threadIdx.x; c <= p.C; c += CB_THREADS) rb[c] = N > 0 ? range_begin(c, N, p.C) : 0;
+  __syncthreads();
 
   // 1. per token: the CTAs holding its pieces, the max lse and the normaliser
   if (threadIdx.x < CB_TOK) {
@@ -44,21 +54,16 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
     if (t < ntok) {
       const int tok = tok0 + t, b = tok / n_q, qi = tok % n_q;
       const int r = qi * s.n_h + h, g = r / p.RG, rr = r % p.RG;
-      off = (g * B + b) * p.RG + rr;  // slot (c + g*B + b) * RG + rr = c*RG + off
+      off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
       if (tiles[b] > 0) {
         const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
         c0 = cta_of_item(first, N, p.C);
         c1 = cta_of_item(last, N, p.C);
-        for (int c = c0; c <= c1; ++c) {
-          if (range_begin(c, N, p.C) == range_begin(c + 1, N, p.C)) continue;
-          M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
-        }
-        if (M != -INFINITY) {
-          for (int c = c0; c <= c1; ++c) {
-            if (range_begin(c, N, p.C) == range_begin(c + 1, N, p.C)) continue;
-            den += expf(part_lse[static_cast<size_t>(c) * p.RG + off] - M);
-          }
-        }
+        for (int c = c0; c <= c1; ++c)
+          if (rb[c] != rb[c + 1]) M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
+        if (M != -INFINITY)
+          for (int c = c0; c <= c1; ++c)
+            if (rb[c] != rb[c + 1]) den += expf(part_lse[static_cast<size_t>(c) * p.RG + off] - M);
       }
     }
     c_lo[t] = c0;
@@ -68,33 +73,67 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
     inv_den[t] = den > 0.f ? 1.f / den : 0.f;
   }
   __syncthreads();
-  // 2. o_lat = weighted sum of the normalised partials
+
+  // 2. o_lat = weighted sum of the normalised partials (coalesced over d_c)
   for (int t = 0; t < CB_TOK; ++t) {
     for (int dc = threadIdx.x; dc < s.d_c; dc += CB_THREADS) {
       float acc = 0.f;
       for (int c = c_lo[t]; c <= c_hi[t]; ++c) {
-        if (range_begin(c, N, p.C) == range_begin(c + 1, N, p.C)) continue;
+        if (rb[c] == rb[c + 1]) continue;
         const size_t row = static_cast<size_t>(c) * p.RG + row_off[t];
-        const float w = expf(part_lse[row] - m_max[t]) * inv_den[t];
-        acc = fmaf(w, part_o[row * s.d_c + dc], acc);
+        acc = fmaf(expf(part_lse[row] - m_max[t]) * inv_den[t], part_o[row * s.d_c + dc], acc);
       }
-      olat[t * s.d_c + dc] = acc;
+      olat[dc * CB_TOK + t] = acc;
     }
   }
   __syncthreads();
-  // 3. out = o_lat W_uv[h]
-  const T* W = w_uv + static_cast<size_t>(h) * s.d_c * s.d_v;
-  for (int dv = threadIdx.x; dv < s.d_v; dv += CB_THREADS) {
+
+  // 3. out = o_lat W_uv[h]: W_uv is packed [h][d_v][d_c]. A thread owns one
+  // output column for all 16 tokens and half of the d_c reduction.
+  constexpr int V = Vec<T>::N;
+  const T* W = w_uv + static_cast<size_t>(h) * s.d_v * s.d_c;
+  const int dc_half = (s.d_c + 1) / 2;
+  const bool vec_ok = s.d_c % (2 * V) == 0;
+  for (int idx = threadIdx.x; idx < 2 * s.d_v; idx += CB_THREADS) {
+    const int dv = idx % s.d_v, part = idx / s.d_v;
+    const int k0 = part * dc_half, k1 = min(s.d_c, k0 + dc_half);
     float acc[CB_TOK];
 #pragma unroll
     for (int t = 0; t < CB_TOK; ++t) acc[t] = 0.f;
-    for (int dc = 0; dc < s.d_c; ++dc) {
-      const float w = to_f32<T>(W[static_cast<size_t>(dc) * s.d_v + dv]);
+    const T* wr = W + static_cast<size_t>(dv) * s.d_c;
+    if (vec_ok) {
+#pragma unroll 2
+      for (int k = k0; k < k1; k += V) {
+        float wv[V];
+        load_vec<T>(wr + k, wv);
 #pragma unroll
-      for (int t = 0; t < CB_TOK; ++t) acc[t] = fmaf(olat[t * s.d_c + dc], w, acc[t]);
+        for (int j = 0; j < V; ++j) {
+          const float4* ov = reinterpret_cast<const float4*>(olat + (k + j) * CB_TOK);
+#pragma unroll
+          for (int u = 0; u < CB_TOK / 4; ++u) {
+            const float4 x = ov[u];
+            acc[4 * u + 0] = fmaf(wv[j], x.x, acc[4 * u + 0]);
+            acc[4 * u + 1] = fmaf(wv[j], x.y, acc[4 * u + 1]);
+            acc[4 * u + 2] = fmaf(wv[j], x.z, acc[4 * u + 2]);
+            acc[4 * u + 3] = fmaf(wv[j], x.w, acc[4 * u + 3]);
+          }
+        }
+      }
+    } else {
+      for (int k = k0; k < k1; ++k) {
+        const float wv = to_f32<T>(wr[k]);
+#pragma unroll
+        for (int t = 0; t < CB_TOK; ++t) acc[t] = fmaf(wv, olat[k * CB_TOK + t], acc[t]);
+      }
     }
-    for (int t = 0; t < ntok; ++t)
-      out[(static_cast<size_t>(tok0 + t) * s.n_h + h) * s.d_v + dv] = acc[t];
+#pragma unroll
+    for (int t = 0; t < CB_TOK; ++t) half_out[(part * CB_TOK + t) * s.d_v + dv] = acc[t];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ntok * s.d_v; i += CB_THREADS) {
+    const int t = i / s.d_v, dv = i % s.d_v;
+    out[(static_cast<size_t>(tok0 + t) * s.n_h + h) * s.d_v + dv] =
+        half_out[t * s.d_v + dv] + half_out[(CB_TOK + t) * s.d_v + dv];
   }
 }
 
@@ -103,9 +142,10 @@ cudaError_t combine_t(const Shape& s, const Weights* w, int B, int n_q, const Pa
                       const WsView& ws, float* out, cudaStream_t st) {
   const int Tq = B * n_q;
   dim3 grid(s.n_h, (Tq + CB_TOK - 1) / CB_TOK);
-  const size_t smem = sizeof(float) * CB_TOK * s.d_c;
+  const size_t smem = sizeof(float) * (CB_TOK * s.d_c + 2 * CB_TOK * s.d_v) +
+                      sizeof(long long) * (p.C + 1);
   auto kern = combine_kernel<T>;
-  if (smem > 40 * 1024) {
+  if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -57,7 +57,8 @@ struct Weights {
                   // The d_r rotary columns are interleaved so that rotary
                   // dims i and i + d_r/2 sit in adjacent packed columns.
   void* w_uk;     // [n_h][d_c][d_nope]
-  void* w_uv;     // [n_h][d_c][d_v]
+  void* w_uv;     // [n_h][d_v][d_c]: per head, one contiguous d_c row per output
+  double* inv_freq;  // [d_r/2] rope_base^(-2i/d_r), computed on the host in fp64
 };
 
 // ---------------------------------------------------------------- launchers

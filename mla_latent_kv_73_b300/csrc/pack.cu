@@ -6,6 +6,7 @@
 // per head for the query-side fold, W_uv per head for the output-side fold,
 // and [W_dkv | W_kr] one output column per row for the compress-and-append
 // kernel. The packing only copies and transposes. It does no arithmetic.
+// (The RoPE inverse-frequency table is filled on the host.)
 #include "device_common.cuh"
 
 namespace mla {
@@ -55,6 +56,21 @@ __global__ void pack_per_head_kernel(const T* __restrict__ W, T* __restrict__ Wp
   }
 }
 
+// W [d_c, n_h*d] (row-major) -> Wp [n_h][d][d_c]: each output column contiguous
+template <typename T>
+__global__ void pack_per_head_t_kernel(const T* __restrict__ W, T* __restrict__ Wp, int d_c,
+                                       int n_h, int d) {
+  const size_t total = static_cast<size_t>(n_h) * d_c * d;
+  for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total;
+       o += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(o % d_c);
+    const size_t t = o / d_c;
+    const int j = static_cast<int>(t % d);
+    const int h = static_cast<int>(t / d);
+    Wp[o] = W[static_cast<size_t>(c) * n_h * d + static_cast<size_t>(h) * d + j];
+  }
+}
+
 template <typename T>
 cudaError_t pack_all(const Shape& s, const void* W_dkv, const void* W_kr, const void* W_uk,
                      const void* W_uv, Weights* w, cudaStream_t st) {
@@ -69,8 +85,8 @@ cudaError_t pack_all(const Shape& s, const void* W_dkv, const void* W_kr, const 
                                                 static_cast<T*>(w->w_uk), s.d_c, s.n_h, s.d_nope);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pack_per_head_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(W_uv),
-                                                static_cast<T*>(w->w_uv), s.d_c, s.n_h, s.d_v);
+  pack_per_head_t_kernel<T><<<1024, 256, 0, st>>>(static_cast<const T*>(W_uv),
+                                                  static_cast<T*>(w->w_uv), s.d_c, s.n_h, s.d_v);
   return cudaGetLastError();
 }
 
