@@ -197,6 +197,33 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
                               int32_t B, int32_t n_q, float* out, void* workspace,
                               size_t ws_bytes, cudaStream_t stream);
 
+/* Size of the fixed device array that mla_decode_no_alloc uses in place of a
+ * workspace: 32 MiB. */
+#define MLA_NO_ALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/* mla_decode for callers that cannot allocate device memory. The paper has
+ * no counterpart to this call: it is a deployment convenience.
+ * Some callers are not allowed to call cudaMalloc or any other allocator on
+ * the decode path. Examples are a serving loop that must not take an
+ * allocator lock mid-step, and a runtime that hands out all device memory
+ * itself. Such callers cannot supply mla_decode's workspace. This call takes
+ * the same arguments as mla_decode minus the workspace, and computes the same
+ * result. Its scratch space is one array of MLA_NO_ALLOC_WORKSPACE_BYTES
+ * inside the library's device image, which every GPU that loads the library
+ * holds until the process exits. The call allocates nothing.
+ *  - Returns MLA_ERR_WORKSPACE, and queues nothing, when the request needs
+ *    more scratch than the array holds (see mla_decode_workspace_size).
+ *  - The first call on each device looks up the array's device address.
+ *    Make that first call before any stream capture.
+ *  - All calls on a device share the array. It keeps the previous call's
+ *    contents, and nothing in it needs to start at zero. Calls whose GPU work
+ *    overlaps (other streams, other host threads) race on it, so order them,
+ *    for example by issuing them on one stream. */
+mla_status mla_decode_no_alloc(const mla_config* cfg, mla_weights w, const void* q,
+                               const void* cache, int32_t num_blocks, const int32_t* page_table,
+                               int32_t max_blocks, const int32_t* seq_lens, int32_t B,
+                               int32_t n_q, float* out, cudaStream_t stream);
+
 /* Which decode kernel mla_decode would run for this config on the current
  * device. Writes an mla_impl value other than MLA_IMPL_AUTO to *impl, a host
  * pointer. */

@@ -24,7 +24,8 @@ MLA_DEVERR_PAGE_RANGE, MLA_DEVERR_SEQ_LEN, MLA_DEVERR_APPEND_INDEX, MLA_DEVERR_T
 EXPORTS = ["mla_absorb_weights", "mla_weights_free", "mla_append_kv",
            "mla_decode_workspace_size", "mla_decode", "mla_decode_absorb_q",
            "mla_decode_attend", "mla_decode_combine", "mla_decode_impl",
-           "mla_get_last_device_error", "mla_status_string"]
+           "mla_get_last_device_error", "mla_status_string", "mla_decode_no_alloc"]
+MLA_NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
 class mla_config(ctypes.Structure):
@@ -59,6 +60,7 @@ def _declare(lib):
         "mla_decode_attend": [cfgp, _P, _I, _P, _I, _P, _I, _I, _P, ctypes.c_size_t, _P],
         "mla_decode_combine": [cfgp, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_decode_impl": [cfgp, ctypes.POINTER(_I)],
+        "mla_decode_no_alloc": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P],
         "mla_get_last_device_error": [_P, ctypes.POINTER(ctypes.c_uint32)],
         "mla_status_string": [_I],
     }
@@ -149,6 +151,14 @@ def mla_decode(cfg, w, q, cache, page_table, seq_lens, out, workspace, stream=No
         ctypes.byref(cfg), w, ptr(q), ptr(cache), cache.shape[0], ptr(page_table),
         page_table.shape[1], ptr(seq_lens), B, n_q, ptr(out), ptr(workspace),
         workspace.numel() * workspace.element_size(), stream_handle(stream)))
+
+
+def mla_decode_no_alloc(cfg, w, q, cache, page_table, seq_lens, out, stream=None):
+    """mla_decode without a workspace argument (see include/mla.h)."""
+    B, n_q = q.shape[0], q.shape[1]
+    check("mla_decode_no_alloc", load().mla_decode_no_alloc(
+        ctypes.byref(cfg), w, ptr(q), ptr(cache), cache.shape[0], ptr(page_table),
+        page_table.shape[1], ptr(seq_lens), B, n_q, ptr(out), stream_handle(stream)))
 
 
 def mla_decode_absorb_q(cfg, w, q, seq_lens, max_blocks, workspace, stream=None):
