@@ -17,49 +17,12 @@
 // Block (0, 0) also writes the split-KV plan: the tiles of each sequence and
 // their prefix sum. The attention and combine kernels both read it.
 #include "device_common.cuh"
+#include "plan.cuh"
 
 namespace mla {
 namespace {
 
 constexpr int AQ_TOK = 16, AQ_THREADS = 256;
-
-__device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks,
-                           int bs, int TS, int32_t* tiles, int32_t* prefix, uint32_t* err) {
-  __shared__ int32_t warp_sums[AQ_THREADS / 32];
-  __shared__ int32_t carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-  for (int b0 = 0; b0 < B; b0 += AQ_THREADS) {
-    const int b = b0 + threadIdx.x;
-    int t = 0;
-    if (b < B) {
-      const long long L = seq_lens[b];
-      if (L < n_q || L > static_cast<long long>(max_blocks) * bs) {
-        set_error(err, MLA_DEVERR_SEQ_LEN);
-      } else {
-        t = static_cast<int>((L + TS - 1) / TS);
-      }
-      tiles[b] = t;
-    }
-    // inclusive warp scan
-    int v = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += u;
-    }
-    if (lane == 31) warp_sums[warp] = v;
-    __syncthreads();
-    int before = carry;
-    for (int w = 0; w < warp; ++w) before += warp_sums[w];
-    if (b < B) prefix[b] = before + v - t;
-    __syncthreads();
-    if (threadIdx.x == AQ_THREADS - 1) carry = before + v;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) prefix[B] = carry;
-}
 
 template <typename T>
 __global__ void __launch_bounds__(AQ_THREADS)
@@ -73,7 +36,7 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
   const int Tq = B * n_q;
   const int dq = s.d_nope + s.d_r, R = s.R();
   if (blockIdx.x == 0 && blockIdx.y == 0)
-    write_plan(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
+    write_plan<AQ_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
 
   const int ntok = min(AQ_TOK, Tq - tok0);
   for (int i = threadIdx.x; i < AQ_TOK * s.d_nope; i += AQ_THREADS) {

@@ -1,0 +1,212 @@
+// a2 (tensor-core variant): fold each head's query into latent space.
+//
+//   qabs[t, h, 0:512]   = W_uk[h] q_nope[t, h]       (q_lat)
+//   qabs[t, h, 512:576] = RoPE(q_rope[t, h], pos_t)   (q_pe)
+//
+// Source: "Multi-head Latent Attention and KV Cache Compression", section
+// "The absorption trick and decoupled RoPE". The content score q.(W_uk c)
+// equals (W_uk^T q).c, so each query is moved into latent space once per step
+// and dotted against cached latents directly. Only the position block is
+// rotated, at the query's own position ("Multi-head Latent Attention: the KV
+// cache, compressed", section "RoPE, and why the explanations stop here").
+//
+// Per head this is a dense [512 x 128] x [128 x tokens] product, so it runs on
+// tcgen05: one CTA per (head, up to 128 query tokens). TMA stages the head's
+// whole W_uk slice (128 KB, eight 128 x 64 boxes) and the tokens' q_nope
+// (a 3-D box over [token][head][dim]) into shared memory in one go, so the
+// weight stream has 128 KB in flight per SM. One thread issues 32 MMAs with
+// M = 128 latent rows, N = tokens, K = 128, accumulating q_lat^T in TMEM
+// (4 blocks of up to 128 columns). Four warps read it back, one latent row per
+// lane, and store bf16. The other four warps rotate q_rope meanwhile.
+//
+// Block (0, 0) also writes the split-KV plan (tiles per sequence and their
+// prefix sum), which the attention and combine kernels read.
+#include "device_common.cuh"
+#include "plan.cuh"
+#include "sm100_ptx.cuh"
+#include "tmap.h"
+
+namespace mla {
+namespace {
+
+using namespace mla_ptx;
+
+constexpr int AT_TOK = 128;                    // query tokens per CTA (MMA N)
+constexpr int AT_THREADS = 256;
+constexpr uint32_t AT_WBOX = 128 * 128;        // 128 rows x 64 bf16
+constexpr long long AT_WAIT = 2000000000LL;    // ~1 s
+
+struct __align__(1024) AbsSmem {
+  uint8_t w[8][AT_WBOX];          // box (M-block j, K-chunk kc) at index 2*j + kc
+  uint8_t q[2][AT_TOK * 128];     // K-chunk kc: token rows of 128 B
+  uint64_t full, done;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ uint64_t kdesc(const void* base, uint32_t byte_off) {
+  return smem_desc(smem_u32(base) + byte_off, 16, 1024, kSwizzle128B);
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_q, Shape s,
+                   const __nv_bfloat16* __restrict__ q, const double* __restrict__ inv_freq,
+                   const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
+                   int n_tok_box, __nv_bfloat16* __restrict__ qabs, int32_t* tiles,
+                   int32_t* prefix, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  AbsSmem& sm = *reinterpret_cast<AbsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    write_plan<AT_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
+
+  const int h = blockIdx.x;
+  const int t0 = blockIdx.y * AT_TOK;
+  const int Tq = B * n_q;
+  const int ntok = min(AT_TOK, Tq - t0);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  constexpr int R = 576, DQ = 192;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.full, 1);
+    mbar_init(&sm.done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  bool ok = true;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_q);
+    mbar_arrive_expect_tx(&sm.full, 8 * AT_WBOX + 2 * n_tok_box * 128);
+    for (int j = 0; j < 4; ++j)
+      for (int kc = 0; kc < 2; ++kc)
+        tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full);
+    for (int kc = 0; kc < 2; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full);
+  }
+  if (warp == 1 && lane == 0) {
+    ok = mbar_wait(&sm.full, 0, AT_WAIT);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, n_tok_box, false, false);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_bf16_ss(tmem + 128 * j, kdesc(sm.w[2 * j + (k >> 2)], (k & 3) * 32),
+                      kdesc(sm.q[k >> 2], (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
+      mma_commit(&sm.done);
+    } else {
+      set_error(err, MLA_DEVERR_TIMEOUT);
+    }
+  }
+
+  if (warp >= 4) {
+    // rotary block of each query, rotated at the query's own position
+    for (int i = threadIdx.x - 128; i < ntok * 32; i += 128) {
+      const int tt = i / 32, k = i % 32;
+      const int tok = t0 + tt, b = tok / n_q, qi = tok % n_q;
+      const int pos = seq_lens[b] - n_q + qi;
+      const __nv_bfloat16* qr = q + (static_cast<size_t>(tok) * s.n_h + h) * DQ + 128;
+      const float x1 = __bfloat162float(qr[k]), x2 = __bfloat162float(qr[k + 32]);
+      float c, sn;
+      rope_cos_sin(pos, inv_freq[k], &c, &sn);
+      __nv_bfloat16* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + 512;
+      o[k] = __float2bfloat16_rn(x1 * c - x2 * sn);
+      o[k + 32] = __float2bfloat16_rn(x1 * sn + x2 * c);
+    }
+  } else {
+    // q_lat^T from TMEM: lane = latent row inside M-block j, column = token
+    const bool done = mbar_wait(&sm.done, 0, 2 * AT_WAIT);
+    tc_fence_after();
+    if (!done) {
+      if (lane == 0 && warp == 0) set_error(err, MLA_DEVERR_TIMEOUT);
+    } else {
+      const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+      for (int j = 0; j < 4; ++j) {
+        const int dc = 128 * j + 32 * warp + lane;
+        for (int c0 = 0; c0 < n_tok_box; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + lane_base + 128 * j + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int tt = c0 + i;
+            if (tt < ntok)
+              qabs[(static_cast<size_t>(t0 + tt) * s.n_h + h) * R + dc] = __float2bfloat16_rn(v[i]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool absorb_tc_supported(const Shape& s, mla_dtype dt) {
+  return dt == MLA_BF16 && s.d_c == 512 && s.d_nope == 128 && s.d_r == 64;
+}
+
+cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
+                               const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                               const Partition& p, const WsView& ws, uint32_t* err,
+                               cudaStream_t st) {
+  const int Tq = B * n_q;
+  const int n_tok_box = min(AT_TOK, ((Tq + 15) / 16) * 16);
+  TmapSpec ws_spec{};
+  ws_spec.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  ws_spec.rank = 2;
+  ws_spec.base = w->w_uk;
+  ws_spec.dims[0] = 128;
+  ws_spec.dims[1] = static_cast<uint64_t>(s.n_h) * 512;
+  ws_spec.strides[0] = 256;
+  ws_spec.box[0] = 64;
+  ws_spec.box[1] = 128;
+  ws_spec.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  TmapSpec qs{};
+  qs.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  qs.rank = 3;
+  qs.base = q;
+  qs.dims[0] = 192;
+  qs.dims[1] = s.n_h;
+  qs.dims[2] = Tq;
+  qs.strides[0] = 192 * 2;
+  qs.strides[1] = static_cast<uint64_t>(s.n_h) * 192 * 2;
+  qs.box[0] = 64;
+  qs.box[1] = 1;
+  qs.box[2] = n_tok_box;
+  qs.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap tw, tq;
+  if (!get_tmap(ws_spec, &tw) || !get_tmap(qs, &tq)) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(AbsSmem) + 1024;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  dim3 grid(s.n_h, (Tq + AT_TOK - 1) / AT_TOK);
+  absorb_q_tc_kernel<<<grid, AT_THREADS, smem, st>>>(
+      tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
+      p.TS, n_tok_box, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles, ws.prefix, err);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

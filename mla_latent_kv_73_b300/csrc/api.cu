@@ -376,6 +376,9 @@ mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void*
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
   const WsView v = ws_view(workspace, p.lay);
+  if (p.impl == MLA_IMPL_TENSOR_CORE && absorb_tc_supported(p.s, cfg->dtype) && aligned16(q))
+    return from_cuda(launch_absorb_q_tc(p.s, &w->w, q, seq_lens, max_blocks, B, n_q, p.part, v,
+                                        di->err, stream));
   return from_cuda(launch_absorb_q(p.s, cfg->dtype, &w->w, q, seq_lens, max_blocks, B, n_q,
                                    p.part, v, di->err, stream));
 }
@@ -413,6 +416,8 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
   const WsView v = ws_view(workspace, p.lay);
+  if (p.impl == MLA_IMPL_TENSOR_CORE && combine_tc_supported(p.s, cfg->dtype))
+    return from_cuda(launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream));
   return from_cuda(launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out,
                                   stream));
 }

@@ -10,14 +10,19 @@
 // "DeepSeek V3 Multi-Head Latent Attention (MLA): How It Slashes KV Cache
 // Memory", section "Low-Rank Key-Value Joint Compression".
 //
-// Two kernels share one epilogue:
-//  * append_gemv_kernel for decode-sized T. The weight read (d_model x R)
-//    dominates. Each CTA owns 4 packed columns and splits d_model over its
-//    threads, so every weight element is read once per 8 tokens.
+// Three kernels share one epilogue:
+//  * append_staged_kernel for decode-sized T (up to 256 tokens). The weight
+//    read (d_model x R) dominates. Each CTA owns 4 packed columns. One thread
+//    bulk-copies their d_model weights and the first 16 tokens' hidden states
+//    into shared memory at entry, so the whole slice is in flight at once,
+//    and later 16-token chunks reuse the staged weights.
+//  * append_gemv_kernel, the same product with direct global loads, for
+//    inputs the bulk copy cannot take (misaligned or very wide rows).
 //  * append_gemm_kernel for bulk fills: a 64 x 64 register-tiled fp32 GEMM.
 // The packed weight stores rotary dims i and i + d_r/2 in adjacent columns,
 // so one thread (gemm) or one CTA (gemv) always holds both halves of a pair.
 #include "device_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
@@ -140,6 +145,116 @@ append_gemv_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
   }
 }
 
+constexpr int ST_COLS = 4, ST_TOK = 16, ST_THREADS = 256;
+constexpr long long ST_WAIT = 2000000000LL;
+
+// Dynamic shared memory: W slice [ST_COLS][d_model], then x chunk
+// [ST_TOK][d_model], both in the input dtype; the barrier sits in static
+// shared memory. Requires d_model * sizeof(T) % 16 == 0 and 16-byte aligned x.
+template <typename T>
+__global__ void __launch_bounds__(ST_THREADS)
+append_staged_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
+                     T* __restrict__ cache, AppendArgs a) {
+  using namespace mla_ptx;
+  constexpr int V = Vec<T>::N;
+  extern __shared__ __align__(128) uint8_t st_raw[];
+  T* ws = reinterpret_cast<T*>(st_raw);
+  T* xs = ws + static_cast<size_t>(ST_COLS) * s.d_model;
+  __shared__ uint64_t bar;
+  __shared__ float red[ST_THREADS / 32][ST_COLS * 4];
+  __shared__ float res[ST_COLS * ST_TOK];
+  __shared__ int failed;
+  const int R = s.R();
+  const int col0 = blockIdx.x * ST_COLS;
+  const int ncol = min(ST_COLS, R - col0);
+  const uint32_t row_bytes = static_cast<uint32_t>(s.d_model) * sizeof(T);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tg = threadIdx.x / 64, ks = threadIdx.x % 64;  // token group, k slice
+  if (threadIdx.x == 0) {
+    failed = 0;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  int chunk = 0;
+  for (int t0 = 0; t0 < a.T; t0 += ST_TOK, ++chunk) {
+    const int nt = min(ST_TOK, a.T - t0);
+    if (threadIdx.x == 0) {
+      const uint32_t wbytes = chunk == 0 ? ncol * row_bytes : 0u;
+      mbar_arrive_expect_tx(&bar, wbytes + nt * row_bytes);
+      if (chunk == 0) bulk_load(ws, Wp + static_cast<size_t>(col0) * s.d_model, wbytes, &bar);
+      bulk_load(xs, x + static_cast<size_t>(t0) * s.d_model, nt * row_bytes, &bar);
+    }
+    if (!mbar_wait(&bar, chunk & 1, ST_WAIT)) failed = 1;
+    __syncthreads();
+    if (failed) {
+      if (threadIdx.x == 0) set_error(a.err, MLA_DEVERR_TIMEOUT);
+      return;
+    }
+    float acc[ST_COLS][4];
+#pragma unroll
+    for (int c = 0; c < ST_COLS; ++c)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) acc[c][t] = 0.f;
+    for (int k = V * ks; k < s.d_model; k += 64 * V) {
+      float wv[ST_COLS][V];
+#pragma unroll
+      for (int c = 0; c < ST_COLS; ++c) {
+        if (c < ncol) {
+          load_vec<T>(ws + static_cast<size_t>(c) * s.d_model + k, wv[c]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < V; ++i) wv[c][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int tt = 4 * tg + t;
+        if (tt < nt) {
+          float xv[V];
+          load_vec<T>(xs + static_cast<size_t>(tt) * s.d_model + k, xv);
+#pragma unroll
+          for (int c = 0; c < ST_COLS; ++c)
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[c][t] = fmaf(wv[c][i], xv[i], acc[c][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < ST_COLS; ++c)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        float v = acc[c][t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[warp][c * 4 + t] = v;
+      }
+    __syncthreads();
+    if (threadIdx.x < ST_COLS * ST_TOK) {
+      const int c = threadIdx.x / ST_TOK, tt = threadIdx.x % ST_TOK;
+      const int g = tt / 4, t = tt % 4;  // warps 2g and 2g+1 hold token group g
+      res[threadIdx.x] = red[2 * g][c * 4 + t] + red[2 * g + 1][c * 4 + t];
+    }
+    __syncthreads();
+    if (threadIdx.x < ST_COLS * ST_TOK) {
+      const int c = threadIdx.x / ST_TOK, tt = threadIdx.x % ST_TOK;
+      const int pc = col0 + c, tok = t0 + tt;
+      if (c < ncol && tt < nt) {
+        const long long row = append_row(a, s, tok);
+        if (row >= 0) {
+          const int ce = c & ~1;  // even member of the rotary pair inside this CTA
+          float out;
+          const int dst = finish_column(s, a.inv_freq, pc, res[c * ST_TOK + tt],
+                                        res[ce * ST_TOK + tt], res[(ce + 1) * ST_TOK + tt],
+                                        a.pos[tok], &out);
+          cache[row * R + dst] = from_f32<T>(out);
+        }
+      }
+    }
+    __syncthreads();  // x chunk and res are reused
+  }
+}
+
 constexpr int GM_BT = 64, GM_BC = 64, GM_BK = 32;
 
 template <typename T>
@@ -214,7 +329,23 @@ cudaError_t append_t(const Shape& s, const Weights* w, const void* x, AppendArgs
                      cudaStream_t st) {
   const int R = s.R();
   const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0;
-  if (a.T <= 32 && aligned && s.d_model % Vec<T>::N == 0) {
+  const size_t staged_smem = sizeof(T) * static_cast<size_t>(ST_COLS + ST_TOK) * s.d_model;
+  if (a.T <= 256 && aligned && s.d_model % Vec<T>::N == 0 && staged_smem <= 200 * 1024) {
+    static int attr_bytes[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (staged_smem > 48 * 1024 &&
+        (dev < 0 || dev >= 64 || attr_bytes[dev] < static_cast<int>(staged_smem))) {
+      cudaError_t e = cudaFuncSetAttribute(append_staged_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(staged_smem));
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_bytes[dev] = static_cast<int>(staged_smem);
+    }
+    const int grid = (R + ST_COLS - 1) / ST_COLS;
+    append_staged_kernel<T><<<grid, ST_THREADS, staged_smem, st>>>(
+        s, static_cast<const T*>(x), static_cast<const T*>(w->w_dkvr), static_cast<T*>(cache), a);
+  } else if (a.T <= 32 && aligned && s.d_model % Vec<T>::N == 0) {
     const int grid = (R + GEMV_COLS - 1) / GEMV_COLS;
     append_gemv_kernel<T><<<grid, GEMV_THREADS, 0, st>>>(
         s, static_cast<const T*>(x), static_cast<const T*>(w->w_dkvr), static_cast<T*>(cache), a);

@@ -1,0 +1,251 @@
+// a4 + a5 (tensor-core variant): merge the split-KV partials by their
+// log-sum-exps, then up-project the latent output through W_uv.
+//
+//   lse   = log sum_s exp(lse_s)
+//   o_lat = sum_s exp(lse_s - lse) * o_s          (each o_s already divided by l_s)
+//   out   = W_uv[h] o_lat                          (d_v = 128 outputs per head)
+//
+// The value up-projection runs once per head and query, after the weighted
+// sum, rather than once per cached token. Source: "Multi-head Latent
+// Attention and KV Cache Compression", section "The absorption trick and
+// decoupled RoPE" (W_uv is absorbed on the output side the way W_uk is on the
+// query side).
+//
+// One CTA per (head, up to 32 query tokens). At entry, one thread starts the
+// TMA of the head's whole W_uv slice (128 KB, eight 128 x 64 boxes) so the
+// weight stream overlaps the combine. All threads then merge the partials of
+// their tokens into o_lat (fp32 in registers), split each value into a bf16
+// high part and a bf16 remainder, and store both as MMA operands in shared
+// memory. One thread issues the product out^T = W_uv[h] (o_hi + o_lo)^T as
+// 2 x 32 MMAs with M = 128 outputs, N = tokens, K = 512. The hi + lo split keeps
+// about 16 bits of o_lat's mantissa, so rounding o_lat for the tensor core
+// costs no measurable accuracy. Four warps read the fp32 result from TMEM,
+// one output column per lane, and store it.
+#include <cmath>
+
+#include "device_common.cuh"
+#include "sm100_ptx.cuh"
+#include "tmap.h"
+
+namespace mla {
+namespace {
+
+using namespace mla_ptx;
+
+constexpr int CT_TOK = 32;                   // query tokens per CTA (MMA N)
+constexpr int CT_THREADS = 256;
+constexpr uint32_t CT_WBOX = 128 * 128;      // 128 rows x 64 bf16
+constexpr uint32_t CT_OBOX = CT_TOK * 128;   // 32 token rows x 64 bf16
+constexpr long long CT_WAIT = 2000000000LL;
+
+struct __align__(1024) CombSmem {
+  uint8_t w[8][CT_WBOX];          // K-chunk kc of W_uv[h]: 128 output rows x 64 latent dims
+  uint8_t o[2][8][CT_OBOX];       // [hi/lo][K-chunk]: token rows x 64 latent dims
+  uint64_t wfull, done;
+  uint32_t tmem_base;
+  int c_lo[CT_TOK], c_hi[CT_TOK], row_off[CT_TOK];
+  float m_max[CT_TOK], inv_den[CT_TOK];
+};
+
+__device__ __forceinline__ uint64_t kdesc(const void* base, uint32_t byte_off) {
+  return smem_desc(smem_u32(base) + byte_off, 16, 1024, kSwizzle128B);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(CT_THREADS, 1)
+combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
+                  const int32_t* __restrict__ tiles, const int32_t* __restrict__ prefix, int B,
+                  int n_q, Partition p, const float* __restrict__ part_o,
+                  const float* __restrict__ part_lse, float* __restrict__ out, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  CombSmem& sm = *reinterpret_cast<CombSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  long long* rb = reinterpret_cast<long long*>(&sm + 1);  // [C + 1] range starts
+  const int h = blockIdx.x, t0 = blockIdx.y * CT_TOK;
+  const int Tq = B * n_q, ntok = min(CT_TOK, Tq - t0);
+  const int n_box = ((ntok + 15) / 16) * 16;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.wfull, 1);
+    mbar_init(&sm.done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_w);
+    mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
+    for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
+  }
+
+  // 1. per token: the CTAs holding its pieces, the largest lse and the normaliser
+  const long long T_all = prefix[B];
+  const long long N = T_all * p.G;
+  for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = N > 0 ? range_begin(c, N, p.C) : 0;
+  __syncthreads();
+  if (threadIdx.x < CT_TOK) {
+    const int t = threadIdx.x;
+    int c0 = 0, c1 = -1, off = 0;
+    float M = -INFINITY, den = 0.f;
+    if (t < ntok) {
+      const int tok = t0 + t, b = tok / n_q, qi = tok % n_q;
+      const int r = qi * n_h + h, g = r / p.RG, rr = r % p.RG;
+      off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
+      if (tiles[b] > 0) {
+        const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
+        c0 = cta_of_item(first, N, p.C);
+        c1 = cta_of_item(last, N, p.C);
+        for (int c = c0; c <= c1; ++c)
+          if (rb[c] != rb[c + 1]) M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
+        if (M != -INFINITY)
+          for (int c = c0; c <= c1; ++c)
+            if (rb[c] != rb[c + 1]) den += expf(part_lse[static_cast<size_t>(c) * p.RG + off] - M);
+      }
+    }
+    sm.c_lo[t] = c0;
+    sm.c_hi[t] = (M == -INFINITY) ? -1 : c1;
+    sm.row_off[t] = off;
+    sm.m_max[t] = M;
+    sm.inv_den[t] = den > 0.f ? 1.f / den : 0.f;
+  }
+  __syncthreads();
+
+  // 2. o_lat = weighted sum of the partials; thread owns 8 latent dims of a token
+  {
+    const int u = threadIdx.x % 64;  // 16-byte unit: latent dims [8u, 8u + 8)
+    const int kc = u / 8, uu = u % 8;
+    for (int tt = threadIdx.x / 64; tt < CT_TOK; tt += CT_THREADS / 64) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      if (tt < ntok) {
+        const int lo = sm.c_lo[tt], hi = sm.c_hi[tt];
+        for (int c = lo; c <= hi; ++c) {
+          if (rb[c] == rb[c + 1]) continue;
+          const size_t row = static_cast<size_t>(c) * p.RG + sm.row_off[tt];
+          const float wgt = expf(part_lse[row] - sm.m_max[tt]) * sm.inv_den[tt];
+          const float4* src = reinterpret_cast<const float4*>(part_o + row * 512 + 8 * u);
+          const float4 a = src[0], b2 = src[1];
+          acc[0] = fmaf(wgt, a.x, acc[0]);
+          acc[1] = fmaf(wgt, a.y, acc[1]);
+          acc[2] = fmaf(wgt, a.z, acc[2]);
+          acc[3] = fmaf(wgt, a.w, acc[3]);
+          acc[4] = fmaf(wgt, b2.x, acc[4]);
+          acc[5] = fmaf(wgt, b2.y, acc[5]);
+          acc[6] = fmaf(wgt, b2.z, acc[6]);
+          acc[7] = fmaf(wgt, b2.w, acc[7]);
+        }
+      }
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        lw[i] = pack_bf16x2(acc[2 * i] - __low2float(hv), acc[2 * i + 1] - __high2float(hv));
+      }
+      const uint32_t off = tt * 128 + ((uu ^ (tt & 7)) * 16);
+      *reinterpret_cast<uint4*>(sm.o[0][kc] + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sm.o[1][kc] + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // 3. out^T = W_uv[h] o_lat^T on the tensor core
+  if (warp == 1 && lane == 0) {
+    if (mbar_wait(&sm.wfull, 0, CT_WAIT)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, n_box, false, false);
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          mma_bf16_ss(tmem, kdesc(sm.w[k >> 2], (k & 3) * 32),
+                      kdesc(sm.o[part][k >> 2], (k & 3) * 32), idesc,
+                      (part == 0 && k == 0) ? 0u : 1u);
+      mma_commit(&sm.done);
+    } else {
+      set_error(err, MLA_DEVERR_TIMEOUT);
+    }
+  }
+  if (warp < 4) {
+    const bool done = mbar_wait(&sm.done, 0, 2 * CT_WAIT);
+    tc_fence_after();
+    if (done) {
+      const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+      const int dv = 32 * warp + lane;
+      for (int c0 = 0; c0 < n_box; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + lane_base + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int tt = c0 + i;
+          if (tt < ntok) out[(static_cast<size_t>(t0 + tt) * n_h + h) * 128 + dv] = v[i];
+        }
+      }
+    } else if (warp == 0 && lane == 0) {
+      set_error(err, MLA_DEVERR_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+}  // namespace
+
+bool combine_tc_supported(const Shape& s, mla_dtype dt) {
+  return dt == MLA_BF16 && s.d_c == 512 && s.d_v == 128;
+}
+
+cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
+                              const Partition& p, const WsView& ws, float* out, uint32_t* err,
+                              cudaStream_t st) {
+  const int Tq = B * n_q;
+  TmapSpec spec{};
+  spec.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  spec.rank = 2;
+  spec.base = w->w_uv;
+  spec.dims[0] = 512;
+  spec.dims[1] = static_cast<uint64_t>(s.n_h) * 128;
+  spec.strides[0] = 1024;
+  spec.box[0] = 64;
+  spec.box[1] = 128;
+  spec.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap tw;
+  if (!get_tmap(spec, &tw)) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(CombSmem) + 1024 + sizeof(long long) * (p.C + 1);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  static int attr_bytes[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || attr_bytes[dev] < static_cast<int>(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_bytes[dev] = static_cast<int>(smem);
+  }
+  dim3 grid(s.n_h, (Tq + CT_TOK - 1) / CT_TOK);
+  combine_tc_kernel<<<grid, CT_THREADS, smem, st>>>(tw, s.n_h, ws.tiles, ws.prefix, B, n_q, p,
+                                                     ws.part_o, ws.part_lse, out, err);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

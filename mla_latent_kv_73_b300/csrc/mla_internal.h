@@ -87,6 +87,18 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
                              const Partition& p, const WsView& ws, const int32_t* seq_lens,
                              uint32_t* err, cudaStream_t st);
 
+// Tensor-core absorption and combine (bf16, d_c = 512, d_nope = 128, d_r = 64,
+// d_v = 128). The query pointer must be 16-byte aligned for the TMA.
+bool absorb_tc_supported(const Shape& s, mla_dtype dt);
+cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
+                               const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                               const Partition& p, const WsView& ws, uint32_t* err,
+                               cudaStream_t st);
+bool combine_tc_supported(const Shape& s, mla_dtype dt);
+cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
+                              const Partition& p, const WsView& ws, float* out, uint32_t* err,
+                              cudaStream_t st);
+
 cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
                            const WsView& ws, float* out, cudaStream_t st);
