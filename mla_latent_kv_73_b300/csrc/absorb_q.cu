@@ -28,8 +28,8 @@ template <typename T>
 __global__ void __launch_bounds__(AQ_THREADS)
 absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
                 const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
-                int n_q, int max_blocks, int TS, T* __restrict__ qabs, int32_t* tiles,
-                int32_t* prefix, uint32_t* err) {
+                int n_q, int max_blocks, int TS, float out_scale, T* __restrict__ qabs,
+                int32_t* tiles, int32_t* prefix, uint32_t* err) {
   extern __shared__ __align__(16) float qn[];  // [d_nope][AQ_TOK], token fastest
   const int h = blockIdx.x;
   const int tok0 = blockIdx.y * AQ_TOK;
@@ -93,8 +93,8 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
     }
     for (int t = 0; t < ntok; ++t) {
       T* o = qabs + (static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc0;
-      o[0] = from_f32<T>(acc0[t]);
-      if (two) o[1] = from_f32<T>(acc1[t]);
+      o[0] = from_f32<T>(acc0[t] * out_scale);
+      if (two) o[1] = from_f32<T>(acc1[t] * out_scale);
     }
   }
 
@@ -109,21 +109,21 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
     float c, sn;
     rope_cos_sin(pos, inv_freq[k], &c, &sn);
     T* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
-    o[k] = from_f32<T>(x1 * c - x2 * sn);
-    o[k + half] = from_f32<T>(x1 * sn + x2 * c);
+    o[k] = from_f32<T>((x1 * c - x2 * sn) * out_scale);
+    o[k + half] = from_f32<T>((x1 * sn + x2 * c) * out_scale);
   }
 }
 
 template <typename T>
 cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const int32_t* seq_lens,
                        int max_blocks, int B, int n_q, const Partition& p, const WsView& ws,
-                       uint32_t* err, cudaStream_t st) {
+                       float out_scale, uint32_t* err, cudaStream_t st) {
   const int Tq = B * n_q;
   dim3 grid(s.n_h, (Tq + AQ_TOK - 1) / AQ_TOK);
   const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;
   absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
       s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
-      max_blocks, p.TS, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
+      max_blocks, p.TS, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
   return cudaGetLastError();
 }
 
@@ -131,9 +131,12 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
 
 cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
                             const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                            const Partition& p, const WsView& ws, uint32_t* err, cudaStream_t st) {
-  if (dt == MLA_F32) return absorb_q_t<float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, err, st);
-  return absorb_q_t<__nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, err, st);
+                            const Partition& p, const WsView& ws, float out_scale, uint32_t* err,
+                            cudaStream_t st) {
+  if (dt == MLA_F32)
+    return absorb_q_t<float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err, st);
+  return absorb_q_t<__nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err,
+                                   st);
 }
 
 }  // namespace mla

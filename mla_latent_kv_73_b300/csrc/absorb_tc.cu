@@ -52,7 +52,7 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_q, Shape s,
                    const __nv_bfloat16* __restrict__ q, const double* __restrict__ inv_freq,
                    const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
-                   int n_tok_box, __nv_bfloat16* __restrict__ qabs, int32_t* tiles,
+                   int n_tok_box, float out_scale, __nv_bfloat16* __restrict__ qabs, int32_t* tiles,
                    int32_t* prefix, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   AbsSmem& sm = *reinterpret_cast<AbsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -119,8 +119,8 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
       float c, sn;
       rope_cos_sin(pos, inv_freq[k], &c, &sn);
       __nv_bfloat16* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + 512;
-      o[k] = __float2bfloat16_rn(x1 * c - x2 * sn);
-      o[k + 32] = __float2bfloat16_rn(x1 * sn + x2 * c);
+      o[k] = __float2bfloat16_rn((x1 * c - x2 * sn) * out_scale);
+      o[k + 32] = __float2bfloat16_rn((x1 * sn + x2 * c) * out_scale);
     }
   } else {
     // q_lat^T from TMEM: lane = latent row inside M-block j, column = token
@@ -140,7 +140,8 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
           for (int i = 0; i < 16; ++i) {
             const int tt = c0 + i;
             if (tt < ntok)
-              qabs[(static_cast<size_t>(t0 + tt) * s.n_h + h) * R + dc] = __float2bfloat16_rn(v[i]);
+              qabs[(static_cast<size_t>(t0 + tt) * s.n_h + h) * R + dc] =
+                  __float2bfloat16_rn(v[i] * out_scale);
           }
         }
       }
@@ -162,8 +163,8 @@ bool absorb_tc_supported(const Shape& s, mla_dtype dt) {
 
 cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
                                const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                               const Partition& p, const WsView& ws, uint32_t* err,
-                               cudaStream_t st) {
+                               const Partition& p, const WsView& ws, float out_scale,
+                               uint32_t* err, cudaStream_t st) {
   const int Tq = B * n_q;
   const int n_tok_box = min(AT_TOK, ((Tq + 15) / 16) * 16);
   TmapSpec ws_spec{};
@@ -205,7 +206,7 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
   dim3 grid(s.n_h, (Tq + AT_TOK - 1) / AT_TOK);
   absorb_q_tc_kernel<<<grid, AT_THREADS, smem, st>>>(
       tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
-      p.TS, n_tok_box, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles, ws.prefix, err);
+      p.TS, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles, ws.prefix, err);
   return cudaGetLastError();
 }
 

@@ -15,8 +15,6 @@ __device__ uint32_t g_mla_device_error = 0;
 
 namespace mla {
 
-size_t attend_tc_smem_bytes();
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -30,6 +28,7 @@ int current_device() {
 struct DeviceInfo {
   bool ready = false;
   int sms = 0, major = 0, minor = 0;
+  int tc_pairs = 0;  // CTA pairs the tensor-core attention grid holds (0: unavailable)
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -51,6 +50,7 @@ const DeviceInfo* device_info() {
       cudaGetLastError();
       return nullptr;
     }
+    if (di.major == 10 && di.minor == 3) di.tc_pairs = attend_tc_max_pairs();
     di.ready = true;
   }
   return &di;
@@ -87,7 +87,9 @@ Shape shape_of(const mla_config* c) {
 
 int dtype_bytes(mla_dtype d) { return d == MLA_F32 ? 4 : 2; }
 
-bool tc_device(const DeviceInfo* di) { return di && di->major == 10 && di->minor == 3; }
+bool tc_device(const DeviceInfo* di) {
+  return di && di->major == 10 && di->minor == 3 && di->tc_pairs > 0;
+}
 
 // Decode kernel for this config on this device, or -1 if the requested one cannot run.
 int resolve_impl(const mla_config* c, const DeviceInfo* di) {
@@ -119,7 +121,7 @@ mla_status make_plan(const mla_config* cfg, int B, int n_q, const DeviceInfo* di
                      Plan* out) {
   out->s = shape_of(cfg);
   out->impl = impl;
-  out->part = partition_for(impl, out->s, B, n_q, di->sms);
+  out->part = partition_for(impl, out->s, B, n_q, di->sms, di->tc_pairs);
   out->lay = ws_layout(out->s, dtype_bytes(cfg->dtype), B, n_q, out->part);
   return MLA_OK;
 }
@@ -135,13 +137,14 @@ mla_status check_decode_args(const mla_config* cfg, int B, int n_q) {
 
 }  // namespace
 
-Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms) {
+Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms, int tc_pairs) {
   Partition p;
   const int rows = n_q * s.n_h;
   if (impl == MLA_IMPL_TENSOR_CORE) {
-    p.RG = rows <= 64 ? ((rows + 15) / 16) * 16 : 64;
+    // 128 query rows per group (the MMA's M); one work range per CTA pair
+    p.RG = 128;
     p.TS = 64;
-    p.C = num_sms;
+    p.C = tc_pairs;
   } else {
     p.RG = 16;
     p.TS = 64;
@@ -376,11 +379,14 @@ mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void*
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
   const WsView v = ws_view(workspace, p.lay);
+  // The tensor-core attention reads queries pre-multiplied by scale * log2(e).
+  const float out_scale =
+      p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (p.impl == MLA_IMPL_TENSOR_CORE && absorb_tc_supported(p.s, cfg->dtype) && aligned16(q))
     return from_cuda(launch_absorb_q_tc(p.s, &w->w, q, seq_lens, max_blocks, B, n_q, p.part, v,
-                                        di->err, stream));
+                                        out_scale, di->err, stream));
   return from_cuda(launch_absorb_q(p.s, cfg->dtype, &w->w, q, seq_lens, max_blocks, B, n_q,
-                                   p.part, v, di->err, stream));
+                                   p.part, v, out_scale, di->err, stream));
 }
 
 mla_status mla_decode_attend(const mla_config* cfg, const void* cache, int32_t num_blocks,

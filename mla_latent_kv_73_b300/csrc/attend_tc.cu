@@ -1,107 +1,133 @@
 // a3 (tensor-core variant): split-KV attention of absorbed queries over the
-// paged latent cache on tcgen05 / TMEM, with TMA-staged tiles.
+// paged latent cache, on tcgen05 / TMEM with TMA-staged tiles, one pair of
+// CTAs (a 2-CTA cluster) per work range.
 //
-//   S     = Q K^T * scale        Q: [64 query rows x 576], K: [64 tokens x 576]
-//   P     = online softmax of S (causal mask j <= pos_q), bf16
-//   O^T  += C^T P^T              C: the 512 latent columns of the same tile
+//   S   = Q K^T * scale        Q: [128 query rows x 576], K: [64 tokens x 576]
+//   P   = online softmax of S (causal mask j <= pos_q)
+//   O  += P C                  C: the 512 latent columns of the same tile
 //
 // Sources: "Multi-head Latent Attention: the KV cache, compressed", sections
 // "Absorption: the part that makes it free" (queries are projected into
 // latent space and dotted against the cache; keys are never built) and
-// "RoPE, and why the explanations stop here" (the score is the sum of a
-// content part and a decoupled RoPE part, which a single 576-wide dot
-// product over [c | k_rope] computes); "Multi-head Latent Attention and KV
-// Cache Compression", section "The absorption trick and decoupled RoPE"
-// (the output is the softmax-weighted sum of latents, up-projected later).
+// "RoPE, and why the explanations stop here" (the score is a content part
+// plus a decoupled RoPE part, which one 576-wide dot product over
+// [c | k_rope] computes); "Multi-head Latent Attention and KV Cache
+// Compression", section "The absorption trick and decoupled RoPE" (the
+// output is the softmax-weighted sum of latents, up-projected later).
 //
-// Why this shape on sm_103a. All heads share one 576-wide key row and one
-// 512-wide value row per token, so both products are dense contractions.
-// The fp32 latent accumulator of 64 query rows is 64 x 512 x 4 B = 128 KB.
-// Kept transposed (latent dims in TMEM lanes, query rows in columns), it
-// fills 4 M=128 blocks of 64 columns = 256 of the 512 TMEM columns. That
-// leaves room for two 64-column score buffers, so the score MMA of tile i+1
-// overlaps the softmax of tile i. The score MMA uses M = 64 query rows.
-// The value MMA reads its A operand (C^T) straight from the same swizzled
-// tile in shared memory, as an MN-major operand, so the tile is loaded once
-// and feeds both products.
+// Why a CTA pair on sm_103a. All heads share one 576-wide key row and one
+// 512-wide value row per token, so for 128 query rows both products are
+// dense M = 128 contractions. The fp32 accumulator of 128 rows x 512 latent
+// columns is 256 KB, the whole TMEM of one SM, with no room left for
+// scores. So the two CTAs of a cluster split the columns: CTA r holds latent
+// columns [256r, 256r + 256) and rotary columns [512 + 32r, 512 + 32r + 32)
+// of every tile and of Q, and accumulates O for its 256 latent columns
+// (256 TMEM columns). Each CTA computes a partial score over its 288
+// columns (M = 128, N = 64, K = 288). The pair swaps the partials through
+// distributed shared memory: 16-byte st.async stores that count their bytes
+// on the receiver's mbarrier. Each then adds the two partials. fp32
+// addition is commutative, so both CTAs hold bit-identical scores, run the
+// same softmax and agree on every row maximum and sum without further
+// messages. Every cache byte is read from HBM once, by one CTA.
+//
+// TMEM (512 columns): two 64-column score buffers, two 32-column buffers for
+// P (bf16 pairs, read by the value MMA straight from TMEM as its A operand),
+// and the 256-column latent accumulator.
 //
 // Warp roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: Q rows once per piece, then 9 boxes of 64 x 64
-//               bf16 per 64-token page, 2-stage ring
+//   warp 0      TMA producer: Q (4 + 1 boxes) once per piece, then per
+//               64-token page 4 latent boxes (128B swizzle) and 1 rotary box
+//               (64B swizzle), 3-stage ring
 //   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..9  softmax, lazy rescale of O^T and the epilogue of each piece.
-//               Query row r lives in TMEM lane 32*(r/16) + r%16. Each lane
-//               quarter is read by two warps, one per 32-column half of the
-//               score tile. The halves meet once per tile, in shared memory,
-//               to agree on the row maximum.
+//   warps 2..9  softmax. Warp w reads TMEM lane quarter w % 4 (query rows
+//               32(w % 4) .. +31, one row per lane) and score columns
+//               [32h, 32h + 32), h = (w - 2) / 4. The two warps of a lane
+//               quarter meet at a 64-thread named barrier to agree on the
+//               row maximum.
 //
 // Lazy rescale: a row's running max is only raised when the new max exceeds
 // it by more than 8 (log2 units). Otherwise P is computed against the stale
-// max, so its entries stay <= 2^8. The final division by the row sum l
-// cancels the offset exactly.
+// max, so its entries stay <= 2^8. The final division by the row sum cancels
+// the offset exactly.
 //
 // Every mbarrier wait is bounded. On a timeout the CTA sets
-// MLA_DEVERR_TIMEOUT, stops issuing work, drains what it issued, frees
-// TMEM and returns.
+// MLA_DEVERR_TIMEOUT and stops issuing work. It still drains what it issued,
+// meets its peer at the final cluster barrier, frees TMEM and returns.
 #include <cuda.h>
-#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
 #include <mutex>
 
 #include "device_common.cuh"
 #include "sm100_ptx.cuh"
+#include "tmap.h"
 
 namespace mla {
 namespace {
 
 using namespace mla_ptx;
 
-constexpr int TC_ROWS = 64;                 // query rows per group (score MMA M)
-constexpr int TC_TOK = 64;                  // tokens per tile = page size
-constexpr int TC_KCH = 9;                   // 576 / 64 column chunks
-constexpr int TC_STAGES = 2;
-constexpr int TC_THREADS = 320;              // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
-constexpr int TC_SM_THREADS = 256;
-constexpr uint32_t CHUNK_BYTES = 64 * 128;  // 64 rows x 128 B (one 128B-swizzled box)
-constexpr uint32_t TILE_BYTES = TC_KCH * CHUNK_BYTES;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;                // two score buffers at columns 0 and 64
-constexpr uint32_t TM_O = 128;              // O^T block j at columns 128 + 64 j
+constexpr int TP_ROWS = 128;                  // query rows per group (MMA M)
+constexpr int TP_TOK = 64;                    // tokens per tile = page size
+constexpr int TP_STAGES = 3;
+constexpr int TP_THREADS = 384;               // warp 0 TMA, 1 value MMA, 2..9 softmax, 10-11 score MMA
+constexpr int TP_SM_WARPS = 8;                // two softmax groups of four warps
+constexpr int TP_GRP_WARPS = 4;
+constexpr uint32_t QC_BOX = 128 * 128;        // 128 rows x 64 bf16, 128B swizzle
+constexpr uint32_t QR_BOX = 128 * 64;         // 128 rows x 32 bf16, 64B swizzle
+constexpr uint32_t KC_BOX = 64 * 128;         // 64 tokens x 64 bf16
+constexpr uint32_t KR_BOX = 64 * 64;          // 64 tokens x 32 bf16
+constexpr uint32_t Q_BYTES = 2 * QC_BOX + QR_BOX;   // Q through TMA (the rest goes to TMEM)
+constexpr uint32_t STAGE_BYTES = 4 * KC_BOX + KR_BOX;
+constexpr uint32_t X_BYTES = TP_ROWS * TP_TOK * 2;  // fp16 partial scores
+constexpr uint32_t TM_S = 0;                  // score buffers at columns 0 and 64
+constexpr uint32_t TM_P = 128;                // P buffers at columns 128 and 160
+constexpr uint32_t TM_Q = 192;                // Q latent columns 128..255 of this CTA (bf16 pairs)
+constexpr uint32_t TM_O = 256;                // latent accumulator, 256 columns
 constexpr long long WAIT_LIMIT = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float RESCALE_THRESHOLD = 8.f;        // log2 units
 
-struct __align__(1024) TcSmem {
-  uint8_t q[TC_KCH][CHUNK_BYTES];
-  uint8_t kv[TC_STAGES][TC_KCH][CHUNK_BYTES];
-  uint8_t p[CHUNK_BYTES];  // 64 rows x 64 tokens bf16, K-major, 128B swizzle
-  uint64_t kv_full[TC_STAGES], kv_empty[TC_STAGES];
+struct __align__(1024) PairSmem {
+  uint8_t qc[2][QC_BOX];  // Q latent columns 0..127 of this CTA's half
+  uint8_t qr[QR_BOX];
+  struct Stage {
+    uint8_t c[4][KC_BOX];
+    uint8_t r[KR_BOX];
+  } kv[TP_STAGES];
+  // peer's partial scores, fp16 pairs: [buffer][row][64 tokens], 16-byte units swizzled
+  uint32_t xbuf[2][TP_ROWS * TP_TOK / 2];
+  uint32_t sbuf[2][TP_ROWS * TP_TOK / 2];  // own partial scores, staged for the bulk copy
+  uint64_t kv_full[TP_STAGES], kv_empty[TP_STAGES];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];
-  uint64_t p_full, p_empty;
+  uint64_t x_full[2], x_sendok[2];
+  uint64_t p_full[2], pv_done[2];
+  uint64_t m_ready[2], stats[2], sready[2];
   uint64_t o_full, o_empty;
-  uint64_t drain;
+  uint64_t drain[3];
   uint32_t tmem_base;
   int abort_flag;
-  float row_alpha[TC_ROWS];
-  float row_inv_l[TC_ROWS];
-  float xmax[2][TC_ROWS];  // partial row maxima of the two column halves
-  float xsum[TC_ROWS];     // row sum of the second column half
+  float mrow[2][TP_ROWS];   // running row max after tile kv, in slot kv & 1
+  float st_l[2][TP_ROWS];   // per softmax group: row sum at the end of a piece
+  float st_m[2][TP_ROWS];   // ... and the max that sum is referred to
 };
 
-struct TcArgs {
+struct PairArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   const int32_t* tiles;
   const int32_t* prefix;
   float* part_o;
   float* part_lse;
+  const __nv_bfloat16* qabs;  // [q_rows][576] absorbed queries (for the TMEM part of Q)
   uint32_t* err;
-  int num_blocks, max_blocks, B, n_q, n_h, RG, G, C;
-  float scale_log2;
+  long long q_rows;
+  int num_blocks, max_blocks, B, n_q, n_h, G, P;
+  int chunked;  // 1: latent boxes come as one 3-D box per stage / per Q; 0: as 2-D boxes
 };
 
-// One piece: consecutive tiles of one (group, sequence) inside a CTA's range.
+// One piece: consecutive tiles of one (group, sequence) inside a pair's range.
 struct Piece {
   int g, b, t_first, n_tiles;
 };
@@ -124,6 +150,45 @@ __device__ __forceinline__ Piece locate_piece(long long it, long long end, long 
   return pc;
 }
 
+// Walks the tiles of a pair's range in order: kv counts tiles from 0, i is
+// the index inside the current piece, piece counts pieces from 0.
+struct TileCursor {
+  long long it, end, T_all;
+  const int32_t* prefix;
+  const int32_t* tiles;
+  int B;
+  Piece pc;
+  int i, piece;
+  uint32_t kv;
+  __device__ void init(long long b, long long e, long long T, const int32_t* pf, const int32_t* tl,
+                       int nb) {
+    it = b;
+    end = e;
+    T_all = T;
+    prefix = pf;
+    tiles = tl;
+    B = nb;
+    i = 0;
+    piece = 0;
+    kv = 0;
+    if (it < end) pc = locate_piece(it, end, T_all, prefix, tiles, B);
+  }
+  __device__ bool valid() const { return it < end; }
+  __device__ bool first() const { return i == 0; }
+  __device__ bool last() const { return i == pc.n_tiles - 1; }
+  __device__ int tile() const { return pc.t_first + i; }
+  __device__ void next() {
+    ++it;
+    ++i;
+    ++kv;
+    if (i == pc.n_tiles) {
+      i = 0;
+      ++piece;
+      if (it < end) pc = locate_piece(it, end, T_all, prefix, tiles, B);
+    }
+  }
+};
+
 // 2^x with the hardware ex2 unit (max relative error about 2^-22); 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -131,98 +196,223 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void note_timeout(TcSmem& sm, uint32_t* err) {
+__device__ __forceinline__ void note_timeout(PairSmem& sm, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
   set_error(err, MLA_DEVERR_TIMEOUT);
 }
 
-// Descriptors. Q and K tiles: K-major, 128 B rows, 8-row groups 1024 B apart.
-// Advancing K by 16 bf16 (32 B) inside a swizzle atom advances the start address.
-__device__ __forceinline__ uint64_t desc_kmajor(const void* chunk, uint32_t k_byte_off) {
-  return smem_desc(smem_u32(chunk) + k_byte_off, 16, 1024, kSwizzle128B);
-}
-// C^T as an MN-major operand: latent dims are contiguous (64 per 128 B row, next
-// 64 dims one box = 8192 B further), tokens step 128 B, 8-token groups 1024 B apart.
-__device__ __forceinline__ uint64_t desc_ct(const void* chunk, uint32_t token_byte_off) {
-  return smem_desc(smem_u32(chunk) + token_byte_off, CHUNK_BYTES, 1024, kSwizzle128B);
+__device__ __forceinline__ bool aborted(PairSmem& sm) {
+  return *reinterpret_cast<volatile int*>(&sm.abort_flag) != 0;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1)
-attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                 const __grid_constant__ CUtensorMap tmap_kv, TcArgs a) {
+// Partial score (already in log2 units) -> fp16, round to nearest. Scores
+// beyond the fp16 range saturate to +-65504 instead of becoming inf.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_half2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
+
+// Byte offset of 16-byte unit u (0..7) of query row `row` in an exchange buffer.
+__device__ __forceinline__ uint32_t xoff(int row, int u) {
+  return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) * 16));
+}
+
+// What a softmax thread needs to ship its partial scores to the peer CTA.
+struct SendCtx {
+  uint32_t tmem, lane_base;
+  int row, lane, gtid;
+  uint32_t xbuf_peer[2], xfull_peer[2];
+};
+
+// Reads this CTA's partial scores of tile kv from TMEM (query row `row`, all
+// 64 tokens; the queries carry scale * log2(e), so these are in log2 units),
+// rounds them to fp16 into h and into the staging buffer kv & 1. Once the
+// group's four warps have staged theirs, one thread bulk-copies the 16 KB to
+// the peer's exchange buffer kv & 1 (the TMA engine moves it, so no thread
+// stalls on the cluster network). Returns true if a wait timed out.
+__device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uint32_t kv,
+                                             uint32_t (&h)[32]) {
+  const int sb = kv & 1;
+  bool bad = !mbar_wait(&sm.s_full[sb], (kv >> 1) & 1, WAIT_LIMIT);
+  tc_fence_after();
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float v[16];
+    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 * sb + 16 * q, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[8 * q + k] = pack_half2(v[2 * k], v[2 * k + 1]);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(&sm.s_empty[sb]);
+  // The staging buffer and the peer's exchange buffer are free once the
+  // peer has consumed tile kv - 2 (the bulk copy had finished reading then).
+  if (kv >= 2) bad |= !mbar_wait(&sm.x_sendok[sb], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
+  uint8_t* st = reinterpret_cast<uint8_t*>(sm.sbuf[sb]);
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<uint4*>(st + xoff(c.row, u)) =
+        make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(&sm.sready[sb]);
+  if (c.gtid == 0) {
+    mbar_arrive_expect_tx(&sm.x_full[sb], X_BYTES);
+    bad |= !mbar_wait(&sm.sready[sb], (kv >> 1) & 1, WAIT_LIMIT);
+    if (!bad) bulk_copy_to_peer(c.xbuf_peer[sb], st, X_BYTES, c.xfull_peer[sb]);
+  }
+  return bad;
+}
+
+// Group 0 puts this CTA's Q latent columns 128..255 of the piece's 128 query
+// rows into TMEM (bf16 pairs, row per lane), where the score MMAs read them
+// as their A operand, once the previous piece's score MMAs are done with
+// them. Rows past the end of the queries are zero. Returns true on timeout.
+__device__ __forceinline__ bool load_q_tmem(PairSmem& sm, const PairArgs& a, uint32_t tmem,
+                                            uint32_t lane_base, int row, int lane, uint32_t rank,
+                                            const TileCursor& cur) {
+  bool bad = false;
+  if (cur.piece > 0) bad = !mbar_wait(&sm.q_empty, (cur.piece - 1) & 1, WAIT_LIMIT);
+  tc_fence_after();
+  const long long grow =
+      static_cast<long long>(cur.pc.b) * a.n_q * a.n_h + cur.pc.g * TP_ROWS + row;
+  const uint4* src = reinterpret_cast<const uint4*>(a.qabs + grow * 576 + 256 * rank + 128);
+  const bool in = grow < a.q_rows;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 v = in ? src[4 * j + u] : make_uint4(0, 0, 0, 0);
+      w[4 * u] = v.x;
+      w[4 * u + 1] = v.y;
+      w[4 * u + 2] = v.z;
+      w[4 * u + 3] = v.w;
+    }
+    tmem_st16u(tmem + lane_base + TM_Q + 16 * j, w);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sm.q_full);
+  return bad;
+}
+
+__global__ void __launch_bounds__(TP_THREADS, 1)
+attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
+                 const __grid_constant__ CUtensorMap tmap_qr,
+                 const __grid_constant__ CUtensorMap tmap_kc,
+                 const __grid_constant__ CUtensorMap tmap_kr, PairArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem& sm = *reinterpret_cast<TcSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                          ~static_cast<uintptr_t>(1023));
+  PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int pair = static_cast<int>(cluster_id_x());
   const long long T_all = a.prefix[a.B];
   const long long N = T_all * a.G;
+  // Both CTAs of a pair see the same range, so they leave here together.
   if (N == 0) return;
-  const long long it_begin = range_begin(blockIdx.x, N, a.C);
-  const long long it_end = range_begin(blockIdx.x + 1, N, a.C);
+  const long long it_begin = range_begin(pair, N, a.P);
+  const long long it_end = range_begin(pair + 1, N, a.P);
   if (it_begin == it_end) return;
   const int rows_total = a.n_q * a.n_h;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_STAGES; ++s) {
+    for (int s = 0; s < TP_STAGES; ++s) {
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_full, 1 + TP_GRP_WARPS);  // TMA bytes + the TMEM loader warps
+    mbar_init(&sm.q_empty, 2);  // one commit from each score-MMA issuer
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], TC_SM_THREADS / 32);
+      mbar_init(&sm.s_empty[i], TP_GRP_WARPS);
+      mbar_init(&sm.x_full[i], 1);
+      mbar_init(&sm.x_sendok[i], TP_GRP_WARPS);
+      mbar_init(&sm.p_full[i], TP_GRP_WARPS);
+      mbar_init(&sm.pv_done[i], 1);
+      mbar_init(&sm.m_ready[i], TP_GRP_WARPS);
+      mbar_init(&sm.stats[i], TP_SM_WARPS);
+      mbar_init(&sm.sready[i], TP_GRP_WARPS);
     }
-    mbar_init(&sm.p_full, 1);
-    mbar_init(&sm.p_empty, 1);
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, 1);
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.o_empty, TP_GRP_WARPS);
+    for (int i = 0; i < 3; ++i) mbar_init(&sm.drain[i], 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers exist before either arrives remotely
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tmap(&tmap_q);
-      prefetch_tmap(&tmap_kv);
+      prefetch_tmap(&tmap_qc);
+      prefetch_tmap(&tmap_qr);
+      prefetch_tmap(&tmap_kc);
+      prefetch_tmap(&tmap_kr);
       const uint64_t pol = policy_evict_first();
+      const int xr = 512 + 32 * static_cast<int>(rank);
       uint32_t kv_it = 0;
       int piece_idx = 0;
-      uint32_t issued[TC_STAGES] = {0, 0};  // loads issued per stage
-      for (long long it = it_begin; it < it_end && !*reinterpret_cast<volatile int*>(&sm.abort_flag);) {
+      uint32_t issued[TP_STAGES] = {0, 0, 0};
+      bool stop = false;
+      for (long long it = it_begin; it < it_end && !stop && !aborted(sm);) {
         const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
         if (piece_idx > 0 && !mbar_wait(&sm.q_empty, (piece_idx - 1) & 1, WAIT_LIMIT)) {
           note_timeout(sm, a.err);
           break;
         }
-        mbar_arrive_expect_tx(&sm.q_full, TILE_BYTES);
-        const int qrow0 = pc.b * rows_total + pc.g * a.RG;
-        for (int c = 0; c < TC_KCH; ++c) tma_load_2d(sm.q[c], &tmap_q, 64 * c, qrow0, &sm.q_full);
+        const int qrow0 = pc.b * rows_total + pc.g * TP_ROWS;
+        mbar_arrive_expect_tx(&sm.q_full, Q_BYTES);
+        if (a.chunked) {
+          tma_load_3d(sm.qc[0], &tmap_qc, 0, qrow0, 4 * static_cast<int>(rank), &sm.q_full);
+        } else {
+          for (int j = 0; j < 2; ++j)
+            tma_load_2d(sm.qc[j], &tmap_qc, 256 * static_cast<int>(rank) + 64 * j, qrow0,
+                        &sm.q_full);
+        }
+        tma_load_2d(sm.qr, &tmap_qr, xr, qrow0, &sm.q_full);
+        const int32_t* pt = a.page_table + static_cast<size_t>(pc.b) * a.max_blocks;
+        int page_next = pt[pc.t_first];
         for (int t = pc.t_first; t < pc.t_first + pc.n_tiles; ++t) {
-          const int s = kv_it % TC_STAGES;
-          const uint32_t n = kv_it / TC_STAGES;
-          if (kv_it >= TC_STAGES && !mbar_wait(&sm.kv_empty[s], (n - 1) & 1, WAIT_LIMIT)) {
+          int page = page_next;
+          if (t + 1 < pc.t_first + pc.n_tiles) page_next = pt[t + 1];
+          const int s = kv_it % TP_STAGES;
+          const uint32_t n = kv_it / TP_STAGES;
+          if (kv_it >= TP_STAGES && !mbar_wait(&sm.kv_empty[s], (n - 1) & 1, WAIT_LIMIT)) {
             note_timeout(sm, a.err);
+            stop = true;
             break;
           }
-          int page = a.page_table[static_cast<size_t>(pc.b) * a.max_blocks + t];
           if (page < 0 || page >= a.num_blocks) {
             set_error(a.err, MLA_DEVERR_PAGE_RANGE);
             page = 0;
           }
-          mbar_arrive_expect_tx(&sm.kv_full[s], TILE_BYTES);
-          for (int c = 0; c < TC_KCH; ++c)
-            tma_load_2d_hint(sm.kv[s][c], &tmap_kv, 64 * c, page * TC_TOK, &sm.kv_full[s], pol);
+          mbar_arrive_expect_tx(&sm.kv_full[s], STAGE_BYTES);
+          if (a.chunked) {
+            tma_load_3d_hint(sm.kv[s].c[0], &tmap_kc, 0, page * TP_TOK,
+                             4 * static_cast<int>(rank), &sm.kv_full[s], pol);
+          } else {
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d_hint(sm.kv[s].c[j], &tmap_kc, 256 * static_cast<int>(rank) + 64 * j,
+                               page * TP_TOK, &sm.kv_full[s], pol);
+          }
+          tma_load_2d_hint(sm.kv[s].r, &tmap_kr, xr, page * TP_TOK, &sm.kv_full[s], pol);
           ++issued[s];
           ++kv_it;
         }
@@ -230,388 +420,491 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         it += pc.n_tiles;
       }
       // Never leave a TMA write in flight past the end of the CTA.
-      for (int s = 0; s < TC_STAGES; ++s)
+      for (int s = 0; s < TP_STAGES; ++s)
         if (issued[s] > 0) mbar_wait(&sm.kv_full[s], (issued[s] - 1) & 1, WAIT_LIMIT);
       if (piece_idx > 0) mbar_wait(&sm.q_full, (piece_idx - 1) & 1, WAIT_LIMIT);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ value-MMA issuer
+    // O (this CTA's 256 latent columns) += P C, with P read from TMEM.
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(TC_ROWS, TC_TOK, false, false);
-      const uint32_t idPV = idesc_bf16_f32(128, a.RG, true, false);
-      // Descriptor bases. Offsets inside the buffers are added to the
-      // start-address field (bits 0-13, in 16-byte units); shared addresses
-      // stay below 2^18 bytes, so the field never overflows.
-      const uint64_t dQ = desc_kmajor(sm.q[0], 0);
-      const uint64_t dP = desc_kmajor(sm.p, 0);
-      uint64_t dK[TC_STAGES], dC[TC_STAGES];
-      for (int s2 = 0; s2 < TC_STAGES; ++s2) {
-        dK[s2] = desc_kmajor(sm.kv[s2][0], 0);
-        dC[s2] = desc_ct(sm.kv[s2][0], 0);
-      }
-      uint32_t kv_it = 0;
-      int piece_idx = 0;
-      bool pend = false, pend_first = false, pend_last = false;
-      uint32_t pend_it = 0;
-      int pend_piece = 0;
+      const uint32_t idPV = idesc_bf16_f32(128, 256, false, true);
+      // C as the MN-major B operand: latent columns are contiguous (64 per
+      // 128-byte row, the next 64 one box further), tokens step 128 B,
+      // 8-token groups are 1024 B apart.
+      uint64_t dC[TP_STAGES];
+      for (int s = 0; s < TP_STAGES; ++s)
+        dC[s] = smem_desc(smem_u32(sm.kv[s].c[0]), KC_BOX, 1024, kSwizzle128B);
       bool ok = true;
-
-      auto issue_pv = [&](uint32_t pit, bool first, bool last, int ppiece) -> bool {
-        if (!mbar_wait(&sm.p_full, pit & 1, WAIT_LIMIT)) return false;
-        if (first && ppiece > 0 && !mbar_wait(&sm.o_empty, (ppiece - 1) & 1, WAIT_LIMIT))
-          return false;
-        tc_fence_after();
-        const int s2 = pit % TC_STAGES;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = dC[s2] + ((2 * j * CHUNK_BYTES + kk * 2048) >> 4);
-            const uint64_t bd = dP + ((kk * 32) >> 4);
-            mma_bf16_ss(tmem + TM_O + 64 * j, ad, bd, idPV, (first && kk == 0) ? 0u : 1u);
-          }
+      TileCursor cur;
+      cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
+      for (; cur.valid() && ok; cur.next()) {
+        const uint32_t t = cur.kv;
+        if (!mbar_wait(&sm.p_full[t & 1], (t >> 1) & 1, WAIT_LIMIT)) { ok = false; break; }
+        if (cur.first() && cur.piece > 0 &&
+            !mbar_wait(&sm.o_empty, (cur.piece - 1) & 1, WAIT_LIMIT)) {
+          ok = false;
+          break;
         }
-        mma_commit(&sm.kv_empty[s2]);
-        mma_commit(&sm.p_empty);
-        if (last) mma_commit(&sm.o_full);
-        return true;
-      };
-
-      for (long long it = it_begin; it < it_end && ok;) {
-        const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
-        if (!mbar_wait(&sm.q_full, piece_idx & 1, WAIT_LIMIT)) { ok = false; break; }
         tc_fence_after();
-        for (int i = 0; i < pc.n_tiles; ++i) {
-          const int sb = kv_it & 1;
-          if (kv_it >= 2 && !mbar_wait(&sm.s_empty[sb], ((kv_it >> 1) - 1) & 1, WAIT_LIMIT)) {
+        const int s = t % TP_STAGES;
+        const uint32_t pcol = tmem + TM_P + 32 * (t & 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ts(tmem + TM_O, pcol + 8 * kk, dC[s] + ((2048u * kk) >> 4), idPV,
+                      (cur.first() && kk == 0) ? 0u : 1u);
+        mma_commit(&sm.kv_empty[s]);
+        mma_commit(&sm.pv_done[t & 1]);
+        if (cur.last()) mma_commit(&sm.o_full);
+      }
+      if (!ok) note_timeout(sm, a.err);
+      // Every MMA issued above completes before TMEM is freed.
+      mma_commit(&sm.drain[0]);
+      mbar_wait(&sm.drain[0], 0, WAIT_LIMIT);
+    }
+  } else if (warp >= 2 + TP_SM_WARPS) {
+    // ------------------------------------------------------------ score-MMA issuers
+    // Warp 10 issues the score MMAs of even tiles, warp 11 those of odd
+    // tiles, so two threads hide each other's issue latency. Each owns one
+    // TMEM score buffer.
+    if (lane == 0) {
+      const uint32_t par = static_cast<uint32_t>(warp - 2 - TP_SM_WARPS);  // 0 or 1
+      const uint32_t idS = idesc_bf16_f32(128, TP_TOK, false, false);
+      const uint64_t dQc = smem_desc(smem_u32(sm.qc[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dQr = smem_desc(smem_u32(sm.qr), 16, 512, kSwizzle64B);
+      uint64_t dKc[TP_STAGES], dKr[TP_STAGES];
+      for (int s = 0; s < TP_STAGES; ++s) {
+        dKc[s] = smem_desc(smem_u32(sm.kv[s].c[0]), 16, 1024, kSwizzle128B);
+        dKr[s] = smem_desc(smem_u32(sm.kv[s].r), 16, 512, kSwizzle64B);
+      }
+      const uint32_t dS = tmem + TM_S + 64 * par;
+      bool ok = true;
+      TileCursor cur;
+      cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
+      while (cur.valid() && ok) {
+        // one piece: wait for its Q, issue this thread's tiles, release Q
+        if (!mbar_wait(&sm.q_full, cur.piece & 1, WAIT_LIMIT)) { ok = false; break; }
+        tc_fence_after();
+        const int piece = cur.piece;
+        for (; cur.valid() && cur.piece == piece; cur.next()) {
+          const uint32_t t = cur.kv;
+          if ((t & 1) != par) continue;
+          if (t >= 2 && !mbar_wait(&sm.s_empty[par], ((t >> 1) - 1) & 1, WAIT_LIMIT)) {
             ok = false;
             break;
           }
-          const int s2 = kv_it % TC_STAGES;
-          if (!mbar_wait(&sm.kv_full[s2], (kv_it / TC_STAGES) & 1, WAIT_LIMIT)) {
-            ok = false;
-            break;
-          }
+          const int s = t % TP_STAGES;
+          if (!mbar_wait(&sm.kv_full[s], (t / TP_STAGES) & 1, WAIT_LIMIT)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4 * TC_KCH; ++k) {
-            const uint32_t off = ((k >> 2) * CHUNK_BYTES + (k & 3) * 32) >> 4;
-            mma_bf16_ss(tmem + TM_S + 64 * sb, dQ + off, dK[s2] + off, idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 16; ++k) {
+            const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+            if (k < 8) {  // Q from shared memory
+              const uint32_t off = (QC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+              mma_bf16_ss(dS, dQc + off, dKc[s] + koff, idS, k > 0 ? 1u : 0u);
+            } else {      // Q from TMEM
+              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc[s] + koff, idS, 1u);
+            }
           }
-          mma_commit(&sm.s_full[sb]);
-          if (i == pc.n_tiles - 1) mma_commit(&sm.q_empty);
-          if (pend && !issue_pv(pend_it, pend_first, pend_last, pend_piece)) {
-            ok = false;
-            break;
-          }
-          pend = true;
-          pend_it = kv_it;
-          pend_first = (i == 0);
-          pend_last = (i == pc.n_tiles - 1);
-          pend_piece = piece_idx;
-          ++kv_it;
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr[s] + ((32u * k) >> 4), idS, 1u);
+          mma_commit(&sm.s_full[par]);
         }
-        ++piece_idx;
-        it += pc.n_tiles;
+        if (!ok) break;
+        mma_commit(&sm.q_empty);
       }
-      if (ok && pend && !issue_pv(pend_it, pend_first, pend_last, pend_piece)) ok = false;
       if (!ok) note_timeout(sm, a.err);
-      // Wait until every MMA issued above has completed before TMEM is freed.
-      mma_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, WAIT_LIMIT);
+      mma_commit(&sm.drain[1 + par]);
+      mbar_wait(&sm.drain[1 + par], 0, WAIT_LIMIT);
     }
   } else {
     // ------------------------------------------------------------ softmax warps 2..9
-    // A failed (timed-out) wait only sets `bad`. Every thread still passes
-    // every named barrier, and the group leaves the loop together at the
-    // end-of-tile barrier, so no barrier can be left half-filled.
-    const int qd = warp & 3;                   // TMEM lane quarter this warp may access
-    const int hf = (warp - 2) >> 2;            // score column half: [32*hf, 32*hf + 32)
+    // Group g = (w - 2) / 4 handles the tiles with kv % 2 == g, so one group's
+    // exchange and softmax overlap the other's. Warp w reads TMEM lane quarter
+    // w % 4: query rows 32 (w % 4) .. +31, one row per lane, all 64 tokens.
+    // The running row max is handed from tile to tile through shared memory
+    // (mrow, m_ready). Each group keeps its own row sum, referred to the max
+    // it last used; the epilogue merges the two.
+    const int grp = (warp - 2) >> 2;
+    const int qd = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
-    const int row = 16 * qd + lane;            // score row held by this lane (lane < 16)
-    const bool lane_has_row = lane < 16;
-    const int tid_sm = threadIdx.x - 64;       // 0..255
-    uint32_t kv_it = 0;
-    int piece_idx = 0;
-    bool abort = false;
-    for (long long it = it_begin; it < it_end && !abort;) {
-      const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
-      const int L = a.seq_lens[pc.b];
-      const int rg = pc.g * a.RG + row;
-      const int rows_valid = min(a.RG, rows_total - pc.g * a.RG);
-      const bool row_ok = lane_has_row && row < rows_valid;
-      const int pos_q = L - a.n_q + (row_ok ? rg / a.n_h : 0);
-      float m = -INFINITY, l = 0.f;  // m: running max (shared by both halves); l: this half
-
-      for (int i = 0; i < pc.n_tiles && !abort; ++i) {
-        bool bad = false;
-        const int t = pc.t_first + i;
-        const int sb = kv_it & 1;
-        const int s2 = kv_it % TC_STAGES;
-        bad |= !mbar_wait(&sm.s_full[sb], (kv_it >> 1) & 1, WAIT_LIMIT);
-        tc_fence_after();
-        float sc[32];
-        {
-          float v[16];
-          tmem_ld16(tmem + lane_base + TM_S + 64 * sb + 32 * hf, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) sc[k] = v[k];
-          tmem_ld16(tmem + lane_base + TM_S + 64 * sb + 32 * hf + 16, v);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) sc[16 + k] = v[k];
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
-
-        const int j0 = t * TC_TOK + 32 * hf;  // token of sc[0]
-        if (row_ok && j0 + 31 <= L - a.n_q) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) sc[c] *= a.scale_log2;
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] * a.scale_log2 : -INFINITY;
-        }
-        float pm[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          pm[u] = fmaxf(fmaxf(sc[4 * u], sc[4 * u + 1]), fmaxf(sc[4 * u + 2], sc[4 * u + 3]));
-        const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-        const bool first = (i == 0);
-        if (lane_has_row) sm.xmax[hf][row] = pmax;
-        // One barrier: publishes both halves' maxima and tells everyone
-        // whether any row must rescale (or any wait failed).
-        const bool flag = bad || (!first && row_ok && pmax > m + RESCALE_THRESHOLD);
-        const bool any = named_bar_or(1, TC_SM_THREADS, flag);
-        const float m_new =
-            lane_has_row ? fmaxf(m, fmaxf(sm.xmax[0][row], sm.xmax[1][row])) : -INFINITY;
-        const bool need = !first && row_ok && (m_new > m + RESCALE_THRESHOLD);
-        const float m_use = (first || need) ? m_new : m;
-        const float alpha = (m == -INFINITY || first) ? 0.f : fast_exp2(m - m_use);
-        // A row with nothing visible yet keeps m_use = -inf; subtracting 0
-        // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
-        const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-
-        // P buffer free and O^T stable once the previous value MMA has finished.
-        if (kv_it > 0) bad |= !mbar_wait(&sm.p_empty, (kv_it - 1) & 1, WAIT_LIMIT);
-        tc_fence_after();
-        if (any) {
-          if (named_bar_or(1, TC_SM_THREADS, bad)) {
-            abort = true;
-          } else {
-            if (hf == 0 && lane_has_row) sm.row_alpha[row] = need ? alpha : 1.f;
-            named_bar_sync(1, TC_SM_THREADS);
-            for (int j = 2 * hf; j < 2 * hf + 2; ++j) {
-              for (int c0 = 0; c0 < a.RG; c0 += 16) {
-                float v[16];
-                const uint32_t ta = tmem + lane_base + TM_O + 64 * j + c0;
-                tmem_ld16(ta, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] *= sm.row_alpha[c0 + k];
-                tmem_st16(ta, v);
-              }
-            }
-            tmem_wait_st();
-          }
-        }
-        // P half-row -> shared memory (bf16, 128B-swizzled K-major)
-        if (lane_has_row && !abort) {
-          float psum = 0.f;
-          uint8_t* prow = sm.p + row * 128;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float x0 = sc[ch * 8 + 2 * k], x1 = sc[ch * 8 + 2 * k + 1];
-              const float p0 = fast_exp2(x0 - m_sub), p1 = fast_exp2(x1 - m_sub);
-              const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-              psum += __low2float(pb) + __high2float(pb);
-              w[k] = *reinterpret_cast<const uint32_t*>(&pb);
-            }
-            const int unit = 4 * hf + ch;
-            *reinterpret_cast<uint4*>(prow + ((unit ^ (row & 7)) * 16)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          if (row_ok) {
-            l = l * alpha + psum;
-            m = m_use;
-          }
-        }
-        // Rows past the end of the sequence may hold anything; zero their
-        // latent columns so that 0 * garbage cannot reach the accumulator.
-        const int jt = t * TC_TOK;
-        if (!abort && jt + TC_TOK > L) {
-          const int r0 = L - jt;  // first invalid row in this tile
-          const int nrow = TC_TOK - r0;
-          for (int i2 = tid_sm; i2 < nrow * 8 * 8; i2 += TC_SM_THREADS) {
-            const int rr = r0 + i2 / 64, ch = (i2 / 8) % 8, u = i2 % 8;
-            *reinterpret_cast<uint4*>(sm.kv[s2][ch] + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (named_bar_or(1, TC_SM_THREADS, bad)) abort = true;
-        if (tid_sm == 0 && !abort) mbar_arrive(&sm.p_full);
-        ++kv_it;
+    const int row = 32 * qd + lane;
+    const int gtid = ((warp - 2) & 3) * 32 + lane;  // 0..127 inside the group
+    const SendCtx sx{tmem, lane_base, row, lane, gtid,
+                     {mapa_shared(smem_u32(sm.xbuf[0]), peer),
+                      mapa_shared(smem_u32(sm.xbuf[1]), peer)},
+                     {mapa_shared(smem_u32(&sm.x_full[0]), peer),
+                      mapa_shared(smem_u32(&sm.x_full[1]), peer)}};
+    const uint32_t xsendok_peer[2] = {mapa_shared(smem_u32(&sm.x_sendok[0]), peer),
+                                      mapa_shared(smem_u32(&sm.x_sendok[1]), peer)};
+    TileCursor cur;
+    cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
+    float l = 0.f, mref = -INFINITY;  // this group's row sum and the max it refers to
+    int L = 0, rows_valid = 0, pos_q = 0;
+    bool row_ok = false, bad = false;
+    for (; cur.valid() && !bad; cur.next()) {
+      const uint32_t kv = cur.kv;
+      const bool first = cur.first();
+      if (first) {
+        l = 0.f;
+        mref = -INFINITY;
+        L = a.seq_lens[cur.pc.b];
+        rows_valid = min(TP_ROWS, rows_total - cur.pc.g * TP_ROWS);
+        row_ok = row < rows_valid;
+        pos_q = L - a.n_q + (row_ok ? (cur.pc.g * TP_ROWS + row) / a.n_h : 0);
+        if (grp == 0) bad |= load_q_tmem(sm, a, tmem, lane_base, row, lane, rank, cur);
       }
-      if (abort) break;
+      if ((kv & 1) != static_cast<uint32_t>(grp)) {
+        // The other group's tile. At the end of a piece, hand over this
+        // group's row sums, once that tile has published its max: this keeps
+        // the two groups at most one piece apart, which the two stats
+        // barriers (one per piece parity) rely on.
+        if (cur.last()) {
+          bad |= !mbar_wait(&sm.m_ready[kv & 1], (kv >> 1) & 1, WAIT_LIMIT);
+          sm.st_l[grp][row] = l;
+          sm.st_m[grp][row] = mref;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
+        }
+        continue;
+      }
+      const int t = cur.tile();
+      const int s2 = kv % TP_STAGES;
+      uint32_t own[32];
+      bad |= send_partial(sm, sx, kv, own);
 
-      // ---- epilogue of the piece: O^T / l -> workspace slot
-      bool bad = !mbar_wait(&sm.o_full, piece_idx & 1, WAIT_LIMIT);
+      // 1. full scaled scores = own partial + the peer's (both fp16-rounded)
+      const int xb = kv & 1;
+      bad |= !mbar_wait(&sm.x_full[xb], (kv >> 1) & 1, WAIT_LIMIT);
+      float sc[64];
+      {
+        const uint8_t* xin = reinterpret_cast<const uint8_t*>(sm.xbuf[xb]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 pv = *reinterpret_cast<const uint4*>(xin + xoff(row, u));
+          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float2 x0 = unpack_half2(own[4 * u + w]), x1 = unpack_half2(pw[w]);
+            sc[8 * u + 2 * w] = x0.x + x1.x;
+            sc[8 * u + 2 * w + 1] = x0.y + x1.y;
+          }
+        }
+      }
+      __syncwarp();
+      // At the end of a piece the epilogue borrows this exchange buffer, so
+      // the peer may only refill it afterwards.
+      if (lane == 0 && !cur.last()) mbar_arrive_remote_relaxed(xsendok_peer[xb]);
+
+      // 2. causal mask, row max
+      const int j0 = t * TP_TOK;  // token of sc[0]
+      if (!(row_ok && j0 + TP_TOK - 1 <= L - a.n_q)) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] : -INFINITY;
+      }
+      float pm[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        pm[u] = fmaxf(fmaxf(fmaxf(sc[8 * u], sc[8 * u + 1]), fmaxf(sc[8 * u + 2], sc[8 * u + 3])),
+                      fmaxf(fmaxf(sc[8 * u + 4], sc[8 * u + 5]), fmaxf(sc[8 * u + 6], sc[8 * u + 7])));
+      }
+      const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      // 3. running max from the previous tile (the other group's)
+      if (kv > 0) bad |= !mbar_wait(&sm.m_ready[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+      const float m_prev = first ? -INFINITY : sm.mrow[(kv - 1) & 1][row];
+      const float m_new = fmaxf(m_prev, pmax);
+      const bool need = !first && row_ok && (m_new > m_prev + RESCALE_THRESHOLD);
+      const float m_use = (first || need) ? m_new : m_prev;
+      sm.mrow[kv & 1][row] = m_use;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.m_ready[kv & 1]);
+      // A row with nothing visible yet keeps m_use = -inf; subtracting 0
+      // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
+      const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
+
+      // 4. lazy rescale of this warp's rows of O
+      if (__any_sync(0xffffffffu, need)) {
+        bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+        tc_fence_after();
+        if (!__any_sync(0xffffffffu, bad)) {
+          const float f = need ? fast_exp2(m_prev - m_use) : 1.f;
+          for (int c0 = 0; c0 < 256; c0 += 16) {
+            float v[16];
+            const uint32_t ta = tmem + lane_base + TM_O + c0;
+            tmem_ld16(ta, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] *= f;
+            tmem_st16(ta, v);
+          }
+          tmem_wait_st();
+        }
+      }
+
+      // 5. P (bf16 pairs) into its TMEM buffer, once the value MMA two tiles
+      // back has read that buffer
+      if (kv >= 2) bad |= !mbar_wait(&sm.pv_done[kv & 1], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
       tc_fence_after();
-      if (hf == 1 && lane_has_row) sm.xsum[row] = l;
-      if (named_bar_or(1, TC_SM_THREADS, bad)) {
-        abort = true;
-        break;
-      }
-      const int slot = blockIdx.x + pc.g * a.B + pc.b;
-      if (hf == 0 && lane_has_row) {
-        const float lt = l + sm.xsum[row];
-        sm.row_inv_l[row] = (row_ok && lt > 0.f) ? 1.f / lt : 0.f;
-        if (row_ok)
-          a.part_lse[static_cast<size_t>(slot) * a.RG + row] =
-              lt > 0.f ? (m + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-      }
-      named_bar_sync(1, TC_SM_THREADS);
-      float* dst = a.part_o + static_cast<size_t>(slot) * a.RG * 512;
-      for (int j = 2 * hf; j < 2 * hf + 2; ++j) {
-        for (int c0 = 0; c0 < a.RG; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + TM_O + 64 * j + c0, v);
-          tmem_wait_ld();
+      {
+        float psum = 0.f;
+        uint32_t w[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int n = c0 + k;
-            if (n < rows_valid) dst[static_cast<size_t>(n) * 512 + 128 * j + 32 * qd + lane] =
-                v[k] * sm.row_inv_l[n];
+            const float p0 = fast_exp2(sc[32 * hh + 2 * k] - m_sub);
+            const float p1 = fast_exp2(sc[32 * hh + 2 * k + 1] - m_sub);
+            psum += p0 + p1;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            w[k] = *reinterpret_cast<const uint32_t*>(&pb);
           }
+          if (!__any_sync(0xffffffffu, bad))
+            tmem_st16u(tmem + lane_base + TM_P + 32 * (kv & 1) + 16 * hh, w);
+        }
+        tmem_wait_st();
+        if (row_ok) {
+          l = (mref == -INFINITY) ? psum : l * fast_exp2(mref - m_use) + psum;
+          mref = m_use;
         }
       }
+      // Rows past the end of the sequence may hold anything; zero their
+      // latent columns so that 0 * garbage cannot reach the accumulator.
+      const int jt = t * TP_TOK;
+      if (jt + TP_TOK > L) {
+        const int r0 = max(L - jt, 0);            // first invalid row in this tile
+        const int n16 = (TP_TOK - r0) * 4 * 8;    // rows x boxes x 16-byte units
+        for (int i2 = gtid; i2 < n16; i2 += TP_GRP_WARPS * 32) {
+          const int rr = r0 + i2 / 32, box = (i2 / 8) % 4, u = i2 % 8;
+          *reinterpret_cast<uint4*>(sm.kv[s2].c[box] + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
-      named_bar_sync(1, TC_SM_THREADS);
-      if (tid_sm == 0) mbar_arrive(&sm.o_empty);
-      ++piece_idx;
-      it += pc.n_tiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[kv & 1]);
+
+      if (cur.last()) {
+        // ---- epilogue of the piece (done by the group of its last tile):
+        // O / l -> workspace slot
+        sm.st_l[grp][row] = l;
+        sm.st_m[grp][row] = mref;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
+        bad |= !mbar_wait(&sm.stats[cur.piece & 1], (cur.piece >> 1) & 1, WAIT_LIMIT);
+        bad |= !mbar_wait(&sm.o_full, cur.piece & 1, WAIT_LIMIT);
+        tc_fence_after();
+        float lt = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          const float mg = sm.st_m[g2][row];
+          if (mg != -INFINITY) lt += sm.st_l[g2][row] * fast_exp2(mg - m_use);
+        }
+        const float inv_l = (row_ok && lt > 0.f) ? 1.f / lt : 0.f;
+        const int slot = pair + cur.pc.g * a.B + cur.pc.b;
+        if (rank == 0 && row_ok)
+          a.part_lse[static_cast<size_t>(slot) * TP_ROWS + row] =
+              lt > 0.f ? (m_use + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+        // O / l goes out 32 columns at a time through this warp's 4 KB of
+        // the (already consumed) exchange buffer: each lane writes its row,
+        // then the warp stores one 128-byte row segment per instruction.
+        if (!__any_sync(0xffffffffu, bad)) {
+          uint8_t* stg = reinterpret_cast<uint8_t*>(sm.xbuf[xb]) + qd * 4096;
+          float* dst0 = a.part_o + (static_cast<size_t>(slot) * TP_ROWS + 32 * qd) * 512 +
+                        256 * rank + lane;
+          for (int c0 = 0; c0 < 256; c0 += 32) {
+            float v[32];
+            tmem_ld16(tmem + lane_base + TM_O + c0, *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(tmem + lane_base + TM_O + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ (lane & 7)) * 16)) =
+                  make_float4(v[4 * u] * inv_l, v[4 * u + 1] * inv_l, v[4 * u + 2] * inv_l,
+                              v[4 * u + 3] * inv_l);
+            __syncwarp();
+            // All loads of a half before its stores: the compiler cannot prove
+            // that the staging buffer and the output do not alias, so mixing
+            // them would serialise every load behind the previous store.
+#pragma unroll
+            for (int r0 = 0; r0 < 32; r0 += 16) {
+              float x[16];
+#pragma unroll
+              for (int r = 0; r < 16; ++r)
+                x[r] = *reinterpret_cast<const float*>(
+                    stg + (r0 + r) * 128 + (((lane >> 2) ^ ((r0 + r) & 7)) * 16) + (lane & 3) * 4);
+#pragma unroll
+              for (int r = 0; r < 16; ++r)
+                if (32 * qd + r0 + r < rows_valid)
+                  dst0[static_cast<size_t>(r0 + r) * 512 + c0] = x[r];
+            }
+            __syncwarp();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.o_empty);
+          mbar_arrive_remote_relaxed(xsendok_peer[xb]);  // the exchange buffer is free again
+        }
+      }
     }
-    if (abort && tid_sm == 0) note_timeout(sm, a.err);
+    if (bad && lane == 0) note_timeout(sm, a.err);
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  // The peer may still address this CTA's shared memory (st.async stores,
+  // remote arrivals) until it reaches this barrier.
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, 512);
   }
 }
 
-// ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
+size_t smem_bytes() { return sizeof(PairSmem) + 1024; }
+
+bool set_smem_attr() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes())) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < 64) done[dev] = true;
+  return true;
 }
 
-bool encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {576, rows};
-  cuuint64_t strides[1] = {576 * 2};
-  cuuint32_t box[2] = {64, 64};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+bool rows_map(TmapSpec* sp, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle sw) {
+  *sp = TmapSpec{};
+  sp->dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  sp->rank = 2;
+  sp->base = base;
+  sp->dims[0] = 576;
+  sp->dims[1] = rows;
+  sp->strides[0] = 576 * 2;
+  sp->box[0] = box_cols;
+  sp->box[1] = box_rows;
+  sp->swizzle = sw;
+  return true;
 }
 
-// Tensor maps depend only on (base address, rows), so recent ones are kept.
-struct MapCache {
-  static constexpr int kSlots = 32;
-  struct Entry {
-    const void* base = nullptr;
-    uint64_t rows = 0;
-    CUtensorMap map;
-  } e[kSlots];
-  int next = 0;
-  std::mutex mu;
-};
-
-bool make_rows_map(CUtensorMap* m, const void* base, uint64_t rows) {
-  static MapCache cache;
-  std::lock_guard<std::mutex> lk(cache.mu);
-  for (auto& x : cache.e) {
-    if (x.base == base && x.rows == rows) {
-      *m = x.map;
-      return true;
-    }
-  }
-  if (!encode_rows_map(m, base, rows)) return false;
-  auto& slot = cache.e[cache.next];
-  cache.next = (cache.next + 1) % MapCache::kSlots;
-  slot.base = base;
-  slot.rows = rows;
-  slot.map = *m;
+// A [rows][576] bf16 matrix seen as 3-D: (64 columns of a chunk, rows, the
+// nine 64-column chunks). A box of (64, box_rows, n_chunks) lands in shared
+// memory as n_chunks consecutive [box_rows][64] tiles with 128-byte swizzle,
+// which is the layout of n_chunks separate 2-D boxes, in one TMA instruction.
+bool chunks_map(TmapSpec* sp, const void* base, uint64_t rows, uint32_t box_rows,
+                uint32_t n_chunks) {
+  *sp = TmapSpec{};
+  sp->dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  sp->rank = 3;
+  sp->base = base;
+  sp->dims[0] = 64;
+  sp->dims[1] = rows;
+  sp->dims[2] = 9;
+  sp->strides[0] = 576 * 2;
+  sp->strides[1] = 128;
+  sp->box[0] = 64;
+  sp->box[1] = box_rows;
+  sp->box[2] = n_chunks;
+  sp->swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
   return true;
 }
 
 }  // namespace
 
 bool attend_tc_supported(const Shape& s, mla_dtype dt) {
-  return dt == MLA_BF16 && s.d_c == 512 && s.d_r == 64 && s.bs == TC_TOK;
+  return dt == MLA_BF16 && s.d_c == 512 && s.d_r == 64 && s.bs == TP_TOK;
 }
 
-size_t attend_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+// Number of CTA pairs that can be resident at once (the attention grid is
+// that many clusters of two), or 0 if the kernel cannot be configured.
+int attend_tc_max_pairs() {
+  if (!set_smem_attr()) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(TP_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
 
 cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
                              const int32_t* page_table, int max_blocks, int B, int n_q,
                              const Partition& p, const WsView& ws, const int32_t* seq_lens,
                              uint32_t* err, cudaStream_t st) {
-  CUtensorMap tq, tkv;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * s.n_h;
-  if (!make_rows_map(&tq, ws.qabs, q_rows)) return cudaErrorInvalidValue;
-  if (!make_rows_map(&tkv, cache, static_cast<uint64_t>(num_blocks) * TC_TOK))
-    return cudaErrorInvalidValue;
-  TcArgs a;
+  const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * TP_TOK;
+  TmapSpec sp;
+  CUtensorMap tqc, tqr, tkc, tkr;
+  // One 3-D box per latent half; if the driver does not take that view,
+  // plain 2-D boxes of 64 columns.
+  bool chunked = true;
+  chunks_map(&sp, ws.qabs, q_rows, 128, 2);
+  if (!get_tmap(sp, &tqc)) chunked = false;
+  rows_map(&sp, ws.qabs, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!get_tmap(sp, &tqr)) return cudaErrorInvalidValue;
+  if (chunked) {
+    chunks_map(&sp, cache, kv_rows, 64, 4);
+    if (!get_tmap(sp, &tkc)) chunked = false;
+  }
+  if (!chunked) {
+    rows_map(&sp, ws.qabs, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!get_tmap(sp, &tqc)) return cudaErrorInvalidValue;
+    rows_map(&sp, cache, kv_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!get_tmap(sp, &tkc)) return cudaErrorInvalidValue;
+  }
+  rows_map(&sp, cache, kv_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!get_tmap(sp, &tkr)) return cudaErrorInvalidValue;
+  if (!set_smem_attr()) return cudaErrorInvalidValue;
+  PairArgs a;
   a.page_table = page_table;
   a.seq_lens = seq_lens;
   a.tiles = ws.tiles;
   a.prefix = ws.prefix;
   a.part_o = ws.part_o;
   a.part_lse = ws.part_lse;
+  a.qabs = static_cast<const __nv_bfloat16*>(ws.qabs);
+  a.q_rows = static_cast<long long>(q_rows);
+  a.chunked = chunked ? 1 : 0;
   a.err = err;
   a.num_blocks = num_blocks;
   a.max_blocks = max_blocks;
   a.B = B;
   a.n_q = n_q;
   a.n_h = s.n_h;
-  a.RG = p.RG;
   a.G = p.G;
-  a.C = p.C;
-  a.scale_log2 = s.scale * 1.4426950408889634f;
-  const size_t smem = attend_tc_smem_bytes();
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
-  }
-  attend_tc_kernel<<<p.C, TC_THREADS, smem, st>>>(tq, tkv, a);
-  return cudaGetLastError();
+  a.P = p.C;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.C, 1, 1);
+  cfg.blockDim = dim3(TP_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tqc, tqr, tkc, tkr, a);
 }
 
 }  // namespace mla

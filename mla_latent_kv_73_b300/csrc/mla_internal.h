@@ -22,12 +22,13 @@ struct Shape {
 //
 // The query rows of a sequence, r = i*n_h + h for query token i and head h,
 // are cut into G groups of RG rows. The cached tokens of sequence b form
-// tiles_b = ceil(L_b / TS) tiles. The attention grid of C CTAs splits the
-// flat list of work items (g, b, tile), ordered group-major, into C
-// contiguous ranges of near-equal length. One CTA's range therefore covers
-// pieces of several (g, b) pairs. The piece of CTA c on pair (g, b) writes
-// its partial result to slot c + g*B + b. The slots are unique, and
-// slots = C + G*B bound their number.
+// tiles_b = ceil(L_b / TS) tiles. The attention grid splits the flat list of
+// work items (g, b, tile), ordered group-major, into C contiguous ranges of
+// near-equal length: one per CTA (CUDA-core kernel) or per 2-CTA cluster
+// (tensor-core kernel). One range therefore covers pieces of several (g, b)
+// pairs. The piece of range c on pair (g, b) writes its partial result to
+// slot c + g*B + b. The slots are unique, and slots = C + G*B bound their
+// number.
 struct Partition {
   int RG, G, TS, C, slots;
 };
@@ -71,17 +72,23 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st);
 
+// out_scale multiplies q_lat and q_pe before they are rounded to the cache
+// dtype (the tensor-core attention folds scale * log2(e) in here).
 cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
                             const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                            const Partition& p, const WsView& ws, uint32_t* err, cudaStream_t st);
+                            const Partition& p, const WsView& ws, float out_scale, uint32_t* err,
+                            cudaStream_t st);
 
 cudaError_t launch_attend_simt(const Shape& s, mla_dtype dt, const void* cache, int num_blocks,
                                const int32_t* page_table, int max_blocks, int B, int n_q,
                                const Partition& p, const WsView& ws, const int32_t* seq_lens,
                                uint32_t* err, cudaStream_t st);
 
-// Tensor-core attention (bf16, d_c = 512, d_r = 64, block_size = 64).
+// Tensor-core attention (bf16, d_c = 512, d_r = 64, block_size = 64), one
+// 2-CTA cluster per work range; attend_tc_max_pairs() is how many clusters
+// fit on the current device at once (0 if none).
 bool attend_tc_supported(const Shape& s, mla_dtype dt);
+int attend_tc_max_pairs();
 cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
                              const int32_t* page_table, int max_blocks, int B, int n_q,
                              const Partition& p, const WsView& ws, const int32_t* seq_lens,
@@ -92,8 +99,8 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
 bool absorb_tc_supported(const Shape& s, mla_dtype dt);
 cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
                                const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                               const Partition& p, const WsView& ws, uint32_t* err,
-                               cudaStream_t st);
+                               const Partition& p, const WsView& ws, float out_scale,
+                               uint32_t* err, cudaStream_t st);
 bool combine_tc_supported(const Shape& s, mla_dtype dt);
 cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
                               const Partition& p, const WsView& ws, float* out, uint32_t* err,
@@ -104,6 +111,7 @@ cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const WsView& ws, float* out, cudaStream_t st);
 
 // Partition parameters for each attention kernel.
-Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms);
+// tc_pairs: CTA pairs resident at once for the tensor-core attention kernel.
+Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms, int tc_pairs);
 
 }  // namespace mla
