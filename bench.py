@@ -265,13 +265,20 @@ def run_ours(args, world, rank, local):
         step(s, st)
         pin_out.copy_(out, non_blocking=True)
 
-    # One CUDA graph per input set: a whole step; the attention kernel alone;
-    # a whole step with its host<->device copies.
-    g_step, g_att, g_e2e = [], [], []
+    # One CUDA graph per input set: a whole step; each of its four stages
+    # alone (the attention kernel is the roofline kernel); a whole step with
+    # its host<->device copies.
+    g_step, g_att, g_e2e, g_app, g_abs, g_cmb = [], [], [], [], [], []
     for s in sets:
         for lst, fn in ((g_step, lambda st, s=s: step(s, st)),
                         (g_att, lambda st, s=s: _lib.mla_decode_attend(
                             cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, st)),
+                        (g_app, lambda st, s=s: _lib.mla_append_kv(
+                            cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], st)),
+                        (g_abs, lambda st, s=s: _lib.mla_decode_absorb_q(
+                            cfg, s["w"].handle, s["q"], seq_lens, max_blocks, ws, st)),
+                        (g_cmb, lambda st, s=s: _lib.mla_decode_combine(
+                            cfg, s["w"].handle, seq_lens, B, n_q, out, ws, st)),
                         (g_e2e, lambda st, s=s: e2e_step(s, st))):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
@@ -319,6 +326,20 @@ def run_ours(args, world, rank, local):
         ev_b[i].record()
     torch.cuda.synchronize()
     attend_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(Ka)]
+
+    # the other three stages, timed the same way (launch by launch, cold sets)
+    def stage_us(graphs, n=200):
+        a_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        b_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            a_ev[i].record()
+            graphs[i % n_sets].replay()
+            b_ev[i].record()
+        torch.cuda.synchronize()
+        return round(1e3 * statistics.mean(a_ev[i].elapsed_time(b_ev[i]) for i in range(n)), 2)
+    stages = {"append": stage_us(g_app), "absorb_q": stage_us(g_abs),
+              "attend": round(1e3 * statistics.mean(attend_ms), 2), "combine": stage_us(g_cmb)}
 
     # end to end: pinned host inputs in, host result out, every step
     Ke = max(n_sets, K // 2)
@@ -393,6 +414,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke, "graph": True,
                 "no_graph_value": round(e2e_direct, 1)},
+        "stage_us": stages,
         "gpu_launches": 4 * K,
         "host_enqueue_us_per_step": round(host_us, 2),
         "clocks": clocks,

@@ -70,7 +70,7 @@ using namespace mla_ptx;
 
 constexpr int TP_ROWS = 128;                  // query rows per group (MMA M)
 constexpr int TP_TOK = 64;                    // tokens per tile = page size
-constexpr int TP_STAGES = 3;
+constexpr int TP_STAGES = 4;
 constexpr int TP_THREADS = 384;               // warp 0 TMA, 1 value MMA, 2..9 softmax, 10-11 score MMA
 constexpr int TP_SM_WARPS = 8;                // two softmax groups of four warps
 constexpr int TP_GRP_WARPS = 4;
@@ -81,7 +81,7 @@ constexpr uint32_t KR_BOX = 64 * 64;          // 64 tokens x 32 bf16
 constexpr uint32_t Q_BYTES = 2 * QC_BOX + QR_BOX;   // Q through TMA (the rest goes to TMEM)
 constexpr uint32_t STAGE_BYTES = 4 * KC_BOX + KR_BOX;
 constexpr uint32_t X_BYTES = TP_ROWS * TP_TOK * 2;  // fp16 partial scores
-constexpr uint32_t TM_S = 0;                  // score buffers at columns 0 and 64
+constexpr uint32_t TM_S = 0;                  // score slot: two K-half accumulators at 0 and 64
 constexpr uint32_t TM_P = 128;                // P buffers at columns 128 and 160
 constexpr uint32_t TM_Q = 192;                // Q latent columns 128..255 of this CTA (bf16 pairs)
 constexpr uint32_t TM_O = 256;                // latent accumulator, 256 columns
@@ -97,10 +97,9 @@ struct __align__(1024) PairSmem {
   } kv[TP_STAGES];
   // peer's partial scores, fp16 pairs: [buffer][row][64 tokens], 16-byte units swizzled
   uint32_t xbuf[2][TP_ROWS * TP_TOK / 2];
-  uint32_t sbuf[2][TP_ROWS * TP_TOK / 2];  // own partial scores, staged for the bulk copy
   uint64_t kv_full[TP_STAGES], kv_empty[TP_STAGES];
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[2], s_empty;  // s_full by tile parity: each softmax group waits only on its own
   uint64_t x_full[2], x_sendok[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t m_ready[2], stats[2], sready[2];
@@ -230,11 +229,12 @@ struct SendCtx {
 };
 
 // Reads this CTA's partial scores of tile kv from TMEM (query row `row`, all
-// 64 tokens; the queries carry scale * log2(e), so these are in log2 units),
-// rounds them to fp16 into h and into the staging buffer kv & 1. Once the
-// group's four warps have staged theirs, one thread bulk-copies the 16 KB to
-// the peer's exchange buffer kv & 1 (the TMA engine moves it, so no thread
-// stalls on the cluster network). Returns true if a wait timed out.
+// 64 tokens; the queries carry scale * log2(e), so these are in log2 units).
+// They sit in two accumulators, one per half of this CTA's K columns, which
+// two threads issued in parallel; their sum is rounded to fp16 into h and
+// stored straight from registers into the peer's exchange buffer kv & 1
+// (16-byte st.async stores that count on the peer's mbarrier). Returns true
+// if a wait timed out (then nothing is sent).
 __device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uint32_t kv,
                                              uint32_t (&h)[32]) {
   const int sb = kv & 1;
@@ -242,30 +242,25 @@ __device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uin
   tc_fence_after();
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    float v[16];
-    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 * sb + 16 * q, v);
+    float v0[16], v1[16];
+    tmem_ld16(c.tmem + c.lane_base + TM_S + 16 * q, v0);
+    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 + 16 * q, v1);
     tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < 8; ++k) h[8 * q + k] = pack_half2(v[2 * k], v[2 * k + 1]);
+    for (int k = 0; k < 8; ++k)
+      h[8 * q + k] = pack_half2(v0[2 * k] + v1[2 * k], v0[2 * k + 1] + v1[2 * k + 1]);
   }
   tc_fence_before();
   __syncwarp();
-  if (c.lane == 0) mbar_arrive(&sm.s_empty[sb]);
-  // The staging buffer and the peer's exchange buffer are free once the
-  // peer has consumed tile kv - 2 (the bulk copy had finished reading then).
+  if (c.lane == 0) mbar_arrive(&sm.s_empty);
+  // The peer's buffer kv & 1 is free once it has consumed tile kv - 2.
   if (kv >= 2) bad |= !mbar_wait(&sm.x_sendok[sb], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
-  uint8_t* st = reinterpret_cast<uint8_t*>(sm.sbuf[sb]);
+  if (c.gtid == 0) mbar_arrive_expect_tx(&sm.x_full[sb], X_BYTES);
+  if (!bad) {
 #pragma unroll
-  for (int u = 0; u < 8; ++u)
-    *reinterpret_cast<uint4*>(st + xoff(c.row, u)) =
-        make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (c.lane == 0) mbar_arrive(&sm.sready[sb]);
-  if (c.gtid == 0) {
-    mbar_arrive_expect_tx(&sm.x_full[sb], X_BYTES);
-    bad |= !mbar_wait(&sm.sready[sb], (kv >> 1) & 1, WAIT_LIMIT);
-    if (!bad) bulk_copy_to_peer(c.xbuf_peer[sb], st, X_BYTES, c.xfull_peer[sb]);
+    for (int u = 0; u < 8; ++u)
+      st_async_v4u(c.xbuf_peer[sb] + xoff(c.row, u), h[4 * u], h[4 * u + 1], h[4 * u + 2],
+                   h[4 * u + 3], c.xfull_peer[sb]);
   }
   return bad;
 }
@@ -331,9 +326,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     }
     mbar_init(&sm.q_full, 1 + TP_GRP_WARPS);  // TMA bytes + the TMEM loader warps
     mbar_init(&sm.q_empty, 2);  // one commit from each score-MMA issuer
+    mbar_init(&sm.s_full[0], 2);             // one commit from each score-MMA issuer
+    mbar_init(&sm.s_full[1], 2);
+    mbar_init(&sm.s_empty, TP_GRP_WARPS);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], TP_GRP_WARPS);
       mbar_init(&sm.x_full[i], 1);
       mbar_init(&sm.x_sendok[i], TP_GRP_WARPS);
       mbar_init(&sm.p_full[i], TP_GRP_WARPS);
@@ -464,11 +460,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     }
   } else if (warp >= 2 + TP_SM_WARPS) {
     // ------------------------------------------------------------ score-MMA issuers
-    // Warp 10 issues the score MMAs of even tiles, warp 11 those of odd
-    // tiles, so two threads hide each other's issue latency. Each owns one
-    // TMEM score buffer.
+    // Each tile's 18 K-steps are split between warp 10 (latent steps 0..8)
+    // and warp 11 (latent steps 9..15 and the 2 rotary steps), into two
+    // accumulators that the softmax adds. Two threads hide each other's
+    // issue latency, which halves the time from a tile's arrival to its
+    // scores.
     if (lane == 0) {
-      const uint32_t par = static_cast<uint32_t>(warp - 2 - TP_SM_WARPS);  // 0 or 1
+      const uint32_t half = static_cast<uint32_t>(warp - 2 - TP_SM_WARPS);  // 0 or 1
       const uint32_t idS = idesc_bf16_f32(128, TP_TOK, false, false);
       const uint64_t dQc = smem_desc(smem_u32(sm.qc[0]), 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(smem_u32(sm.qr), 16, 512, kSwizzle64B);
@@ -477,46 +475,50 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         dKc[s] = smem_desc(smem_u32(sm.kv[s].c[0]), 16, 1024, kSwizzle128B);
         dKr[s] = smem_desc(smem_u32(sm.kv[s].r), 16, 512, kSwizzle64B);
       }
-      const uint32_t dS = tmem + TM_S + 64 * par;
+      const uint32_t dS = tmem + TM_S + 64 * half;
       bool ok = true;
       TileCursor cur;
       cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
       while (cur.valid() && ok) {
-        // one piece: wait for its Q, issue this thread's tiles, release Q
+        // one piece: wait for its Q, issue this thread's share of each tile, release Q
         if (!mbar_wait(&sm.q_full, cur.piece & 1, WAIT_LIMIT)) { ok = false; break; }
         tc_fence_after();
         const int piece = cur.piece;
         for (; cur.valid() && cur.piece == piece; cur.next()) {
           const uint32_t t = cur.kv;
-          if ((t & 1) != par) continue;
-          if (t >= 2 && !mbar_wait(&sm.s_empty[par], ((t >> 1) - 1) & 1, WAIT_LIMIT)) {
-            ok = false;
-            break;
-          }
+          if (t >= 1 && !mbar_wait(&sm.s_empty, (t - 1) & 1, WAIT_LIMIT)) { ok = false; break; }
           const int s = t % TP_STAGES;
           if (!mbar_wait(&sm.kv_full[s], (t / TP_STAGES) & 1, WAIT_LIMIT)) { ok = false; break; }
           tc_fence_after();
+          if (half == 0) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-            if (k < 8) {  // Q from shared memory
-              const uint32_t off = (QC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-              mma_bf16_ss(dS, dQc + off, dKc[s] + koff, idS, k > 0 ? 1u : 0u);
-            } else {      // Q from TMEM
-              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc[s] + koff, idS, 1u);
+            for (int k = 0; k < 9; ++k) {
+              const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+              if (k < 8) {  // Q from shared memory
+                const uint32_t off = (QC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+                mma_bf16_ss(dS, dQc + off, dKc[s] + koff, idS, k > 0 ? 1u : 0u);
+              } else {      // Q from TMEM
+                mma_bf16_ts(dS, tmem + TM_Q, dKc[s] + koff, idS, 1u);
+              }
             }
-          }
+          } else {
 #pragma unroll
-          for (int k = 0; k < 2; ++k)
-            mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr[s] + ((32u * k) >> 4), idS, 1u);
-          mma_commit(&sm.s_full[par]);
+            for (int k = 9; k < 16; ++k) {
+              const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc[s] + koff, idS, k > 9 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr[s] + ((32u * k) >> 4), idS, 1u);
+          }
+          mma_commit(&sm.s_full[t & 1]);
         }
         if (!ok) break;
         mma_commit(&sm.q_empty);
       }
       if (!ok) note_timeout(sm, a.err);
-      mma_commit(&sm.drain[1 + par]);
-      mbar_wait(&sm.drain[1 + par], 0, WAIT_LIMIT);
+      mma_commit(&sm.drain[1 + half]);
+      mbar_wait(&sm.drain[1 + half], 0, WAIT_LIMIT);
     }
   } else {
     // ------------------------------------------------------------ softmax warps 2..9
