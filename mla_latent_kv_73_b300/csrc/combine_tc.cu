@@ -44,7 +44,6 @@ struct __align__(1024) CombSmem {
   uint64_t wfull, done;
   uint32_t tmem_base;
   int c_lo[CT_TOK], c_hi[CT_TOK], row_off[CT_TOK];
-  float m_max[CT_TOK], inv_den[CT_TOK];
 };
 
 __device__ __forceinline__ uint64_t kdesc(const void* base, uint32_t byte_off) {
@@ -89,15 +88,16 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
     for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
   }
 
-  // 1. per token: the CTAs holding its pieces, the largest lse and the normaliser
+  // 1. per token: the CTAs holding its pieces and their merge weights
+  //    exp(lse_s - lse). One warp per token; the lanes take the pieces, so the
+  //    lse loads of a token are one round trip.
   const long long T_all = prefix[B];
   const long long N = T_all * p.G;
   for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = N > 0 ? range_begin(c, N, p.C) : 0;
   __syncthreads();
-  if (threadIdx.x < CT_TOK) {
-    const int t = threadIdx.x;
+  float* wts = reinterpret_cast<float*>(rb + p.C + 1);  // [CT_TOK][C + 1] merge weights
+  for (int t = warp; t < CT_TOK; t += CT_THREADS / 32) {
     int c0 = 0, c1 = -1, off = 0;
-    float M = -INFINITY, den = 0.f;
     if (t < ntok) {
       const int tok = t0 + t, b = tok / n_q, qi = tok % n_q;
       const int r = qi * n_h + h, g = r / p.RG, rr = r % p.RG;
@@ -106,22 +106,36 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
         const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
         c0 = cta_of_item(first, N, p.C);
         c1 = cta_of_item(last, N, p.C);
-        for (int c = c0; c <= c1; ++c)
-          if (rb[c] != rb[c + 1]) M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
-        if (M != -INFINITY)
-          for (int c = c0; c <= c1; ++c)
-            if (rb[c] != rb[c + 1]) den += expf(part_lse[static_cast<size_t>(c) * p.RG + off] - M);
       }
     }
-    sm.c_lo[t] = c0;
-    sm.c_hi[t] = (M == -INFINITY) ? -1 : c1;
-    sm.row_off[t] = off;
-    sm.m_max[t] = M;
-    sm.inv_den[t] = den > 0.f ? 1.f / den : 0.f;
+    float M = -INFINITY;
+    for (int c = c0 + lane; c <= c1; c += 32) {
+      const float x = rb[c] != rb[c + 1] ? part_lse[static_cast<size_t>(c) * p.RG + off] : -INFINITY;
+      wts[t * (p.C + 1) + (c - c0)] = x;
+      M = fmaxf(M, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    for (int c = c0 + lane; c <= c1; c += 32) {
+      const float e = M == -INFINITY ? 0.f : expf(wts[t * (p.C + 1) + (c - c0)] - M);
+      wts[t * (p.C + 1) + (c - c0)] = e;
+      den += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = c0 + lane; c <= c1; c += 32) wts[t * (p.C + 1) + (c - c0)] *= inv;
+    if (lane == 0) {
+      sm.c_lo[t] = c0;
+      sm.c_hi[t] = (M == -INFINITY) ? -1 : c1;
+      sm.row_off[t] = off;
+    }
   }
   __syncthreads();
 
-  // 2. o_lat = weighted sum of the partials; thread owns 8 latent dims of a token
+  // 2. o_lat = weighted sum of the partials; thread owns 8 latent dims of a
+  //    token. Loads go out four pieces at a time before they are used.
   {
     const int u = threadIdx.x % 64;  // 16-byte unit: latent dims [8u, 8u + 8)
     const int kc = u / 8, uu = u % 8;
@@ -131,20 +145,32 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
       if (tt < ntok) {
         const int lo = sm.c_lo[tt], hi = sm.c_hi[tt];
-        for (int c = lo; c <= hi; ++c) {
-          if (rb[c] == rb[c + 1]) continue;
-          const size_t row = static_cast<size_t>(c) * p.RG + sm.row_off[tt];
-          const float wgt = expf(part_lse[row] - sm.m_max[tt]) * sm.inv_den[tt];
-          const float4* src = reinterpret_cast<const float4*>(part_o + row * 512 + 8 * u);
-          const float4 a = src[0], b2 = src[1];
-          acc[0] = fmaf(wgt, a.x, acc[0]);
-          acc[1] = fmaf(wgt, a.y, acc[1]);
-          acc[2] = fmaf(wgt, a.z, acc[2]);
-          acc[3] = fmaf(wgt, a.w, acc[3]);
-          acc[4] = fmaf(wgt, b2.x, acc[4]);
-          acc[5] = fmaf(wgt, b2.y, acc[5]);
-          acc[6] = fmaf(wgt, b2.z, acc[6]);
-          acc[7] = fmaf(wgt, b2.w, acc[7]);
+        const size_t off = sm.row_off[tt];
+        const float* w = wts + tt * (p.C + 1) - lo;
+        for (int c = lo; c <= hi; c += 4) {
+          float4 va[4], vb[4];
+          float wg[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int cj = min(c + j, hi);
+            wg[j] = (c + j <= hi) ? w[cj] : 0.f;  // empty ranges carry weight 0
+            const float4* src = reinterpret_cast<const float4*>(
+                part_o + (static_cast<size_t>(cj) * p.RG + off) * 512 + 8 * u);
+            va[j] = src[0];
+            vb[j] = src[1];
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (wg[j] == 0.f) continue;  // also skips partials no range wrote
+            acc[0] = fmaf(wg[j], va[j].x, acc[0]);
+            acc[1] = fmaf(wg[j], va[j].y, acc[1]);
+            acc[2] = fmaf(wg[j], va[j].z, acc[2]);
+            acc[3] = fmaf(wg[j], va[j].w, acc[3]);
+            acc[4] = fmaf(wg[j], vb[j].x, acc[4]);
+            acc[5] = fmaf(wg[j], vb[j].y, acc[5]);
+            acc[6] = fmaf(wg[j], vb[j].z, acc[6]);
+            acc[7] = fmaf(wg[j], vb[j].w, acc[7]);
+          }
         }
       }
       uint32_t hw[4], lw[4];
@@ -230,7 +256,8 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
   spec.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
   CUtensorMap tw;
   if (!get_tmap(spec, &tw)) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(CombSmem) + 1024 + sizeof(long long) * (p.C + 1);
+  const size_t smem = sizeof(CombSmem) + 1024 + sizeof(long long) * (p.C + 1) +
+                      sizeof(float) * CT_TOK * (p.C + 1);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   static int attr_bytes[64] = {};
   int dev = 0;
