@@ -71,9 +71,10 @@ using namespace mla_ptx;
 constexpr int TP_ROWS = 128;                  // query rows per group (MMA M)
 constexpr int TP_TOK = 64;                    // tokens per tile = page size
 constexpr int TP_STAGES = 4;
-constexpr int TP_THREADS = 384;               // warp 0 TMA, 1 value MMA, 2..9 softmax, 10-11 score MMA
-constexpr int TP_SM_WARPS = 8;                // two softmax groups of four warps
-constexpr int TP_GRP_WARPS = 4;
+constexpr int TP_THREADS = 640;               // warp 0 TMA, 1 value MMA, 2-3 score MMA, 4..19 softmax
+constexpr int TP_SM_WARP0 = 4;                // first softmax warp
+constexpr int TP_SM_WARPS = 16;               // two softmax groups of eight warps
+constexpr int TP_GRP_WARPS = 8;
 constexpr uint32_t QC_BOX = 128 * 128;        // 128 rows x 64 bf16, 128B swizzle
 constexpr uint32_t QR_BOX = 128 * 64;         // 128 rows x 32 bf16, 64B swizzle
 constexpr uint32_t KC_BOX = 64 * 128;         // 64 tokens x 64 bf16
@@ -102,14 +103,15 @@ struct __align__(1024) PairSmem {
   uint64_t s_full[2], s_empty;  // s_full by tile parity: each softmax group waits only on its own
   uint64_t x_full[2], x_sendok[2];
   uint64_t p_full[2], pv_done[2];
-  uint64_t m_ready[2], stats[2], sready[2];
+  uint64_t m_ready[2], stats[2];
   uint64_t o_full, o_empty;
   uint64_t drain[3];
   uint32_t tmem_base;
   int abort_flag;
-  float mrow[2][TP_ROWS];   // running row max after tile kv, in slot kv & 1
-  float st_l[2][TP_ROWS];   // per softmax group: row sum at the end of a piece
-  float st_m[2][TP_ROWS];   // ... and the max that sum is referred to
+  float mrow[2][TP_ROWS];      // running row max after tile kv, in slot kv & 1
+  float xmax[2][2][TP_ROWS];   // [group][column half] partial row maxima of a tile
+  float st_l[2][2][TP_ROWS];   // [group][column half]: row sum at the end of a piece
+  float st_m[2][TP_ROWS];      // [group]: the max those sums are referred to
 };
 
 struct PairArgs {
@@ -150,40 +152,35 @@ __device__ __forceinline__ Piece locate_piece(long long it, long long end, long 
 }
 
 // Walks the tiles of a pair's range in order: kv counts tiles from 0, i is
-// the index inside the current piece, piece counts pieces from 0.
+// the index inside the current piece, piece counts pieces from 0. The
+// range's invariants stay in the kernel parameters, not in registers.
 struct TileCursor {
-  long long it, end, T_all;
-  const int32_t* prefix;
-  const int32_t* tiles;
-  int B;
+  long long it;
+  int left;  // tiles left in the range, this one included
   Piece pc;
   int i, piece;
   uint32_t kv;
-  __device__ void init(long long b, long long e, long long T, const int32_t* pf, const int32_t* tl,
-                       int nb) {
+  __device__ void init(long long b, long long e, const PairArgs& a) {
     it = b;
-    end = e;
-    T_all = T;
-    prefix = pf;
-    tiles = tl;
-    B = nb;
+    left = static_cast<int>(e - b);
     i = 0;
     piece = 0;
     kv = 0;
-    if (it < end) pc = locate_piece(it, end, T_all, prefix, tiles, B);
+    if (left > 0) pc = locate_piece(it, e, a.prefix[a.B], a.prefix, a.tiles, a.B);
   }
-  __device__ bool valid() const { return it < end; }
+  __device__ bool valid() const { return left > 0; }
   __device__ bool first() const { return i == 0; }
   __device__ bool last() const { return i == pc.n_tiles - 1; }
   __device__ int tile() const { return pc.t_first + i; }
-  __device__ void next() {
+  __device__ void next(const PairArgs& a) {
     ++it;
+    --left;
     ++i;
     ++kv;
     if (i == pc.n_tiles) {
       i = 0;
       ++piece;
-      if (it < end) pc = locate_piece(it, end, T_all, prefix, tiles, B);
+      if (left > 0) pc = locate_piece(it, it + left, a.prefix[a.B], a.prefix, a.tiles, a.B);
     }
   }
 };
@@ -224,27 +221,26 @@ __device__ __forceinline__ uint32_t xoff(int row, int u) {
 // What a softmax thread needs to ship its partial scores to the peer CTA.
 struct SendCtx {
   uint32_t tmem, lane_base;
-  int row, lane, gtid;
-  uint32_t xbuf_peer[2], xfull_peer[2];
+  int row, hh, lane, gtid;
 };
 
-// Reads this CTA's partial scores of tile kv from TMEM (query row `row`, all
-// 64 tokens; the queries carry scale * log2(e), so these are in log2 units).
-// They sit in two accumulators, one per half of this CTA's K columns, which
-// two threads issued in parallel; their sum is rounded to fp16 into h and
-// stored straight from registers into the peer's exchange buffer kv & 1
-// (16-byte st.async stores that count on the peer's mbarrier). Returns true
-// if a wait timed out (then nothing is sent).
+// Reads this CTA's partial scores of tile kv from TMEM (query row `row`,
+// tokens [32 hh, 32 hh + 32); the queries carry scale * log2(e), so these are
+// in log2 units). They sit in two accumulators, one per half of this CTA's K
+// columns, which two threads issued in parallel; their sum is rounded to
+// fp16 into h and stored straight from registers into the peer's exchange
+// buffer kv & 1 (16-byte st.async stores that count on the peer's mbarrier).
+// Returns true if a wait timed out (then nothing is sent).
 __device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uint32_t kv,
-                                             uint32_t (&h)[32]) {
+                                             uint32_t (&h)[16]) {
   const int sb = kv & 1;
   bool bad = !mbar_wait(&sm.s_full[sb], (kv >> 1) & 1, WAIT_LIMIT);
   tc_fence_after();
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     float v0[16], v1[16];
-    tmem_ld16(c.tmem + c.lane_base + TM_S + 16 * q, v0);
-    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 + 16 * q, v1);
+    tmem_ld16(c.tmem + c.lane_base + TM_S + 32 * c.hh + 16 * q, v0);
+    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 + 32 * c.hh + 16 * q, v1);
     tmem_wait_ld();
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -257,10 +253,13 @@ __device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uin
   if (kv >= 2) bad |= !mbar_wait(&sm.x_sendok[sb], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
   if (c.gtid == 0) mbar_arrive_expect_tx(&sm.x_full[sb], X_BYTES);
   if (!bad) {
+    const uint32_t peer = cluster_ctarank() ^ 1u;
+    const uint32_t xbuf_peer = mapa_shared(smem_u32(sm.xbuf[sb]), peer);
+    const uint32_t xfull_peer = mapa_shared(smem_u32(&sm.x_full[sb]), peer);
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      st_async_v4u(c.xbuf_peer[sb] + xoff(c.row, u), h[4 * u], h[4 * u + 1], h[4 * u + 2],
-                   h[4 * u + 3], c.xfull_peer[sb]);
+    for (int u = 0; u < 4; ++u)
+      st_async_v4u(xbuf_peer + xoff(c.row, 4 * c.hh + u), h[4 * u], h[4 * u + 1], h[4 * u + 2],
+                   h[4 * u + 3], xfull_peer);
   }
   return bad;
 }
@@ -324,7 +323,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.q_full, 1 + TP_GRP_WARPS);  // TMA bytes + the TMEM loader warps
+    mbar_init(&sm.q_full, 1 + 4);  // TMA bytes + the four TMEM loader warps
     mbar_init(&sm.q_empty, 2);  // one commit from each score-MMA issuer
     mbar_init(&sm.s_full[0], 2);             // one commit from each score-MMA issuer
     mbar_init(&sm.s_full[1], 2);
@@ -336,7 +335,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mbar_init(&sm.pv_done[i], 1);
       mbar_init(&sm.m_ready[i], TP_GRP_WARPS);
       mbar_init(&sm.stats[i], TP_SM_WARPS);
-      mbar_init(&sm.sready[i], TP_GRP_WARPS);
     }
     mbar_init(&sm.o_full, 1);
     mbar_init(&sm.o_empty, TP_GRP_WARPS);
@@ -428,13 +426,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       // C as the MN-major B operand: latent columns are contiguous (64 per
       // 128-byte row, the next 64 one box further), tokens step 128 B,
       // 8-token groups are 1024 B apart.
-      uint64_t dC[TP_STAGES];
-      for (int s = 0; s < TP_STAGES; ++s)
-        dC[s] = smem_desc(smem_u32(sm.kv[s].c[0]), KC_BOX, 1024, kSwizzle128B);
+      const uint64_t dC0 = smem_desc(smem_u32(sm.kv[0].c[0]), KC_BOX, 1024, kSwizzle128B);
+      constexpr uint32_t kStageDesc = sizeof(PairSmem::Stage) >> 4;  // stage stride, 16-B units
       bool ok = true;
       TileCursor cur;
-      cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
-      for (; cur.valid() && ok; cur.next()) {
+      cur.init(it_begin, it_end, a);
+      for (; cur.valid() && ok; cur.next(a)) {
         const uint32_t t = cur.kv;
         if (!mbar_wait(&sm.p_full[t & 1], (t >> 1) & 1, WAIT_LIMIT)) { ok = false; break; }
         if (cur.first() && cur.piece > 0 &&
@@ -447,7 +444,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         const uint32_t pcol = tmem + TM_P + 32 * (t & 1);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + TM_O, pcol + 8 * kk, dC[s] + ((2048u * kk) >> 4), idPV,
+          mma_bf16_ts(tmem + TM_O, pcol + 8 * kk, dC0 + s * kStageDesc + ((2048u * kk) >> 4), idPV,
                       (cur.first() && kk == 0) ? 0u : 1u);
         mma_commit(&sm.kv_empty[s]);
         mma_commit(&sm.pv_done[t & 1]);
@@ -458,33 +455,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mma_commit(&sm.drain[0]);
       mbar_wait(&sm.drain[0], 0, WAIT_LIMIT);
     }
-  } else if (warp >= 2 + TP_SM_WARPS) {
+  } else if (warp < TP_SM_WARP0) {
     // ------------------------------------------------------------ score-MMA issuers
-    // Each tile's 18 K-steps are split between warp 10 (latent steps 0..8)
-    // and warp 11 (latent steps 9..15 and the 2 rotary steps), into two
+    // Each tile's 18 K-steps are split between warp 2 (latent steps 0..8)
+    // and warp 3 (latent steps 9..15 and the 2 rotary steps), into two
     // accumulators that the softmax adds. Two threads hide each other's
     // issue latency, which halves the time from a tile's arrival to its
     // scores.
     if (lane == 0) {
-      const uint32_t half = static_cast<uint32_t>(warp - 2 - TP_SM_WARPS);  // 0 or 1
+      const uint32_t half = static_cast<uint32_t>(warp - 2);  // 0 or 1
       const uint32_t idS = idesc_bf16_f32(128, TP_TOK, false, false);
       const uint64_t dQc = smem_desc(smem_u32(sm.qc[0]), 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(smem_u32(sm.qr), 16, 512, kSwizzle64B);
-      uint64_t dKc[TP_STAGES], dKr[TP_STAGES];
-      for (int s = 0; s < TP_STAGES; ++s) {
-        dKc[s] = smem_desc(smem_u32(sm.kv[s].c[0]), 16, 1024, kSwizzle128B);
-        dKr[s] = smem_desc(smem_u32(sm.kv[s].r), 16, 512, kSwizzle64B);
-      }
+      const uint64_t dKc0 = smem_desc(smem_u32(sm.kv[0].c[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dKr0 = smem_desc(smem_u32(sm.kv[0].r), 16, 512, kSwizzle64B);
+      constexpr uint32_t kStageDesc = sizeof(PairSmem::Stage) >> 4;  // stage stride, 16-B units
       const uint32_t dS = tmem + TM_S + 64 * half;
       bool ok = true;
       TileCursor cur;
-      cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
+      cur.init(it_begin, it_end, a);
       while (cur.valid() && ok) {
         // one piece: wait for its Q, issue this thread's share of each tile, release Q
         if (!mbar_wait(&sm.q_full, cur.piece & 1, WAIT_LIMIT)) { ok = false; break; }
         tc_fence_after();
         const int piece = cur.piece;
-        for (; cur.valid() && cur.piece == piece; cur.next()) {
+        for (; cur.valid() && cur.piece == piece; cur.next(a)) {
           const uint32_t t = cur.kv;
           if (t >= 1 && !mbar_wait(&sm.s_empty, (t - 1) & 1, WAIT_LIMIT)) { ok = false; break; }
           const int s = t % TP_STAGES;
@@ -496,20 +491,20 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
               const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
               if (k < 8) {  // Q from shared memory
                 const uint32_t off = (QC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-                mma_bf16_ss(dS, dQc + off, dKc[s] + koff, idS, k > 0 ? 1u : 0u);
+                mma_bf16_ss(dS, dQc + off, dKc0 + s * kStageDesc + koff, idS, k > 0 ? 1u : 0u);
               } else {      // Q from TMEM
-                mma_bf16_ts(dS, tmem + TM_Q, dKc[s] + koff, idS, 1u);
+                mma_bf16_ts(dS, tmem + TM_Q, dKc0 + s * kStageDesc + koff, idS, 1u);
               }
             }
           } else {
 #pragma unroll
             for (int k = 9; k < 16; ++k) {
               const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc[s] + koff, idS, k > 9 ? 1u : 0u);
+              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc0 + s * kStageDesc + koff, idS, k > 9 ? 1u : 0u);
             }
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-              mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr[s] + ((32u * k) >> 4), idS, 1u);
+              mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr0 + s * kStageDesc + ((32u * k) >> 4), idS, 1u);
           }
           mma_commit(&sm.s_full[t & 1]);
         }
@@ -521,31 +516,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mbar_wait(&sm.drain[1 + half], 0, WAIT_LIMIT);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps 2..9
-    // Group g = (w - 2) / 4 handles the tiles with kv % 2 == g, so one group's
-    // exchange and softmax overlap the other's. Warp w reads TMEM lane quarter
-    // w % 4: query rows 32 (w % 4) .. +31, one row per lane, all 64 tokens.
-    // The running row max is handed from tile to tile through shared memory
-    // (mrow, m_ready). Each group keeps its own row sum, referred to the max
-    // it last used; the epilogue merges the two.
-    const int grp = (warp - 2) >> 2;
+    // ------------------------------------------------------------ softmax warps 4..19
+    // Group g = (w - 4) / 8 handles the tiles with kv % 2 == g, so one group's
+    // exchange and softmax overlap the other's. Inside a group, warp w reads
+    // TMEM lane quarter w % 4 (query rows 32 (w % 4) .. +31, one row per lane)
+    // and score columns [32 hh, 32 hh + 32), hh = ((w - 4) / 4) % 2. The two
+    // warps of a lane quarter agree on the row maximum at a 64-thread named
+    // barrier. The running max is handed from tile to tile, across the two
+    // groups, through shared memory (mrow, m_ready). Each warp keeps the sum
+    // of its half rows, referred to the max its group last used; the
+    // epilogue merges the four sums of a row.
+    const int sw = warp - TP_SM_WARP0;           // 0..15
+    const int grp = sw >> 3;
+    const int hh = (sw >> 2) & 1;
     const int qd = warp & 3;
+    const uint32_t bar_id = 1 + 4 * grp + qd;   // 64-thread barrier of the two halves
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const int row = 32 * qd + lane;
-    const int gtid = ((warp - 2) & 3) * 32 + lane;  // 0..127 inside the group
-    const SendCtx sx{tmem, lane_base, row, lane, gtid,
-                     {mapa_shared(smem_u32(sm.xbuf[0]), peer),
-                      mapa_shared(smem_u32(sm.xbuf[1]), peer)},
-                     {mapa_shared(smem_u32(&sm.x_full[0]), peer),
-                      mapa_shared(smem_u32(&sm.x_full[1]), peer)}};
-    const uint32_t xsendok_peer[2] = {mapa_shared(smem_u32(&sm.x_sendok[0]), peer),
-                                      mapa_shared(smem_u32(&sm.x_sendok[1]), peer)};
+    const int gtid = (sw & 7) * 32 + lane;      // 0..255 inside the group
+    const SendCtx sx{tmem, lane_base, row, hh, lane, gtid};
     TileCursor cur;
-    cur.init(it_begin, it_end, T_all, a.prefix, a.tiles, a.B);
-    float l = 0.f, mref = -INFINITY;  // this group's row sum and the max it refers to
+    cur.init(it_begin, it_end, a);
+    float l = 0.f, mref = -INFINITY;  // this warp's half-row sum and the max it refers to
     int L = 0, rows_valid = 0, pos_q = 0;
     bool row_ok = false, bad = false;
-    for (; cur.valid() && !bad; cur.next()) {
+    for (; cur.valid() && !bad; cur.next(a)) {
       const uint32_t kv = cur.kv;
       const bool first = cur.first();
       if (first) {
@@ -555,17 +550,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         rows_valid = min(TP_ROWS, rows_total - cur.pc.g * TP_ROWS);
         row_ok = row < rows_valid;
         pos_q = L - a.n_q + (row_ok ? (cur.pc.g * TP_ROWS + row) / a.n_h : 0);
-        if (grp == 0) bad |= load_q_tmem(sm, a, tmem, lane_base, row, lane, rank, cur);
+        if (grp == 0 && hh == 0) bad |= load_q_tmem(sm, a, tmem, lane_base, row, lane, rank, cur);
       }
       if ((kv & 1) != static_cast<uint32_t>(grp)) {
         // The other group's tile. At the end of a piece, hand over this
-        // group's row sums, once that tile has published its max: this keeps
+        // warp's row sums, once that tile has published its max: this keeps
         // the two groups at most one piece apart, which the two stats
         // barriers (one per piece parity) rely on.
         if (cur.last()) {
           bad |= !mbar_wait(&sm.m_ready[kv & 1], (kv >> 1) & 1, WAIT_LIMIT);
-          sm.st_l[grp][row] = l;
-          sm.st_m[grp][row] = mref;
+          sm.st_l[grp][hh][row] = l;
+          if (hh == 0) sm.st_m[grp][row] = mref;
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
         }
@@ -573,18 +568,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       }
       const int t = cur.tile();
       const int s2 = kv % TP_STAGES;
-      uint32_t own[32];
+      uint32_t own[16];
       bad |= send_partial(sm, sx, kv, own);
 
       // 1. full scaled scores = own partial + the peer's (both fp16-rounded)
       const int xb = kv & 1;
       bad |= !mbar_wait(&sm.x_full[xb], (kv >> 1) & 1, WAIT_LIMIT);
-      float sc[64];
+      float sc[32];
       {
         const uint8_t* xin = reinterpret_cast<const uint8_t*>(sm.xbuf[xb]);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 pv = *reinterpret_cast<const uint4*>(xin + xoff(row, u));
+        for (int u = 0; u < 4; ++u) {
+          const uint4 pv = *reinterpret_cast<const uint4*>(xin + xoff(row, 4 * hh + u));
           const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
@@ -597,44 +592,70 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       __syncwarp();
       // At the end of a piece the epilogue borrows this exchange buffer, so
       // the peer may only refill it afterwards.
-      if (lane == 0 && !cur.last()) mbar_arrive_remote_relaxed(xsendok_peer[xb]);
+      if (lane == 0 && !cur.last()) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[xb]), peer));
 
-      // 2. causal mask, row max
-      const int j0 = t * TP_TOK;  // token of sc[0]
-      if (!(row_ok && j0 + TP_TOK - 1 <= L - a.n_q)) {
+      // 2. causal mask, row max (both halves), running max from the previous tile
+      const int j0 = t * TP_TOK + 32 * hh;  // token of sc[0]
+      if (!(row_ok && j0 + 31 <= L - a.n_q)) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] : -INFINITY;
+        for (int c = 0; c < 32; ++c) sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] : -INFINITY;
       }
-      float pm[8];
+      float pm[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 4; ++u)
         pm[u] = fmaxf(fmaxf(fmaxf(sc[8 * u], sc[8 * u + 1]), fmaxf(sc[8 * u + 2], sc[8 * u + 3])),
                       fmaxf(fmaxf(sc[8 * u + 4], sc[8 * u + 5]), fmaxf(sc[8 * u + 6], sc[8 * u + 7])));
-      }
-      const float pmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      // 3. running max from the previous tile (the other group's)
+      sm.xmax[grp][hh][row] = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
       if (kv > 0) bad |= !mbar_wait(&sm.m_ready[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+      if (named_bar_or(bar_id, 64, bad)) {
+        bad = true;
+        break;
+      }
+      const float pmax = fmaxf(sm.xmax[grp][0][row], sm.xmax[grp][1][row]);
       const float m_prev = first ? -INFINITY : sm.mrow[(kv - 1) & 1][row];
       const float m_new = fmaxf(m_prev, pmax);
       const bool need = !first && row_ok && (m_new > m_prev + RESCALE_THRESHOLD);
       const float m_use = (first || need) ? m_new : m_prev;
-      sm.mrow[kv & 1][row] = m_use;
+      if (hh == 0) sm.mrow[kv & 1][row] = m_use;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.m_ready[kv & 1]);
       // A row with nothing visible yet keeps m_use = -inf; subtracting 0
       // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
 
-      // 4. lazy rescale of this warp's rows of O
+      // 3. P (bf16 pairs) into its TMEM buffer, once the value MMA two tiles
+      // back has read that buffer
+      if (kv >= 2) bad |= !mbar_wait(&sm.pv_done[kv & 1], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
+      tc_fence_after();
+      {
+        float psum = 0.f;
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = fast_exp2(sc[2 * k] - m_sub);
+          const float p1 = fast_exp2(sc[2 * k + 1] - m_sub);
+          psum += p0 + p1;
+          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+          w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+        }
+        if (!__any_sync(0xffffffffu, bad))
+          tmem_st16u(tmem + lane_base + TM_P + 32 * (kv & 1) + 16 * hh, w);
+        tmem_wait_st();
+        if (row_ok) {
+          l = (mref == -INFINITY) ? psum : l * fast_exp2(mref - m_use) + psum;
+          mref = m_use;
+        }
+      }
+      // 4. lazy rescale of this warp's rows of O (its half of the columns),
+      // after P so that the scores are no longer live
       if (__any_sync(0xffffffffu, need)) {
         bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
         tc_fence_after();
         if (!__any_sync(0xffffffffu, bad)) {
           const float f = need ? fast_exp2(m_prev - m_use) : 1.f;
-          for (int c0 = 0; c0 < 256; c0 += 16) {
+          for (int c0 = 0; c0 < 128; c0 += 16) {
             float v[16];
-            const uint32_t ta = tmem + lane_base + TM_O + c0;
+            const uint32_t ta = tmem + lane_base + TM_O + 128 * hh + c0;
             tmem_ld16(ta, v);
             tmem_wait_ld();
 #pragma unroll
@@ -645,32 +666,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         }
       }
 
-      // 5. P (bf16 pairs) into its TMEM buffer, once the value MMA two tiles
-      // back has read that buffer
-      if (kv >= 2) bad |= !mbar_wait(&sm.pv_done[kv & 1], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
-      tc_fence_after();
-      {
-        float psum = 0.f;
-        uint32_t w[16];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_exp2(sc[32 * hh + 2 * k] - m_sub);
-            const float p1 = fast_exp2(sc[32 * hh + 2 * k + 1] - m_sub);
-            psum += p0 + p1;
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-            w[k] = *reinterpret_cast<const uint32_t*>(&pb);
-          }
-          if (!__any_sync(0xffffffffu, bad))
-            tmem_st16u(tmem + lane_base + TM_P + 32 * (kv & 1) + 16 * hh, w);
-        }
-        tmem_wait_st();
-        if (row_ok) {
-          l = (mref == -INFINITY) ? psum : l * fast_exp2(mref - m_use) + psum;
-          mref = m_use;
-        }
-      }
       // Rows past the end of the sequence may hold anything; zero their
       // latent columns so that 0 * garbage cannot reach the accumulator.
       const int jt = t * TP_TOK;
@@ -690,8 +685,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       if (cur.last()) {
         // ---- epilogue of the piece (done by the group of its last tile):
         // O / l -> workspace slot
-        sm.st_l[grp][row] = l;
-        sm.st_m[grp][row] = mref;
+        sm.st_l[grp][hh][row] = l;
+        if (hh == 0) sm.st_m[grp][row] = mref;
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
         bad |= !mbar_wait(&sm.stats[cur.piece & 1], (cur.piece >> 1) & 1, WAIT_LIMIT);
@@ -701,46 +696,45 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
           const float mg = sm.st_m[g2][row];
-          if (mg != -INFINITY) lt += sm.st_l[g2][row] * fast_exp2(mg - m_use);
+          if (mg != -INFINITY)
+            lt += (sm.st_l[g2][0][row] + sm.st_l[g2][1][row]) * fast_exp2(mg - m_use);
         }
         const float inv_l = (row_ok && lt > 0.f) ? 1.f / lt : 0.f;
         const int slot = pair + cur.pc.g * a.B + cur.pc.b;
-        if (rank == 0 && row_ok)
+        if (rank == 0 && hh == 0 && row_ok)
           a.part_lse[static_cast<size_t>(slot) * TP_ROWS + row] =
               lt > 0.f ? (m_use + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-        // O / l goes out 32 columns at a time through this warp's 4 KB of
+        // O / l goes out 16 columns at a time through this warp's 2 KB of
         // the (already consumed) exchange buffer: each lane writes its row,
-        // then the warp stores one 128-byte row segment per instruction.
+        // then each store instruction covers two 64-byte row segments.
         if (!__any_sync(0xffffffffu, bad)) {
-          uint8_t* stg = reinterpret_cast<uint8_t*>(sm.xbuf[xb]) + qd * 4096;
-          float* dst0 = a.part_o + (static_cast<size_t>(slot) * TP_ROWS + 32 * qd) * 512 +
-                        256 * rank + lane;
-          for (int c0 = 0; c0 < 256; c0 += 32) {
-            float v[32];
-            tmem_ld16(tmem + lane_base + TM_O + c0, *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tmem + lane_base + TM_O + c0 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          uint8_t* stg = reinterpret_cast<uint8_t*>(sm.xbuf[xb]) + (sw & 7) * 2048;
+          const int rsub = lane >> 4, csub = lane & 15;
+          float* dst0 = a.part_o + (static_cast<size_t>(slot) * TP_ROWS + 32 * qd + rsub) * 512 +
+                        256 * rank + 128 * hh + csub;
+          for (int c0 = 0; c0 < 128; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + TM_O + 128 * hh + c0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ (lane & 7)) * 16)) =
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<float4*>(stg + lane * 64 + ((u ^ (lane & 3)) * 16)) =
                   make_float4(v[4 * u] * inv_l, v[4 * u + 1] * inv_l, v[4 * u + 2] * inv_l,
                               v[4 * u + 3] * inv_l);
             __syncwarp();
-            // All loads of a half before its stores: the compiler cannot prove
-            // that the staging buffer and the output do not alias, so mixing
-            // them would serialise every load behind the previous store.
+            // All loads before the stores: the compiler cannot prove that the
+            // staging buffer and the output do not alias.
+            float x[16];
 #pragma unroll
-            for (int r0 = 0; r0 < 32; r0 += 16) {
-              float x[16];
-#pragma unroll
-              for (int r = 0; r < 16; ++r)
-                x[r] = *reinterpret_cast<const float*>(
-                    stg + (r0 + r) * 128 + (((lane >> 2) ^ ((r0 + r) & 7)) * 16) + (lane & 3) * 4);
-#pragma unroll
-              for (int r = 0; r < 16; ++r)
-                if (32 * qd + r0 + r < rows_valid)
-                  dst0[static_cast<size_t>(r0 + r) * 512 + c0] = x[r];
+            for (int r = 0; r < 16; ++r) {
+              const int rr = 2 * r + rsub;
+              x[r] = *reinterpret_cast<const float*>(stg + rr * 64 + (((csub >> 2) ^ (rr & 3)) * 16) +
+                                                     (csub & 3) * 4);
             }
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+              if (32 * qd + 2 * r + rsub < rows_valid)
+                dst0[static_cast<size_t>(2 * r) * 512 + c0] = x[r];
             __syncwarp();
           }
         }
@@ -748,7 +742,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sm.o_empty);
-          mbar_arrive_remote_relaxed(xsendok_peer[xb]);  // the exchange buffer is free again
+          mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[xb]), peer));  // the exchange buffer is free again
         }
       }
     }

@@ -324,6 +324,18 @@ __device__ __forceinline__ void cluster_sync() {
 }
 constexpr uint32_t kSwizzle64B = 4;
 
+// Register rebalancing between warpgroups (all four warps of a warpgroup
+// execute these together). The counts must be multiples of 8, and the sum
+// over the block must stay within what the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Named barrier over a subset of the block's warps.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
