@@ -24,26 +24,47 @@
 // of every tile and of Q, and accumulates O for its 256 latent columns
 // (256 TMEM columns). Each CTA computes a partial score over its 288
 // columns (M = 128, N = 64, K = 288). The pair swaps the partials through
-// distributed shared memory: 16-byte st.async stores that count their bytes
-// on the receiver's mbarrier. Each then adds the two partials. fp32
+// distributed shared memory: one bulk copy per tile and direction that counts
+// its bytes on the receiver's mbarrier. Each then adds the two partials. fp32
 // addition is commutative, so both CTAs hold bit-identical scores, run the
 // same softmax and agree on every row maximum and sum without further
 // messages. Every cache byte is read from HBM once, by one CTA.
 //
-// TMEM (512 columns): two 64-column score buffers, two 32-column buffers for
-// P (bf16 pairs, read by the value MMA straight from TMEM as its A operand),
-// and the 256-column latent accumulator.
+// The exchange is a pipeline stage of its own, so that its latency overlaps
+// the softmax of the previous tile instead of adding to it:
 //
-// Warp roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: Q (4 + 1 boxes) once per piece, then per
-//               64-token page 4 latent boxes (128B swizzle) and 1 rotary box
-//               (64B swizzle), 3-stage ring
-//   warp 1      TMEM allocator and single-thread MMA issuer
-//   warps 2..9  softmax. Warp w reads TMEM lane quarter w % 4 (query rows
-//               32(w % 4) .. +31, one row per lane) and score columns
-//               [32h, 32h + 32), h = (w - 2) / 4. The two warps of a lane
+//   TMA -> score MMA -> sender warps -> (peer) -> softmax warps -> value MMA
+//
+// TMEM (512 columns): two 64-column score slots (tile parity), a 32-column
+// buffer for P (bf16 pairs, read by the value MMA straight from TMEM as its
+// A operand), 96 columns of Q (192 of this CTA's latent columns) and the
+// 256-column latent accumulator. After the sender warps have read a score
+// slot they write the fp16-rounded partial back into its first 32 columns,
+// where the softmax warps pick up their own half of the sum.
+//
+// The partials travel by the bulk-copy engine (cp.async.bulk from a local
+// staging buffer into the peer's exchange buffer), not by st.async from
+// registers: while a warp streams 16 KB of st.async, the other warps' TMEM
+// loads and 16-byte shared loads on the SM wait behind it for about the
+// length of the transfer, which stalled the softmax warps once per tile.
+//
+// Warp roles (512 threads, one CTA per SM):
+//   warp 0      TMA producer: Q (1 + 1 boxes) once per piece, then per
+//               64-token page the latent columns and the rotary box, 4-stage
+//               ring
+//   warp 1      TMEM allocator and value-MMA issuer
+//   warps 2, 3  score-MMA issuers, warp 2 for even tiles, warp 3 for odd
+//               tiles, each into its own score slot
+//   warps 4..7  senders: warp w reads the score slot's lane quarter w % 4
+//               (one query row per lane, all 64 tokens), rounds the partial
+//               to fp16, writes it back to TMEM and into the staging
+//               buffer, from which one thread copies it to the peer. They
+//               also put the TMEM part of Q in place at each piece.
+//   warps 8..15 softmax: warp w reads lane quarter w % 4 and tokens
+//               [32h, 32h + 32), h = (w - 8) / 4. The two warps of a lane
 //               quarter meet at a 64-thread named barrier to agree on the
-//               row maximum.
+//               row maximum. One set of warps handles every tile, so the
+//               running max and row sums live in registers.
 //
 // Lazy rescale: a row's running max is only raised when the new max exceeds
 // it by more than 8 (log2 units). Otherwise P is computed against the stale
@@ -71,26 +92,27 @@ using namespace mla_ptx;
 constexpr int TP_ROWS = 128;                  // query rows per group (MMA M)
 constexpr int TP_TOK = 64;                    // tokens per tile = page size
 constexpr int TP_STAGES = 4;
-constexpr int TP_THREADS = 640;               // warp 0 TMA, 1 value MMA, 2-3 score MMA, 4..19 softmax
-constexpr int TP_SM_WARP0 = 4;                // first softmax warp
-constexpr int TP_SM_WARPS = 16;               // two softmax groups of eight warps
-constexpr int TP_GRP_WARPS = 8;
+constexpr int TP_THREADS = 512;
+constexpr int TP_SEND_WARP0 = 4;              // first sender warp
+constexpr int TP_SM_WARP0 = 8;                // first softmax warp
+constexpr int TP_SM_WARPS = 8;
 constexpr uint32_t QC_BOX = 128 * 128;        // 128 rows x 64 bf16, 128B swizzle
 constexpr uint32_t QR_BOX = 128 * 64;         // 128 rows x 32 bf16, 64B swizzle
 constexpr uint32_t KC_BOX = 64 * 128;         // 64 tokens x 64 bf16
 constexpr uint32_t KR_BOX = 64 * 64;          // 64 tokens x 32 bf16
-constexpr uint32_t Q_BYTES = 2 * QC_BOX + QR_BOX;   // Q through TMA (the rest goes to TMEM)
+constexpr uint32_t Q_BYTES = QC_BOX + QR_BOX;   // Q through TMA (the rest goes to TMEM)
 constexpr uint32_t STAGE_BYTES = 4 * KC_BOX + KR_BOX;
 constexpr uint32_t X_BYTES = TP_ROWS * TP_TOK * 2;  // fp16 partial scores
-constexpr uint32_t TM_S = 0;                  // score slot: two K-half accumulators at 0 and 64
-constexpr uint32_t TM_P = 128;                // P buffers at columns 128 and 160
-constexpr uint32_t TM_Q = 192;                // Q latent columns 128..255 of this CTA (bf16 pairs)
+constexpr uint32_t TM_S = 0;                  // score slots at columns 0 and 64
+constexpr uint32_t TM_P = 128;                // P buffer, 32 columns
+constexpr uint32_t TM_Q = 160;                // Q latent columns 64..255 of this CTA (bf16 pairs)
 constexpr uint32_t TM_O = 256;                // latent accumulator, 256 columns
+constexpr uint32_t SEND_BAR = 5;              // named barrier of the four sender warps
 constexpr long long WAIT_LIMIT = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float RESCALE_THRESHOLD = 8.f;        // log2 units
 
 struct __align__(1024) PairSmem {
-  uint8_t qc[2][QC_BOX];  // Q latent columns 0..127 of this CTA's half
+  uint8_t qc[QC_BOX];  // Q latent columns 0..63 of this CTA's half
   uint8_t qr[QR_BOX];
   struct Stage {
     uint8_t c[4][KC_BOX];
@@ -98,20 +120,20 @@ struct __align__(1024) PairSmem {
   } kv[TP_STAGES];
   // peer's partial scores, fp16 pairs: [buffer][row][64 tokens], 16-byte units swizzled
   uint32_t xbuf[2][TP_ROWS * TP_TOK / 2];
+  // this CTA's partial scores of the tile being sent, same layout
+  uint32_t sendbuf[TP_ROWS * TP_TOK / 2];
   uint64_t kv_full[TP_STAGES], kv_empty[TP_STAGES];
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], s_empty;  // s_full by tile parity: each softmax group waits only on its own
-  uint64_t x_full[2], x_sendok[2];
+  uint64_t s_full[2], s_empty[2];   // score slot by tile parity
+  uint64_t own_ready[2];            // fp16 own partial written back to the slot
+  uint64_t x_full[2], x_sendok[2];  // peer's partial arrived / peer's buffer free
   uint64_t p_full[2], pv_done[2];
-  uint64_t m_ready[2], stats[2];
   uint64_t o_full, o_empty;
   uint64_t drain[3];
   uint32_t tmem_base;
   int abort_flag;
-  float mrow[2][TP_ROWS];      // running row max after tile kv, in slot kv & 1
-  float xmax[2][2][TP_ROWS];   // [group][column half] partial row maxima of a tile
-  float st_l[2][2][TP_ROWS];   // [group][column half]: row sum at the end of a piece
-  float st_m[2][TP_ROWS];      // [group]: the max those sums are referred to
+  float xmax[2][2][TP_ROWS];   // [tile parity][column half] partial row maxima
+  float st_l[2][TP_ROWS];      // [column half]: row sums at the end of a piece
 };
 
 struct PairArgs {
@@ -125,7 +147,7 @@ struct PairArgs {
   uint32_t* err;
   long long q_rows;
   int num_blocks, max_blocks, B, n_q, n_h, G, P;
-  int chunked;  // 1: latent boxes come as one 3-D box per stage / per Q; 0: as 2-D boxes
+  int chunked;  // 1: a stage's latent boxes come as one 3-D box; 0: as four 2-D boxes
 };
 
 // One piece: consecutive tiles of one (group, sequence) inside a pair's range.
@@ -218,56 +240,75 @@ __device__ __forceinline__ uint32_t xoff(int row, int u) {
   return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) * 16));
 }
 
-// What a softmax thread needs to ship its partial scores to the peer CTA.
-struct SendCtx {
-  uint32_t tmem, lane_base;
-  int row, hh, lane, gtid;
-};
-
-// Reads this CTA's partial scores of tile kv from TMEM (query row `row`,
-// tokens [32 hh, 32 hh + 32); the queries carry scale * log2(e), so these are
-// in log2 units). They sit in two accumulators, one per half of this CTA's K
-// columns, which two threads issued in parallel; their sum is rounded to
-// fp16 into h and stored straight from registers into the peer's exchange
-// buffer kv & 1 (16-byte st.async stores that count on the peer's mbarrier).
-// Returns true if a wait timed out (then nothing is sent).
-__device__ __forceinline__ bool send_partial(PairSmem& sm, const SendCtx& c, uint32_t kv,
-                                             uint32_t (&h)[16]) {
-  const int sb = kv & 1;
-  bool bad = !mbar_wait(&sm.s_full[sb], (kv >> 1) & 1, WAIT_LIMIT);
+// Sender side of tile kv, for query row `row` (one per lane of the warp's
+// lane quarter): reads this CTA's partial scores of all 64 tokens from the
+// score slot (the queries carry scale * log2(e), so they are in log2
+// units), rounds them to fp16 and writes the fp16 words back into the
+// slot's first 32 columns, for this CTA's softmax, and into the staging
+// buffer. The leader thread then copies the staged tile into the peer's
+// exchange buffer kv & 1 with one bulk copy that counts its bytes on the
+// peer's mbarrier. `bad` carries this thread's earlier timeouts. Returns
+// SEND_STOP in all 128 sender threads if any of them had timed out (then
+// this tile is not processed), SEND_LATE in the leader if its wait for the
+// peer's buffer timed out here (then nothing was sent), else SEND_OK.
+enum SendResult { SEND_OK = 0, SEND_LATE = 1, SEND_STOP = 2 };
+__device__ __forceinline__ SendResult send_tile(PairSmem& sm, uint32_t slot, int row, int lane,
+                                                bool leader, uint32_t kv, uint32_t peer,
+                                                bool bad) {
+  const int b = kv & 1;
+  bad |= !mbar_wait(&sm.s_full[b], (kv >> 1) & 1, WAIT_LIMIT);
+  // The previous tile's copy has to be done reading the staging buffer.
+  if (leader && kv > 0) bulk_wait_read_all();
+  if (named_bar_or(SEND_BAR, 128, bad)) return SEND_STOP;
   tc_fence_after();
+  uint32_t h0[16], h1[16];
+  {
+    float v[4][16];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    float v0[16], v1[16];
-    tmem_ld16(c.tmem + c.lane_base + TM_S + 32 * c.hh + 16 * q, v0);
-    tmem_ld16(c.tmem + c.lane_base + TM_S + 64 + 32 * c.hh + 16 * q, v1);
+    for (int q = 0; q < 4; ++q) tmem_ld16(slot + 16 * q, v[q]);
     tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      h[8 * q + k] = pack_half2(v0[2 * k] + v1[2 * k], v0[2 * k + 1] + v1[2 * k + 1]);
+    for (int k = 0; k < 8; ++k) {
+      h0[k] = pack_half2(v[0][2 * k], v[0][2 * k + 1]);
+      h0[8 + k] = pack_half2(v[1][2 * k], v[1][2 * k + 1]);
+      h1[k] = pack_half2(v[2][2 * k], v[2][2 * k + 1]);
+      h1[8 + k] = pack_half2(v[3][2 * k], v[3][2 * k + 1]);
+    }
   }
-  tc_fence_before();
-  __syncwarp();
-  if (c.lane == 0) mbar_arrive(&sm.s_empty);
-  // The peer's buffer kv & 1 is free once it has consumed tile kv - 2.
-  if (kv >= 2) bad |= !mbar_wait(&sm.x_sendok[sb], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
-  if (c.gtid == 0) mbar_arrive_expect_tx(&sm.x_full[sb], X_BYTES);
-  if (!bad) {
-    const uint32_t peer = cluster_ctarank() ^ 1u;
-    const uint32_t xbuf_peer = mapa_shared(smem_u32(sm.xbuf[sb]), peer);
-    const uint32_t xfull_peer = mapa_shared(smem_u32(&sm.x_full[sb]), peer);
+  tmem_st16u(slot, h0);
+  tmem_st16u(slot + 16, h1);
+  const uint32_t stg = smem_u32(sm.sendbuf);
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      st_async_v4u(xbuf_peer + xoff(c.row, 4 * c.hh + u), h[4 * u], h[4 * u + 1], h[4 * u + 2],
-                   h[4 * u + 3], xfull_peer);
+  for (int u = 0; u < 4; ++u)
+    st_shared_v4(stg + xoff(row, u), h0[4 * u], h0[4 * u + 1], h0[4 * u + 2], h0[4 * u + 3]);
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    st_shared_v4(stg + xoff(row, 4 + u), h1[4 * u], h1[4 * u + 1], h1[4 * u + 2], h1[4 * u + 3]);
+  fence_proxy_async_smem();  // the staged words are read by the bulk copy
+  tmem_wait_st();
+  tc_fence_before();
+  named_bar_sync(SEND_BAR, 128);
+  if (lane == 0) mbar_arrive(&sm.own_ready[b]);
+  bool late = false;
+  if (leader) {
+    // The peer's buffer kv & 1 is free once it has consumed tile kv - 2.
+    if (kv >= 2) late = !mbar_wait(&sm.x_sendok[b], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
+    // this CTA's buffer kv & 1 expects the peer's copy of the same tile
+    mbar_arrive_expect_tx(&sm.x_full[b], X_BYTES);
+    if (!late) {
+      bulk_copy_to_peer(mapa_shared(smem_u32(sm.xbuf[b]), peer), sm.sendbuf, X_BYTES,
+                        mapa_shared(smem_u32(&sm.x_full[b]), peer));
+      bulk_commit();
+    }
   }
-  return bad;
+  return late ? SEND_LATE : SEND_OK;
 }
 
-// Group 0 puts this CTA's Q latent columns 128..255 of the piece's 128 query
-// rows into TMEM (bf16 pairs, row per lane), where the score MMAs read them
-// as their A operand, once the previous piece's score MMAs are done with
-// them. Rows past the end of the queries are zero. Returns true on timeout.
+// The sender warps put this CTA's Q latent columns 64..255 of the piece's
+// 128 query rows into TMEM (bf16 pairs, row per lane), where the score MMAs
+// read them as their A operand, once the previous piece's score MMAs are
+// done with them. Rows past the end of the queries are zero. Returns true on
+// timeout.
 __device__ __forceinline__ bool load_q_tmem(PairSmem& sm, const PairArgs& a, uint32_t tmem,
                                             uint32_t lane_base, int row, int lane, uint32_t rank,
                                             const TileCursor& cur) {
@@ -276,10 +317,10 @@ __device__ __forceinline__ bool load_q_tmem(PairSmem& sm, const PairArgs& a, uin
   tc_fence_after();
   const long long grow =
       static_cast<long long>(cur.pc.b) * a.n_q * a.n_h + cur.pc.g * TP_ROWS + row;
-  const uint4* src = reinterpret_cast<const uint4*>(a.qabs + grow * 576 + 256 * rank + 128);
+  const uint4* src = reinterpret_cast<const uint4*>(a.qabs + grow * 576 + 256 * rank + 64);
   const bool in = grow < a.q_rows;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 6; ++j) {
     uint32_t w[16];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -323,21 +364,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
-    mbar_init(&sm.q_full, 1 + 4);  // TMA bytes + the four TMEM loader warps
-    mbar_init(&sm.q_empty, 2);  // one commit from each score-MMA issuer
-    mbar_init(&sm.s_full[0], 2);             // one commit from each score-MMA issuer
-    mbar_init(&sm.s_full[1], 2);
-    mbar_init(&sm.s_empty, TP_GRP_WARPS);
+    mbar_init(&sm.q_full, 1 + 4);  // TMA bytes + the four sender warps' TMEM part
+    mbar_init(&sm.q_empty, 2);     // one commit from each score-MMA issuer
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_empty[i], TP_SM_WARPS);
+      mbar_init(&sm.own_ready[i], 4);
       mbar_init(&sm.x_full[i], 1);
-      mbar_init(&sm.x_sendok[i], TP_GRP_WARPS);
-      mbar_init(&sm.p_full[i], TP_GRP_WARPS);
+      mbar_init(&sm.x_sendok[i], TP_SM_WARPS);
+      mbar_init(&sm.p_full[i], TP_SM_WARPS);
       mbar_init(&sm.pv_done[i], 1);
-      mbar_init(&sm.m_ready[i], TP_GRP_WARPS);
-      mbar_init(&sm.stats[i], TP_SM_WARPS);
     }
     mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_empty, TP_GRP_WARPS);
+    mbar_init(&sm.o_empty, TP_SM_WARPS);
     for (int i = 0; i < 3; ++i) mbar_init(&sm.drain[i], 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
@@ -363,7 +402,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       const int xr = 512 + 32 * static_cast<int>(rank);
       uint32_t kv_it = 0;
       int piece_idx = 0;
-      uint32_t issued[TP_STAGES] = {0, 0, 0};
+      uint32_t issued[TP_STAGES] = {};
       bool stop = false;
       for (long long it = it_begin; it < it_end && !stop && !aborted(sm);) {
         const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
@@ -373,13 +412,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         }
         const int qrow0 = pc.b * rows_total + pc.g * TP_ROWS;
         mbar_arrive_expect_tx(&sm.q_full, Q_BYTES);
-        if (a.chunked) {
-          tma_load_3d(sm.qc[0], &tmap_qc, 0, qrow0, 4 * static_cast<int>(rank), &sm.q_full);
-        } else {
-          for (int j = 0; j < 2; ++j)
-            tma_load_2d(sm.qc[j], &tmap_qc, 256 * static_cast<int>(rank) + 64 * j, qrow0,
-                        &sm.q_full);
-        }
+        tma_load_2d(sm.qc, &tmap_qc, 256 * static_cast<int>(rank), qrow0, &sm.q_full);
         tma_load_2d(sm.qr, &tmap_qr, xr, qrow0, &sm.q_full);
         const int32_t* pt = a.page_table + static_cast<size_t>(pc.b) * a.max_blocks;
         int page_next = pt[pc.t_first];
@@ -421,6 +454,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   } else if (warp == 1) {
     // ------------------------------------------------------------ value-MMA issuer
     // O (this CTA's 256 latent columns) += P C, with P read from TMEM.
+    // pv_done[t & 1] tells the softmax when the P buffer and O are free.
     if (lane == 0) {
       const uint32_t idPV = idesc_bf16_f32(128, 256, false, true);
       // C as the MN-major B operand: latent columns are contiguous (64 per
@@ -441,7 +475,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         }
         tc_fence_after();
         const int s = t % TP_STAGES;
-        const uint32_t pcol = tmem + TM_P + 32 * (t & 1);
+        const uint32_t pcol = tmem + TM_P;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ts(tmem + TM_O, pcol + 8 * kk, dC0 + s * kStageDesc + ((2048u * kk) >> 4), idPV,
@@ -455,17 +489,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mma_commit(&sm.drain[0]);
       mbar_wait(&sm.drain[0], 0, WAIT_LIMIT);
     }
-  } else if (warp < TP_SM_WARP0) {
+  } else if (warp < TP_SEND_WARP0) {
     // ------------------------------------------------------------ score-MMA issuers
-    // Each tile's 18 K-steps are split between warp 2 (latent steps 0..8)
-    // and warp 3 (latent steps 9..15 and the 2 rotary steps), into two
-    // accumulators that the softmax adds. Two threads hide each other's
-    // issue latency, which halves the time from a tile's arrival to its
-    // scores.
+    // Warp 2 issues the even tiles into score slot 0, warp 3 the odd tiles
+    // into slot 1, each as one accumulation of 18 K-steps: latent steps 0..3
+    // with Q from shared memory, 4..15 with Q from TMEM, then the two rotary
+    // steps. Two issuers keep the tensor pipe fed while either waits.
     if (lane == 0) {
-      const uint32_t half = static_cast<uint32_t>(warp - 2);  // 0 or 1
+      const uint32_t half = static_cast<uint32_t>(warp - 2);  // tile parity
       const uint32_t idS = idesc_bf16_f32(128, TP_TOK, false, false);
-      const uint64_t dQc = smem_desc(smem_u32(sm.qc[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dQc = smem_desc(smem_u32(sm.qc), 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(smem_u32(sm.qr), 16, 512, kSwizzle64B);
       const uint64_t dKc0 = smem_desc(smem_u32(sm.kv[0].c[0]), 16, 1024, kSwizzle128B);
       const uint64_t dKr0 = smem_desc(smem_u32(sm.kv[0].r), 16, 512, kSwizzle64B);
@@ -475,38 +508,34 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       TileCursor cur;
       cur.init(it_begin, it_end, a);
       while (cur.valid() && ok) {
-        // one piece: wait for its Q, issue this thread's share of each tile, release Q
+        // one piece: wait for its Q, issue this parity's tiles, release Q
         if (!mbar_wait(&sm.q_full, cur.piece & 1, WAIT_LIMIT)) { ok = false; break; }
         tc_fence_after();
         const int piece = cur.piece;
         for (; cur.valid() && cur.piece == piece; cur.next(a)) {
           const uint32_t t = cur.kv;
-          if (t >= 1 && !mbar_wait(&sm.s_empty, (t - 1) & 1, WAIT_LIMIT)) { ok = false; break; }
+          if ((t & 1) != half) continue;
+          if (t >= 2 && !mbar_wait(&sm.s_empty[half], ((t >> 1) - 1) & 1, WAIT_LIMIT)) {
+            ok = false;
+            break;
+          }
           const int s = t % TP_STAGES;
           if (!mbar_wait(&sm.kv_full[s], (t / TP_STAGES) & 1, WAIT_LIMIT)) { ok = false; break; }
           tc_fence_after();
-          if (half == 0) {
+          const uint64_t dK = dKc0 + s * kStageDesc;
 #pragma unroll
-            for (int k = 0; k < 9; ++k) {
-              const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-              if (k < 8) {  // Q from shared memory
-                const uint32_t off = (QC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-                mma_bf16_ss(dS, dQc + off, dKc0 + s * kStageDesc + koff, idS, k > 0 ? 1u : 0u);
-              } else {      // Q from TMEM
-                mma_bf16_ts(dS, tmem + TM_Q, dKc0 + s * kStageDesc + koff, idS, 1u);
-              }
-            }
-          } else {
+          for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(dS, dQc + ((32u * k) >> 4), dK + ((32u * k) >> 4), idS, k > 0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 9; k < 16; ++k) {
-              const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
-              mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 8), dKc0 + s * kStageDesc + koff, idS, k > 9 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr0 + s * kStageDesc + ((32u * k) >> 4), idS, 1u);
+          for (int k = 4; k < 16; ++k) {
+            const uint32_t koff = (KC_BOX * (k >> 2) + 32 * (k & 3)) >> 4;
+            mma_bf16_ts(dS, tmem + TM_Q + 8 * (k - 4), dK + koff, idS, 1u);
           }
-          mma_commit(&sm.s_full[t & 1]);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_bf16_ss(dS, dQr + ((32u * k) >> 4), dKr0 + s * kStageDesc + ((32u * k) >> 4), idS,
+                        1u);
+          mma_commit(&sm.s_full[half]);
         }
         if (!ok) break;
         mma_commit(&sm.q_empty);
@@ -515,86 +544,102 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       mma_commit(&sm.drain[1 + half]);
       mbar_wait(&sm.drain[1 + half], 0, WAIT_LIMIT);
     }
-  } else {
-    // ------------------------------------------------------------ softmax warps 4..19
-    // Group g = (w - 4) / 8 handles the tiles with kv % 2 == g, so one group's
-    // exchange and softmax overlap the other's. Inside a group, warp w reads
-    // TMEM lane quarter w % 4 (query rows 32 (w % 4) .. +31, one row per lane)
-    // and score columns [32 hh, 32 hh + 32), hh = ((w - 4) / 4) % 2. The two
-    // warps of a lane quarter agree on the row maximum at a 64-thread named
-    // barrier. The running max is handed from tile to tile, across the two
-    // groups, through shared memory (mrow, m_ready). Each warp keeps the sum
-    // of its half rows, referred to the max its group last used; the
-    // epilogue merges the four sums of a row.
-    const int sw = warp - TP_SM_WARP0;           // 0..15
-    const int grp = sw >> 3;
-    const int hh = (sw >> 2) & 1;
+  } else if (warp < TP_SM_WARP0) {
+    // ------------------------------------------------------------ sender warps 4..7
     const int qd = warp & 3;
-    const uint32_t bar_id = 1 + 4 * grp + qd;   // 64-thread barrier of the two halves
     const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
     const int row = 32 * qd + lane;
-    const int gtid = (sw & 7) * 32 + lane;      // 0..255 inside the group
-    const SendCtx sx{tmem, lane_base, row, hh, lane, gtid};
+    const bool leader = warp == TP_SEND_WARP0 && lane == 0;
+    bool bad = false;
     TileCursor cur;
     cur.init(it_begin, it_end, a);
-    float l = 0.f, mref = -INFINITY;  // this warp's half-row sum and the max it refers to
+    // The four warps meet at named barriers inside send_tile, which merge
+    // their timeout flags, so they leave the loop together.
+    for (; cur.valid(); cur.next(a)) {
+      if (cur.first()) bad |= load_q_tmem(sm, a, tmem, lane_base, row, lane, rank, cur);
+      const uint32_t kv = cur.kv;
+      const SendResult r = send_tile(sm, tmem + lane_base + TM_S + 64 * (kv & 1), row, lane,
+                                     leader, kv, peer, bad);
+      bad = r != SEND_OK;
+      if (r == SEND_STOP) break;
+    }
+    if (leader) bulk_wait_all();  // the last copies land before the peer may leave
+    if (bad && lane == 0) note_timeout(sm, a.err);
+  } else {
+    // ------------------------------------------------------------ softmax warps 8..15
+    // Warp w reads TMEM lane quarter w % 4 (query rows 32 (w % 4) .. +31, one
+    // row per lane) and tokens [32 hh, 32 hh + 32), hh = (w - 8) / 4. The two
+    // warps of a lane quarter agree on the row maximum at a 64-thread named
+    // barrier; each keeps the sum of its half rows, referred to the running
+    // max m, which both hold in registers.
+    const int sw = warp - TP_SM_WARP0;          // 0..7
+    const int hh = sw >> 2;
+    const int qd = warp & 3;
+    const uint32_t bar_id = 1 + qd;             // 64-thread barrier of the two halves
+    const uint32_t lane_base = static_cast<uint32_t>(qd * 32) << 16;
+    const int row = 32 * qd + lane;
+    const int gtid = sw * 32 + lane;            // 0..255
+    TileCursor cur;
+    cur.init(it_begin, it_end, a);
+    float l = 0.f, m = -INFINITY;
     int L = 0, rows_valid = 0, pos_q = 0;
     bool row_ok = false, bad = false;
-    for (; cur.valid() && !bad; cur.next(a)) {
+    // The two warps of a lane quarter leave the loop together, right after a
+    // pair barrier has merged their timeout flags, so neither can be left
+    // waiting at a named barrier.
+    for (; cur.valid(); cur.next(a)) {
       const uint32_t kv = cur.kv;
+      const int b = kv & 1;
       const bool first = cur.first();
       if (first) {
         l = 0.f;
-        mref = -INFINITY;
+        m = -INFINITY;
         L = a.seq_lens[cur.pc.b];
         rows_valid = min(TP_ROWS, rows_total - cur.pc.g * TP_ROWS);
         row_ok = row < rows_valid;
         pos_q = L - a.n_q + (row_ok ? (cur.pc.g * TP_ROWS + row) / a.n_h : 0);
-        if (grp == 0 && hh == 0) bad |= load_q_tmem(sm, a, tmem, lane_base, row, lane, rank, cur);
-      }
-      if ((kv & 1) != static_cast<uint32_t>(grp)) {
-        // The other group's tile. At the end of a piece, hand over this
-        // warp's row sums, once that tile has published its max: this keeps
-        // the two groups at most one piece apart, which the two stats
-        // barriers (one per piece parity) rely on.
-        if (cur.last()) {
-          bad |= !mbar_wait(&sm.m_ready[kv & 1], (kv >> 1) & 1, WAIT_LIMIT);
-          sm.st_l[grp][hh][row] = l;
-          if (hh == 0) sm.st_m[grp][row] = mref;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
-        }
-        continue;
       }
       const int t = cur.tile();
       const int s2 = kv % TP_STAGES;
-      uint32_t own[16];
-      bad |= send_partial(sm, sx, kv, own);
 
-      // 1. full scaled scores = own partial + the peer's (both fp16-rounded)
-      const int xb = kv & 1;
-      bad |= !mbar_wait(&sm.x_full[xb], (kv >> 1) & 1, WAIT_LIMIT);
+      // 1. full scaled scores = own fp16 partial (written back into the score
+      // slot by the sender warps) + the peer's (from the exchange buffer)
+      bad |= !mbar_wait(&sm.own_ready[b], (kv >> 1) & 1, WAIT_LIMIT);
+      bad |= !mbar_wait(&sm.x_full[b], (kv >> 1) & 1, WAIT_LIMIT);
+      bad = __any_sync(0xffffffffu, bad);
+      tc_fence_after();
       float sc[32];
       {
-        const uint8_t* xin = reinterpret_cast<const uint8_t*>(sm.xbuf[xb]);
+        float ow[16];
+        tmem_ld16(tmem + lane_base + TM_S + 64 * b + 16 * hh, ow);
+        const uint8_t* xin = reinterpret_cast<const uint8_t*>(sm.xbuf[b]);
+        uint4 pv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pv[u] = *reinterpret_cast<const uint4*>(xin + xoff(row, 4 * hh + u));
+        tmem_wait_ld();
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 pv = *reinterpret_cast<const uint4*>(xin + xoff(row, 4 * hh + u));
-          const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+          const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const float2 x0 = unpack_half2(own[4 * u + w]), x1 = unpack_half2(pw[w]);
+            const float2 x0 = unpack_half2(__float_as_uint(ow[4 * u + w]));
+            const float2 x1 = unpack_half2(pw[w]);
             sc[8 * u + 2 * w] = x0.x + x1.x;
             sc[8 * u + 2 * w + 1] = x0.y + x1.y;
           }
         }
       }
+      tc_fence_before();
       __syncwarp();
-      // At the end of a piece the epilogue borrows this exchange buffer, so
-      // the peer may only refill it afterwards.
-      if (lane == 0 && !cur.last()) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[xb]), peer));
+      if (lane == 0) {
+        mbar_arrive(&sm.s_empty[b]);  // the score slot may take tile kv + 2
+        // At the end of a piece the epilogue borrows this exchange buffer, so
+        // the peer may only refill it afterwards.
+        if (!cur.last()) mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[b]), peer));
+      }
 
-      // 2. causal mask, row max (both halves), running max from the previous tile
+      // 2. causal mask, row max (both halves), running max
       const int j0 = t * TP_TOK + 32 * hh;  // token of sc[0]
       if (!(row_ok && j0 + 31 <= L - a.n_q)) {
 #pragma unroll
@@ -605,27 +650,24 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       for (int u = 0; u < 4; ++u)
         pm[u] = fmaxf(fmaxf(fmaxf(sc[8 * u], sc[8 * u + 1]), fmaxf(sc[8 * u + 2], sc[8 * u + 3])),
                       fmaxf(fmaxf(sc[8 * u + 4], sc[8 * u + 5]), fmaxf(sc[8 * u + 6], sc[8 * u + 7])));
-      sm.xmax[grp][hh][row] = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
-      if (kv > 0) bad |= !mbar_wait(&sm.m_ready[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+      sm.xmax[b][hh][row] = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
       if (named_bar_or(bar_id, 64, bad)) {
         bad = true;
         break;
       }
-      const float pmax = fmaxf(sm.xmax[grp][0][row], sm.xmax[grp][1][row]);
-      const float m_prev = first ? -INFINITY : sm.mrow[(kv - 1) & 1][row];
-      const float m_new = fmaxf(m_prev, pmax);
-      const bool need = !first && row_ok && (m_new > m_prev + RESCALE_THRESHOLD);
-      const float m_use = (first || need) ? m_new : m_prev;
-      if (hh == 0) sm.mrow[kv & 1][row] = m_use;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.m_ready[kv & 1]);
+      const float pmax = fmaxf(sm.xmax[b][0][row], sm.xmax[b][1][row]);
+      const float m_old = m;
+      const float m_new = fmaxf(m_old, pmax);
+      const bool need = !first && row_ok && (m_new > m_old + RESCALE_THRESHOLD);
+      const float m_use = (first || need) ? m_new : m_old;
       // A row with nothing visible yet keeps m_use = -inf; subtracting 0
       // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
 
-      // 3. P (bf16 pairs) into its TMEM buffer, once the value MMA two tiles
-      // back has read that buffer
-      if (kv >= 2) bad |= !mbar_wait(&sm.pv_done[kv & 1], ((kv >> 1) - 1) & 1, WAIT_LIMIT);
+      // 3. P (bf16 pairs) into the TMEM buffer, once the previous tile's
+      // value MMA has read it
+      if (kv >= 1) bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+      bad = __any_sync(0xffffffffu, bad);
       tc_fence_after();
       {
         float psum = 0.f;
@@ -638,21 +680,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           w[k] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        if (!__any_sync(0xffffffffu, bad))
-          tmem_st16u(tmem + lane_base + TM_P + 32 * (kv & 1) + 16 * hh, w);
+        if (!bad) tmem_st16u(tmem + lane_base + TM_P + 16 * hh, w);
         tmem_wait_st();
-        if (row_ok) {
-          l = (mref == -INFINITY) ? psum : l * fast_exp2(mref - m_use) + psum;
-          mref = m_use;
-        }
+        if (row_ok) l = (m_old == -INFINITY) ? psum : l * fast_exp2(m_old - m_use) + psum;
+        m = m_use;
       }
-      // 4. lazy rescale of this warp's rows of O (its half of the columns),
-      // after P so that the scores are no longer live
+      // 4. lazy rescale of this warp's rows of O (its half of the columns);
+      // the previous tile's value MMA is done with O (waited for above)
       if (__any_sync(0xffffffffu, need)) {
-        bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
-        tc_fence_after();
-        if (!__any_sync(0xffffffffu, bad)) {
-          const float f = need ? fast_exp2(m_prev - m_use) : 1.f;
+        if (!bad) {
+          const float f = need ? fast_exp2(m_old - m_use) : 1.f;
           for (int c0 = 0; c0 < 128; c0 += 16) {
             float v[16];
             const uint32_t ta = tmem + lane_base + TM_O + 128 * hh + c0;
@@ -672,7 +709,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       if (jt + TP_TOK > L) {
         const int r0 = max(L - jt, 0);            // first invalid row in this tile
         const int n16 = (TP_TOK - r0) * 4 * 8;    // rows x boxes x 16-byte units
-        for (int i2 = gtid; i2 < n16; i2 += TP_GRP_WARPS * 32) {
+        for (int i2 = gtid; i2 < n16; i2 += TP_SM_WARPS * 32) {
           const int rr = r0 + i2 / 32, box = (i2 / 8) % 4, u = i2 % 8;
           *reinterpret_cast<uint4*>(sm.kv[s2].c[box] + rr * 128 + u * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -680,35 +717,26 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[kv & 1]);
+      if (lane == 0) mbar_arrive(&sm.p_full[b]);
 
       if (cur.last()) {
-        // ---- epilogue of the piece (done by the group of its last tile):
-        // O / l -> workspace slot
-        sm.st_l[grp][hh][row] = l;
-        if (hh == 0) sm.st_m[grp][row] = mref;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.stats[cur.piece & 1]);
-        bad |= !mbar_wait(&sm.stats[cur.piece & 1], (cur.piece >> 1) & 1, WAIT_LIMIT);
+        // ---- epilogue of the piece: O / l -> workspace slot
+        sm.st_l[hh][row] = l;
+        if (named_bar_or(bar_id, 64, bad)) bad = true;
         bad |= !mbar_wait(&sm.o_full, cur.piece & 1, WAIT_LIMIT);
+        bad = __any_sync(0xffffffffu, bad);
         tc_fence_after();
-        float lt = 0.f;
-#pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-          const float mg = sm.st_m[g2][row];
-          if (mg != -INFINITY)
-            lt += (sm.st_l[g2][0][row] + sm.st_l[g2][1][row]) * fast_exp2(mg - m_use);
-        }
+        const float lt = sm.st_l[0][row] + sm.st_l[1][row];
         const float inv_l = (row_ok && lt > 0.f) ? 1.f / lt : 0.f;
         const int slot = pair + cur.pc.g * a.B + cur.pc.b;
         if (rank == 0 && hh == 0 && row_ok)
           a.part_lse[static_cast<size_t>(slot) * TP_ROWS + row] =
-              lt > 0.f ? (m_use + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+              lt > 0.f ? (m + log2f(lt)) * 0.6931471805599453f : -INFINITY;
         // O / l goes out 16 columns at a time through this warp's 2 KB of
         // the (already consumed) exchange buffer: each lane writes its row,
         // then each store instruction covers two 64-byte row segments.
-        if (!__any_sync(0xffffffffu, bad)) {
-          uint8_t* stg = reinterpret_cast<uint8_t*>(sm.xbuf[xb]) + (sw & 7) * 2048;
+        if (!bad) {
+          uint8_t* stg = reinterpret_cast<uint8_t*>(sm.xbuf[b]) + sw * 2048;
           const int rsub = lane >> 4, csub = lane & 15;
           float* dst0 = a.part_o + (static_cast<size_t>(slot) * TP_ROWS + 32 * qd + rsub) * 512 +
                         256 * rank + 128 * hh + csub;
@@ -742,7 +770,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sm.o_empty);
-          mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[xb]), peer));  // the exchange buffer is free again
+          mbar_arrive_remote_relaxed(mapa_shared(smem_u32(&sm.x_sendok[b]), peer));  // the exchange buffer is free again
         }
       }
     }
@@ -850,20 +878,16 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * TP_TOK;
   TmapSpec sp;
   CUtensorMap tqc, tqr, tkc, tkr;
-  // One 3-D box per latent half; if the driver does not take that view,
-  // plain 2-D boxes of 64 columns.
-  bool chunked = true;
-  chunks_map(&sp, ws.qabs, q_rows, 128, 2);
-  if (!get_tmap(sp, &tqc)) chunked = false;
+  rows_map(&sp, ws.qabs, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!get_tmap(sp, &tqc)) return cudaErrorInvalidValue;
   rows_map(&sp, ws.qabs, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!get_tmap(sp, &tqr)) return cudaErrorInvalidValue;
-  if (chunked) {
-    chunks_map(&sp, cache, kv_rows, 64, 4);
-    if (!get_tmap(sp, &tkc)) chunked = false;
-  }
+  // A stage's four latent boxes as one 3-D box; if the driver does not take
+  // that view, four 2-D boxes.
+  bool chunked = true;
+  chunks_map(&sp, cache, kv_rows, 64, 4);
+  if (!get_tmap(sp, &tkc)) chunked = false;
   if (!chunked) {
-    rows_map(&sp, ws.qabs, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!get_tmap(sp, &tqc)) return cudaErrorInvalidValue;
     rows_map(&sp, cache, kv_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!get_tmap(sp, &tkc)) return cudaErrorInvalidValue;
   }
