@@ -39,8 +39,8 @@
 // buffer for P (bf16 pairs, read by the value MMA straight from TMEM as its
 // A operand), 96 columns of Q (192 of this CTA's latent columns) and the
 // 256-column latent accumulator. After the sender warps have read a score
-// slot they write the fp16-rounded partial back into its first 32 columns,
-// where the softmax warps pick up their own half of the sum.
+// slot they write the fp16-rounded partial back into it (as fp32), where
+// the softmax warps pick up their own half of the sum.
 //
 // The partials travel by the bulk-copy engine (cp.async.bulk from a local
 // staging buffer into the peer's exchange buffer), not by st.async from
@@ -57,8 +57,9 @@
 //               tiles, each into its own score slot
 //   warps 4..7  senders: warp w reads the score slot's lane quarter w % 4
 //               (one query row per lane, all 64 tokens), rounds the partial
-//               to fp16, writes it back to TMEM and into the staging
-//               buffer, from which one thread copies it to the peer. They
+//               to fp16, writes the rounded values back to TMEM and the fp16
+//               words into the staging buffer, from which one thread copies
+//               them to the peer. They
 //               also put the TMEM part of Q in place at each piece.
 //   warps 8..15 softmax: warp w reads lane quarter w % 4 and tokens
 //               [32h, 32h + 32), h = (w - 8) / 4. The two warps of a lane
@@ -235,6 +236,19 @@ __device__ __forceinline__ float2 unpack_half2(uint32_t u) {
   return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
+// (fp32) of the low / high fp16 half of u, plus c0 / c1, rounded once: the
+// fp16 value converts exactly, so this is the fp32 sum of the two values.
+__device__ __forceinline__ float2 add_half2_f32(uint32_t u, float c0, float c1) {
+  float d0, d1;
+  asm("{\n\t.reg .f16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %3;\n\t"
+      "add.rn.f32.f16 %1, hi, %4;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(u), "f"(c0), "f"(c1));
+  return make_float2(d0, d1);
+}
+
 // Byte offset of 16-byte unit u (0..7) of query row `row` in an exchange buffer.
 __device__ __forceinline__ uint32_t xoff(int row, int u) {
   return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) * 16));
@@ -243,8 +257,8 @@ __device__ __forceinline__ uint32_t xoff(int row, int u) {
 // Sender side of tile kv, for query row `row` (one per lane of the warp's
 // lane quarter): reads this CTA's partial scores of all 64 tokens from the
 // score slot (the queries carry scale * log2(e), so they are in log2
-// units), rounds them to fp16 and writes the fp16 words back into the
-// slot's first 32 columns, for this CTA's softmax, and into the staging
+// units), rounds them to fp16, writes the rounded values back into the slot
+// (as fp32) for this CTA's softmax and the fp16 words into the staging
 // buffer. The leader thread then copies the staged tile into the peer's
 // exchange buffer kv & 1 with one bulk copy that counts its bytes on the
 // peer's mbarrier. `bad` carries this thread's earlier timeouts. Returns
@@ -262,21 +276,26 @@ __device__ __forceinline__ SendResult send_tile(PairSmem& sm, uint32_t slot, int
   if (named_bar_or(SEND_BAR, 128, bad)) return SEND_STOP;
   tc_fence_after();
   uint32_t h0[16], h1[16];
-  {
-    float v[4][16];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tmem_ld16(slot + 16 * q, v[q]);
+  for (int half = 0; half < 2; ++half) {
+    float v0[16], v1[16];
+    tmem_ld16(slot + 32 * half, v0);
+    tmem_ld16(slot + 32 * half + 16, v1);
     tmem_wait_ld();
+    uint32_t (&h)[16] = half ? h1 : h0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      h0[k] = pack_half2(v[0][2 * k], v[0][2 * k + 1]);
-      h0[8 + k] = pack_half2(v[1][2 * k], v[1][2 * k + 1]);
-      h1[k] = pack_half2(v[2][2 * k], v[2][2 * k + 1]);
-      h1[8 + k] = pack_half2(v[3][2 * k], v[3][2 * k + 1]);
+      h[k] = pack_half2(v0[2 * k], v0[2 * k + 1]);
+      h[8 + k] = pack_half2(v1[2 * k], v1[2 * k + 1]);
+      const float2 r0 = unpack_half2(h[k]), r1 = unpack_half2(h[8 + k]);
+      v0[2 * k] = r0.x;
+      v0[2 * k + 1] = r0.y;
+      v1[2 * k] = r1.x;
+      v1[2 * k + 1] = r1.y;
     }
+    tmem_st16(slot + 32 * half, v0);
+    tmem_st16(slot + 32 * half + 16, v1);
   }
-  tmem_st16u(slot, h0);
-  tmem_st16u(slot + 16, h1);
   const uint32_t stg = smem_u32(sm.sendbuf);
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -602,16 +621,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       const int t = cur.tile();
       const int s2 = kv % TP_STAGES;
 
-      // 1. full scaled scores = own fp16 partial (written back into the score
-      // slot by the sender warps) + the peer's (from the exchange buffer)
+      // 1. full scaled scores = own fp16-rounded partial (written back into
+      // the score slot by the sender warps) + the peer's (exchange buffer)
       bad |= !mbar_wait(&sm.own_ready[b], (kv >> 1) & 1, WAIT_LIMIT);
       bad |= !mbar_wait(&sm.x_full[b], (kv >> 1) & 1, WAIT_LIMIT);
       bad = __any_sync(0xffffffffu, bad);
       tc_fence_after();
       float sc[32];
       {
-        float ow[16];
-        tmem_ld16(tmem + lane_base + TM_S + 64 * b + 16 * hh, ow);
+        float ow[2][16];
+        tmem_ld16(tmem + lane_base + TM_S + 64 * b + 32 * hh, ow[0]);
+        tmem_ld16(tmem + lane_base + TM_S + 64 * b + 32 * hh + 16, ow[1]);
         const uint8_t* xin = reinterpret_cast<const uint8_t*>(sm.xbuf[b]);
         uint4 pv[4];
 #pragma unroll
@@ -623,10 +643,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
           const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const float2 x0 = unpack_half2(__float_as_uint(ow[4 * u + w]));
-            const float2 x1 = unpack_half2(pw[w]);
-            sc[8 * u + 2 * w] = x0.x + x1.x;
-            sc[8 * u + 2 * w + 1] = x0.y + x1.y;
+            const int c = 8 * u + 2 * w;
+            const float2 x = add_half2_f32(pw[w], ow[c >> 4][c & 15], ow[c >> 4][(c & 15) + 1]);
+            sc[c] = x.x;
+            sc[c + 1] = x.y;
           }
         }
       }
