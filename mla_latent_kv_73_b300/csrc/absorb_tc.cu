@@ -14,10 +14,12 @@
 // tcgen05: one CTA per (head, up to 128 query tokens). TMA stages the head's
 // whole W_uk slice (128 KB, eight 128 x 64 boxes) and the tokens' q_nope
 // (a 3-D box over [token][head][dim]) into shared memory in one go, so the
-// weight stream has 128 KB in flight per SM. One thread issues 32 MMAs with
-// M = 128 latent rows, N = tokens, K = 128, accumulating q_lat^T in TMEM
-// (4 blocks of up to 128 columns). Four warps read it back, one latent row per
-// lane, and store bf16. The other four warps rotate q_rope meanwhile.
+// weight stream has 128 KB in flight per SM. Four threads (one per 128-row
+// block of W_uk[h], each starting as soon as its two boxes have landed) issue
+// 8 MMAs each with M = 128 latent rows, N = tokens, K = 128, accumulating
+// q_lat^T in TMEM (4 blocks of up to 128 columns). Four warps read it back,
+// one latent row per lane, and store bf16. The other four warps rotate
+// q_rope meanwhile.
 //
 // Block (0, 0) also writes the split-KV plan (tiles per sequence and their
 // prefix sum), which the attention and combine kernels read.
@@ -39,7 +41,7 @@ constexpr long long AT_WAIT = 2000000000LL;    // ~1 s
 struct __align__(1024) AbsSmem {
   uint8_t w[8][AT_WBOX];          // box (M-block j, K-chunk kc) at index 2*j + kc
   uint8_t q[2][AT_TOK * 128];     // K-chunk kc: token rows of 128 B
-  uint64_t full, done;
+  uint64_t full_q, full_w[4], done;
   uint32_t tmem_base;
 };
 
@@ -68,8 +70,9 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   constexpr int R = 576, DQ = 192;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sm.full, 1);
-    mbar_init(&sm.done, 1);
+    mbar_init(&sm.full_q, 1);
+    for (int j = 0; j < 4; ++j) mbar_init(&sm.full_w[j], 1);
+    mbar_init(&sm.done, 4);  // one commit per 128-row block
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -85,27 +88,29 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_q);
-    mbar_arrive_expect_tx(&sm.full, 8 * AT_WBOX + 2 * n_tok_box * 128);
-    for (int j = 0; j < 4; ++j)
+    mbar_arrive_expect_tx(&sm.full_q, 2 * n_tok_box * 128);
+    for (int kc = 0; kc < 2; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full_q);
+    for (int j = 0; j < 4; ++j) {
+      mbar_arrive_expect_tx(&sm.full_w[j], 2 * AT_WBOX);
       for (int kc = 0; kc < 2; ++kc)
-        tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full);
-    for (int kc = 0; kc < 2; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full);
+        tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full_w[j]);
+    }
   }
-  if (warp == 1 && lane == 0) {
-    ok = mbar_wait(&sm.full, 0, AT_WAIT);
+  if (warp < 4 && lane == 0) {
+    // block j = warp of q_lat^T, as soon as its rows of W_uk[h] are in
+    const int j = warp;
+    ok = mbar_wait(&sm.full_q, 0, AT_WAIT) && mbar_wait(&sm.full_w[j], 0, AT_WAIT);
     if (ok) {
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, n_tok_box, false, false);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16_ss(tmem + 128 * j, kdesc(sm.w[2 * j + (k >> 2)], (k & 3) * 32),
-                      kdesc(sm.q[k >> 2], (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
-      mma_commit(&sm.done);
+      for (int k = 0; k < 8; ++k)
+        mma_bf16_ss(tmem + 128 * j, kdesc(sm.w[2 * j + (k >> 2)], (k & 3) * 32),
+                    kdesc(sm.q[k >> 2], (k & 3) * 32), idesc, k > 0 ? 1u : 0u);
     } else {
       set_error(err, MLA_DEVERR_TIMEOUT);
     }
+    mma_commit(&sm.done);
   }
 
   if (warp >= 4) {

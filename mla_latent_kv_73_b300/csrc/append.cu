@@ -23,6 +23,7 @@
 // so one thread (gemm) or one CTA (gemv) always holds both halves of a pair.
 #include "device_common.cuh"
 #include "sm100_ptx.cuh"
+#include "tmap.h"
 
 namespace mla {
 namespace {
@@ -324,10 +325,254 @@ append_gemm_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
   }
 }
 
+// ---- tensor-core split-K path for decode-sized batches of bf16 tokens ----
+//
+// D[R x T] = Wp[R x d_model] x^T. The R packed columns are cut into blocks of
+// 128 (MMA M; TMA zero-fills the rows past R) and d_model into KC slices (KC
+// = 16, or 8 where clusters of 16 cannot be resident), one CTA each. The KC
+// CTAs of a column block form one cluster: each stages its weight slice (the
+// only large read) and the tokens' matching hidden-state slice with TMA,
+// multiplies them into TMEM (N = tokens), and parks the fp32 partial in
+// shared memory. After a cluster barrier CTA r sums rows [r 128/KC,
+// (r + 1) 128/KC) over all KC partials through distributed shared memory
+// (fixed order, so the result does not depend on timing), applies RoPE to the
+// rotary pairs (adjacent rows of the packed weight) and writes the cache
+// entries.
+constexpr int AT_THREADS = 128;
+constexpr uint32_t AT_WBOX = 128 * 128;  // 128 rows x 64 bf16
+constexpr long long AT_WAIT = 2000000000LL;
+
+__device__ __forceinline__ uint64_t at_desc(const uint8_t* p, uint32_t byte_off) {
+  using namespace mla_ptx;
+  return smem_desc(smem_u32(p) + byte_off, 16, 1024, kSwizzle128B);
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                 Shape s, int kcn, int nkb, int N, uint32_t tmem_cols,
+                 __nv_bfloat16* __restrict__ cache, AppendArgs a) {
+  using namespace mla_ptx;
+  extern __shared__ uint8_t at_raw[];
+  uint8_t* A = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  uint8_t* X = A + nkb * AT_WBOX;                             // nkb boxes of N rows x 128 B
+  float* red = reinterpret_cast<float*>(X + nkb * N * 128);   // [128 rows][N] fp32 partial
+  __shared__ uint64_t full, done;
+  __shared__ uint32_t tmem_base;
+  const uint32_t kc = cluster_ctarank();
+  const int mb = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int R = s.R();
+  if (threadIdx.x == 0) {
+    mbar_init(&full, 1);
+    mbar_init(&done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_x);
+    mbar_arrive_expect_tx(&full, nkb * (AT_WBOX + N * 128));
+    const int k0 = static_cast<int>(kc) * nkb * 64;
+    for (int j = 0; j < nkb; ++j) {
+      tma_load_2d(A + j * AT_WBOX, &tmap_w, k0 + 64 * j, mb * 128, &full);
+      tma_load_2d(X + j * N * 128, &tmap_x, k0 + 64 * j, 0, &full);
+    }
+    if (mbar_wait(&full, 0, AT_WAIT)) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
+      for (int j = 0; j < nkb; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16_ss(tmem, at_desc(A + j * AT_WBOX, 32 * k), at_desc(X + j * N * 128, 32 * k),
+                      idesc, (j > 0 || k > 0) ? 1u : 0u);
+    } else {
+      set_error(a.err, MLA_DEVERR_TIMEOUT);
+    }
+    mma_commit(&done);  // arrives once the MMAs (if any) are done
+  }
+  // partial of this K slice: row (packed column) per lane, token per TMEM column
+  const bool ok = mbar_wait(&done, 0, 2 * AT_WAIT);
+  tc_fence_after();
+  {
+    const int row = 32 * warp + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + lane_base + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) red[row * N + c0 + i] = ok ? v[i] : 0.f;
+    }
+  }
+  if (!ok && threadIdx.x == 0) set_error(a.err, MLA_DEVERR_TIMEOUT);
+  tc_fence_before();
+  cluster_sync();  // every partial of the cluster is in place
+  // CTA kc reduces its 128 / kcn rows: row pairs x N tokens
+  const int rows = 128 / kcn;
+  for (int it = threadIdx.x; it < (rows / 2) * N; it += AT_THREADS) {
+    const int pr = it / N, t = it % N;
+    const int r0 = rows * static_cast<int>(kc) + 2 * pr;  // even row of the pair
+    const int pc0 = mb * 128 + r0;
+    if (t >= a.T || pc0 >= R) continue;
+    float p0[16], p1[16];
+#pragma unroll
+    for (int src = 0; src < 16; ++src) {
+      if (src < kcn) {
+        const float* r = map_to_rank(red, static_cast<uint32_t>(src));
+        p0[src] = r[r0 * N + t];
+        p1[src] = r[(r0 + 1) * N + t];
+      } else {
+        p0[src] = p1[src] = 0.f;
+      }
+    }
+    float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+    for (int src = 0; src < 16; ++src) {
+      v0 += p0[src];
+      v1 += p1[src];
+    }
+    const long long row = append_row(a, s, t);
+    if (row < 0) continue;
+    float out;
+    int dst = finish_column(s, a.inv_freq, pc0, v0, v0, v1, a.pos[t], &out);
+    cache[row * R + dst] = __float2bfloat16_rn(out);
+    if (pc0 + 1 < R) {
+      dst = finish_column(s, a.inv_freq, pc0 + 1, v1, v0, v1, a.pos[t], &out);
+      cache[row * R + dst] = __float2bfloat16_rn(out);
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its partial
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// Dynamic shared memory of append_tc_kernel for N tokens and nkb boxes.
+size_t append_tc_smem(int nkb, int N) {
+  return 1024 + static_cast<size_t>(nkb) * (AT_WBOX + N * 128) + static_cast<size_t>(128) * N * 4;
+}
+
+// Whether clusters of kcn CTAs of append_tc_kernel, each with `smem` bytes,
+// can be resident.
+bool append_tc_clusters_ok(int kcn, size_t smem) {
+  // (the kernel's few static bytes count against the same 227 KB, so the
+  // dynamic limit is raised to what this launch needs, not to the maximum)
+  static size_t attr_bytes[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || attr_bytes[dev] < smem) {
+    if (cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess ||
+        cudaFuncSetAttribute(append_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (dev >= 0 && dev < 64) attr_bytes[dev] = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kcn, 1, 1);
+  cfg.blockDim = dim3(AT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kcn;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const bool ok = cudaOccupancyMaxActiveClusters(&n, append_tc_kernel, &cfg) == cudaSuccess && n >= 1;
+  cudaGetLastError();
+  return ok;
+}
+
+// Cluster size chosen by launch_append_tc for these sizes, or 0 if the path
+// does not apply (for diagnostics).
+int append_tc_cluster_size(const Shape& s, int T, int* nkb_out, size_t* smem_out) {
+  const int N = ((T + 15) / 16) * 16;
+  if (T < 1 || N > 256 || s.d_c % 2 != 0) return 0;
+  for (int kcn : {16, 8}) {
+    if (s.d_model % (kcn * 64) != 0) continue;
+    const int nkb = s.d_model / (kcn * 64);
+    const size_t smem = append_tc_smem(nkb, N);
+    if (smem > 227 * 1024 - 1024 || !append_tc_clusters_ok(kcn, smem)) continue;
+    *nkb_out = nkb;
+    *smem_out = smem;
+    return kcn;
+  }
+  return 0;
+}
+
+// Launches the split-K path if it applies; returns false (nothing launched)
+// otherwise.
+bool launch_append_tc(const Shape& s, const Weights* w, const void* x, const AppendArgs& a,
+                      void* cache, cudaStream_t st, cudaError_t* err) {
+  // (rotary pairs must sit in adjacent, even-aligned rows of a CTA's rows)
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return false;
+  int nkb = 0;
+  size_t smem = 0;
+  const int kcn = append_tc_cluster_size(s, a.T, &nkb, &smem);
+  if (kcn == 0) return false;
+  const int N = ((a.T + 15) / 16) * 16;
+  TmapSpec ws{};
+  ws.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  ws.rank = 2;
+  ws.base = w->w_dkvr;
+  ws.dims[0] = s.d_model;
+  ws.dims[1] = s.R();
+  ws.strides[0] = static_cast<uint64_t>(s.d_model) * 2;
+  ws.box[0] = 64;
+  ws.box[1] = 128;
+  ws.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  TmapSpec xs{};
+  xs.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  xs.rank = 2;
+  xs.base = x;
+  xs.dims[0] = s.d_model;
+  xs.dims[1] = a.T;
+  xs.strides[0] = static_cast<uint64_t>(s.d_model) * 2;
+  xs.box[0] = 64;
+  xs.box[1] = N;
+  xs.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap tw, tx;
+  if (!get_tmap(ws, &tw) || !get_tmap(xs, &tx)) return false;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(N)) cols *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kcn, (s.R() + 127) / 128, 1);
+  cfg.blockDim = dim3(AT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kcn;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  *err = cudaLaunchKernelEx(&cfg, append_tc_kernel, tw, tx, s, kcn, nkb, N, cols,
+                            static_cast<__nv_bfloat16*>(cache), a);
+  return true;
+}
+
 template <typename T>
 cudaError_t append_t(const Shape& s, const Weights* w, const void* x, AppendArgs a, void* cache,
                      cudaStream_t st) {
   const int R = s.R();
+  if constexpr (sizeof(T) == 2) {
+    cudaError_t e = cudaSuccess;
+    if (launch_append_tc(s, w, x, a, cache, st, &e)) return e;
+  }
   const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0;
   const size_t staged_smem = sizeof(T) * static_cast<size_t>(ST_COLS + ST_TOK) * s.d_model;
   if (a.T <= 256 && aligned && s.d_model % Vec<T>::N == 0 && staged_smem <= 200 * 1024) {

@@ -16,11 +16,12 @@
 // weight stream overlaps the combine. All threads then merge the partials of
 // their tokens into o_lat (fp32 in registers), split each value into a bf16
 // high part and a bf16 remainder, and store both as MMA operands in shared
-// memory. One thread issues the product out^T = W_uv[h] (o_hi + o_lo)^T as
-// 2 x 32 MMAs with M = 128 outputs, N = tokens, K = 512. The hi + lo split keeps
-// about 16 bits of o_lat's mantissa, so rounding o_lat for the tensor core
-// costs no measurable accuracy. Four warps read the fp32 result from TMEM,
-// one output column per lane, and store it.
+// memory. Four threads issue the product out^T = W_uv[h] (o_hi + o_lo)^T, each
+// 2 x 8 MMAs with M = 128 outputs, N = tokens over a quarter of K = 512 into
+// its own TMEM accumulator. The hi + lo split keeps about 16 bits of o_lat's
+// mantissa, so rounding o_lat for the tensor core costs no measurable
+// accuracy. Four warps read the four fp32 accumulators from TMEM, one output
+// column per lane, add them in a fixed order and store the sum.
 #include <cmath>
 
 #include "device_common.cuh"
@@ -71,11 +72,11 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.wfull, 1);
-    mbar_init(&sm.done, 1);
+    mbar_init(&sm.done, 4);  // one commit per K quarter
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, 32);
+    tmem_alloc(&sm.tmem_base, 128);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -134,55 +135,80 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   }
   __syncthreads();
 
-  // 2. o_lat = weighted sum of the partials; thread owns 8 latent dims of a
-  //    token. Loads go out four pieces at a time before they are used.
+  // 2. o_lat = weighted sum of the partials; a thread owns 8 latent dims of
+  // tokens g, g + 4, g + 8, ... (g = thread / 64) and keeps the loads of four
+  // of its tokens, four pieces each, in flight together.
   {
     const int u = threadIdx.x % 64;  // 16-byte unit: latent dims [8u, 8u + 8)
     const int kc = u / 8, uu = u % 8;
-    for (int tt = threadIdx.x / 64; tt < CT_TOK; tt += CT_THREADS / 64) {
-      float acc[8];
+    const int g = threadIdx.x / 64;
+    for (int tb = 0; tb < CT_TOK; tb += 16) {
+      float acc[4][8];
+      int lo[4], hi[4];
+      size_t off[4];
+      int nb = 0;  // batches of four pieces
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      if (tt < ntok) {
-        const int lo = sm.c_lo[tt], hi = sm.c_hi[tt];
-        const size_t off = sm.row_off[tt];
-        const float* w = wts + tt * (p.C + 1) - lo;
-        for (int c = lo; c <= hi; c += 4) {
-          float4 va[4], vb[4];
-          float wg[4];
+      for (int j = 0; j < 4; ++j) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int cj = min(c + j, hi);
-            wg[j] = (c + j <= hi) ? w[cj] : 0.f;  // empty ranges carry weight 0
-            const float4* src = reinterpret_cast<const float4*>(
-                part_o + (static_cast<size_t>(cj) * p.RG + off) * 512 + 8 * u);
-            va[j] = src[0];
-            vb[j] = src[1];
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (wg[j] == 0.f) continue;  // also skips partials no range wrote
-            acc[0] = fmaf(wg[j], va[j].x, acc[0]);
-            acc[1] = fmaf(wg[j], va[j].y, acc[1]);
-            acc[2] = fmaf(wg[j], va[j].z, acc[2]);
-            acc[3] = fmaf(wg[j], va[j].w, acc[3]);
-            acc[4] = fmaf(wg[j], vb[j].x, acc[4]);
-            acc[5] = fmaf(wg[j], vb[j].y, acc[5]);
-            acc[6] = fmaf(wg[j], vb[j].z, acc[6]);
-            acc[7] = fmaf(wg[j], vb[j].w, acc[7]);
-          }
+        for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+        const int tt = tb + g + 4 * j;
+        lo[j] = 0;
+        hi[j] = -1;
+        off[j] = 0;
+        if (tt < ntok) {
+          lo[j] = sm.c_lo[tt];
+          hi[j] = sm.c_hi[tt];
+          off[j] = sm.row_off[tt];
+          nb = max(nb, (hi[j] - lo[j] + 4) / 4);
         }
       }
-      uint32_t hw[4], lw[4];
+      for (int bb = 0; bb < nb; ++bb) {
+        float4 va[4][4], vb[4][4];
+        float wg[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 hv = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
-        lw[i] = pack_bf16x2(acc[2 * i] - __low2float(hv), acc[2 * i + 1] - __high2float(hv));
+        for (int j = 0; j < 4; ++j) {
+          const float* w = wts + (tb + g + 4 * j) * (p.C + 1) - lo[j];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = lo[j] + 4 * bb + q;
+            const bool in = c <= hi[j];
+            const int cj = in ? c : max(lo[j], 0);
+            wg[j][q] = in ? w[c] : 0.f;  // empty ranges carry weight 0
+            const float4* src = reinterpret_cast<const float4*>(
+                part_o + (static_cast<size_t>(cj) * p.RG + off[j]) * 512 + 8 * u);
+            va[j][q] = in ? src[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+            vb[j][q] = in ? src[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (wg[j][q] == 0.f) continue;  // also skips partials no range wrote
+            acc[j][0] = fmaf(wg[j][q], va[j][q].x, acc[j][0]);
+            acc[j][1] = fmaf(wg[j][q], va[j][q].y, acc[j][1]);
+            acc[j][2] = fmaf(wg[j][q], va[j][q].z, acc[j][2]);
+            acc[j][3] = fmaf(wg[j][q], va[j][q].w, acc[j][3]);
+            acc[j][4] = fmaf(wg[j][q], vb[j][q].x, acc[j][4]);
+            acc[j][5] = fmaf(wg[j][q], vb[j][q].y, acc[j][5]);
+            acc[j][6] = fmaf(wg[j][q], vb[j][q].z, acc[j][6]);
+            acc[j][7] = fmaf(wg[j][q], vb[j][q].w, acc[j][7]);
+          }
       }
-      const uint32_t off = tt * 128 + ((uu ^ (tt & 7)) * 16);
-      *reinterpret_cast<uint4*>(sm.o[0][kc] + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(sm.o[1][kc] + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tt = tb + g + 4 * j;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(acc[j][2 * i], acc[j][2 * i + 1]);
+          hw[i] = *reinterpret_cast<const uint32_t*>(&hv);
+          lw[i] = pack_bf16x2(acc[j][2 * i] - __low2float(hv), acc[j][2 * i + 1] - __high2float(hv));
+        }
+        const uint32_t o = tt * 128 + ((uu ^ (tt & 7)) * 16);
+        *reinterpret_cast<uint4*>(sm.o[0][kc] + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(sm.o[1][kc] + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
   }
   fence_proxy_async_smem();
@@ -190,21 +216,24 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   __syncthreads();
   tc_fence_after();
 
-  // 3. out^T = W_uv[h] o_lat^T on the tensor core
-  if (warp == 1 && lane == 0) {
+  // 3. out^T = W_uv[h] o_lat^T on the tensor core: K quarter i = warp i
+  // (K-steps 8i .. 8i + 7, both parts) into accumulator columns [32i, 32i + 32)
+  if (warp < 4 && lane == 0) {
     if (mbar_wait(&sm.wfull, 0, CT_WAIT)) {
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, n_box, false, false);
       for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          mma_bf16_ss(tmem, kdesc(sm.w[k >> 2], (k & 3) * 32),
+        for (int kk = 0; kk < 8; ++kk) {
+          const int k = 8 * warp + kk;
+          mma_bf16_ss(tmem + 32 * warp, kdesc(sm.w[k >> 2], (k & 3) * 32),
                       kdesc(sm.o[part][k >> 2], (k & 3) * 32), idesc,
-                      (part == 0 && k == 0) ? 0u : 1u);
-      mma_commit(&sm.done);
+                      (part == 0 && kk == 0) ? 0u : 1u);
+        }
     } else {
       set_error(err, MLA_DEVERR_TIMEOUT);
     }
+    mma_commit(&sm.done);
   }
   if (warp < 4) {
     const bool done = mbar_wait(&sm.done, 0, 2 * CT_WAIT);
@@ -213,9 +242,14 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
       const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
       const int dv = 32 * warp + lane;
       for (int c0 = 0; c0 < n_box; c0 += 16) {
-        float v[16];
+        float v[16], v1[16], v2[16], v3[16];
         tmem_ld16(tmem + lane_base + c0, v);
+        tmem_ld16(tmem + lane_base + 32 + c0, v1);
+        tmem_ld16(tmem + lane_base + 64 + c0, v2);
+        tmem_ld16(tmem + lane_base + 96 + c0, v3);
         tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = (v[i] + v1[i]) + (v2[i] + v3[i]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int tt = c0 + i;
@@ -230,7 +264,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 32);
+    tmem_dealloc(tmem, 128);
   }
 }
 

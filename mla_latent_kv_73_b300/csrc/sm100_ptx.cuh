@@ -336,6 +336,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
                "r"(d)
                : "memory");
 }
+// Generic address of the same shared-memory object in cluster CTA `rank`.
+// Ordinary loads through it read that CTA's shared memory, and the compiler
+// may keep many of them in flight (ordering against other CTAs' writes comes
+// from the cluster barrier, which clobbers memory).
+template <typename T>
+__device__ __forceinline__ const T* map_to_rank(const T* p, uint32_t rank) {
+  uint64_t out;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<const T*>(out);
+}
 // Whole-cluster barrier; every thread of every CTA in the cluster executes it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
