@@ -14,8 +14,9 @@
 // [d_c x d_nope] slice of W_uk once with 16-byte loads. Each thread owns two
 // latent rows and all 16 tokens, so every weight element is read once.
 //
-// Block (0, 0) also writes the split-KV plan: the tiles of each sequence and
-// their prefix sum. The attention and combine kernels both read it.
+// Block (0, 0) also writes the split-KV plan: the tiles of each sequence,
+// their prefix sum and the range boundaries. The attention and combine
+// kernels both read it.
 #include "device_common.cuh"
 #include "plan.cuh"
 
@@ -28,15 +29,17 @@ template <typename T>
 __global__ void __launch_bounds__(AQ_THREADS)
 absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
                 const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
-                int n_q, int max_blocks, int TS, float out_scale, T* __restrict__ qabs,
-                int32_t* tiles, int32_t* prefix, uint32_t* err) {
+                int n_q, int max_blocks, int TS, int G, int C, int K, float out_scale,
+                T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
+                uint32_t* err) {
   extern __shared__ __align__(16) float qn[];  // [d_nope][AQ_TOK], token fastest
   const int h = blockIdx.x;
   const int tok0 = blockIdx.y * AQ_TOK;
   const int Tq = B * n_q;
   const int dq = s.d_nope + s.d_r, R = s.R();
   if (blockIdx.x == 0 && blockIdx.y == 0)
-    write_plan<AQ_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
+    write_plan<AQ_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
+                           err);
 
   const int ntok = min(AQ_TOK, Tq - tok0);
   for (int i = threadIdx.x; i < AQ_TOK * s.d_nope; i += AQ_THREADS) {
@@ -123,7 +126,8 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
   const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;
   absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
       s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
-      max_blocks, p.TS, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, err);
+      max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix,
+      ws.bounds, err);
   return cudaGetLastError();
 }
 

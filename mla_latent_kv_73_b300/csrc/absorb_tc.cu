@@ -21,8 +21,9 @@
 // one latent row per lane, and store bf16. The other four warps rotate
 // q_rope meanwhile.
 //
-// Block (0, 0) also writes the split-KV plan (tiles per sequence and their
-// prefix sum), which the attention and combine kernels read.
+// Block (0, 0) also writes the split-KV plan (tiles per sequence, their
+// prefix sum and the range boundaries), which the attention and combine
+// kernels read.
 #include "device_common.cuh"
 #include "plan.cuh"
 #include "sm100_ptx.cuh"
@@ -54,14 +55,12 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_q, Shape s,
                    const __nv_bfloat16* __restrict__ q, const double* __restrict__ inv_freq,
                    const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
-                   int n_tok_box, float out_scale, __nv_bfloat16* __restrict__ qabs, int32_t* tiles,
-                   int32_t* prefix, uint32_t* err) {
+                   int G, int C, int K, int n_tok_box, float out_scale,
+                   __nv_bfloat16* __restrict__ qabs, int32_t* tiles, int32_t* prefix,
+                   long long* bounds, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   AbsSmem& sm = *reinterpret_cast<AbsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
-  if (blockIdx.x == 0 && blockIdx.y == 0)
-    write_plan<AT_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, tiles, prefix, err);
-
   const int h = blockIdx.x;
   const int t0 = blockIdx.y * AT_TOK;
   const int Tq = B * n_q;
@@ -96,6 +95,10 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full_w[j]);
     }
   }
+  // (after the loads are on their way, so the plan costs this block no time)
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    write_plan<AT_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
+                           err);
   if (warp < 4 && lane == 0) {
     // block j = warp of q_lat^T, as soon as its rows of W_uk[h] are in
     const int j = warp;
@@ -211,7 +214,8 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
   dim3 grid(s.n_h, (Tq + AT_TOK - 1) / AT_TOK);
   absorb_q_tc_kernel<<<grid, AT_THREADS, smem, st>>>(
       tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
-      p.TS, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles, ws.prefix, err);
+      p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles,
+      ws.prefix, ws.bounds, err);
   return cudaGetLastError();
 }
 

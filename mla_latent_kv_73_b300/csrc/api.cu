@@ -145,10 +145,12 @@ Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms, i
     p.RG = 128;
     p.TS = 64;
     p.C = tc_pairs;
+    p.K = 4;  // a piece change stalls the pair's pipeline for about 4 tiles
   } else {
     p.RG = 16;
     p.TS = 64;
     p.C = num_sms * 3;
+    p.K = 0;
   }
   p.G = (rows + p.RG - 1) / p.RG;
   p.slots = p.C + p.G * B;
@@ -164,6 +166,8 @@ WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partit
   off = align256(off + sizeof(int32_t) * B);
   l.prefix = off;
   off = align256(off + sizeof(int32_t) * (B + 1));
+  l.bounds = off;
+  off = align256(off + sizeof(long long) * (p.C + 1));
   l.part_o = off;
   off = align256(off + sizeof(float) * static_cast<size_t>(p.slots) * p.RG * s.d_c);
   l.part_lse = off;
@@ -178,6 +182,7 @@ WsView ws_view(void* base, const WsLayout& l) {
   v.qabs = b + l.qabs;
   v.tiles = reinterpret_cast<int32_t*>(b + l.tiles);
   v.prefix = reinterpret_cast<int32_t*>(b + l.prefix);
+  v.bounds = reinterpret_cast<long long*>(b + l.bounds);
   v.part_o = reinterpret_cast<float*>(b + l.part_o);
   v.part_lse = reinterpret_cast<float*>(b + l.part_lse);
   return v;

@@ -30,8 +30,9 @@ __global__ void __launch_bounds__(SG_THREADS)
 attend_simt_kernel(Shape s, const T* __restrict__ cache, int num_blocks,
                    const int32_t* __restrict__ page_table, int max_blocks, int B, int n_q,
                    Partition p, const T* __restrict__ qabs, const int32_t* __restrict__ tiles,
-                   const int32_t* __restrict__ prefix, const int32_t* __restrict__ seq_lens,
-                   float* __restrict__ part_o, float* __restrict__ part_lse, uint32_t* err) {
+                   const int32_t* __restrict__ prefix, const long long* __restrict__ bounds,
+                   const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
+                   float* __restrict__ part_lse, uint32_t* err) {
   extern __shared__ float sm[];
   const int R = s.R(), RP = R + 1;
   float* qs = sm;                      // [16][RP]
@@ -45,8 +46,8 @@ attend_simt_kernel(Shape s, const T* __restrict__ cache, int num_blocks,
   const long long T_all = prefix[B];
   const long long N = T_all * p.G;
   if (N == 0) return;
-  long long it = range_begin(blockIdx.x, N, p.C);
-  const long long end = range_begin(blockIdx.x + 1, N, p.C);
+  long long it = bounds[blockIdx.x];
+  const long long end = bounds[blockIdx.x + 1];
   const float scale_log2 = s.scale * 1.4426950408889634f;
 
   while (it < end) {
@@ -164,7 +165,7 @@ cudaError_t attend_simt_t(const Shape& s, const void* cache, int num_blocks,
   }
   kern<<<p.C, SG_THREADS, smem, st>>>(s, static_cast<const T*>(cache), num_blocks, page_table,
                                       max_blocks, B, n_q, p, static_cast<const T*>(ws.qabs),
-                                      ws.tiles, ws.prefix, seq_lens, ws.part_o, ws.part_lse, err);
+                                      ws.tiles, ws.prefix, ws.bounds, seq_lens, ws.part_o, ws.part_lse, err);
   return cudaGetLastError();
 }
 

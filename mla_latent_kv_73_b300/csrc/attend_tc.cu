@@ -142,6 +142,7 @@ struct PairArgs {
   const int32_t* seq_lens;
   const int32_t* tiles;
   const int32_t* prefix;
+  const long long* bounds;  // [P + 1] first work item of each pair's range
   float* part_o;
   float* part_lse;
   const __nv_bfloat16* qabs;  // [q_rows][576] absorbed queries (for the TMEM part of Q)
@@ -373,8 +374,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   const long long N = T_all * a.G;
   // Both CTAs of a pair see the same range, so they leave here together.
   if (N == 0) return;
-  const long long it_begin = range_begin(pair, N, a.P);
-  const long long it_end = range_begin(pair + 1, N, a.P);
+  const long long it_begin = a.bounds[pair];
+  const long long it_end = a.bounds[pair + 1];
   if (it_begin == it_end) return;
   const int rows_total = a.n_q * a.n_h;
 
@@ -919,6 +920,7 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   a.seq_lens = seq_lens;
   a.tiles = ws.tiles;
   a.prefix = ws.prefix;
+  a.bounds = ws.bounds;
   a.part_o = ws.part_o;
   a.part_lse = ws.part_lse;
   a.qabs = static_cast<const __nv_bfloat16*>(ws.qabs);

@@ -17,6 +17,7 @@
 #include <cmath>
 
 #include "device_common.cuh"
+#include "plan.cuh"
 
 namespace mla {
 namespace {
@@ -29,7 +30,8 @@ constexpr int CB_TOK = 16, CB_THREADS = 256;
 template <typename T>
 __global__ void __launch_bounds__(CB_THREADS)
 combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ tiles,
-               const int32_t* __restrict__ prefix, int B, int n_q, Partition p,
+               const int32_t* __restrict__ prefix, const long long* __restrict__ bounds, int B,
+               int n_q, Partition p,
                const float* __restrict__ part_o, const float* __restrict__ part_lse,
                float* __restrict__ out) {
   extern __shared__ __align__(16) float sm[];
@@ -43,7 +45,7 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
   const long long T_all = prefix[B];
   const long long N = T_all * p.G;
 
-  for (int c = threadIdx.x; c <= p.C; c += CB_THREADS) rb[c] = N > 0 ? range_begin(c, N, p.C) : 0;
+  for (int c = threadIdx.x; c <= p.C; c += CB_THREADS) rb[c] = N > 0 ? bounds[c] : 0;
   __syncthreads();
 
   // 1. per token: the CTAs holding its pieces, the max lse and the normaliser
@@ -57,8 +59,8 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
       off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
       if (tiles[b] > 0) {
         const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
-        c0 = cta_of_item(first, N, p.C);
-        c1 = cta_of_item(last, N, p.C);
+        c0 = range_of_item(rb, p.C, first);
+        c1 = range_of_item(rb, p.C, last);
         for (int c = c0; c <= c1; ++c)
           if (rb[c] != rb[c + 1]) M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
         if (M != -INFINITY)
@@ -150,8 +152,8 @@ cudaError_t combine_t(const Shape& s, const Weights* w, int B, int n_q, const Pa
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, CB_THREADS, smem, st>>>(s, static_cast<const T*>(w->w_uv), ws.tiles, ws.prefix, B,
-                                       n_q, p, ws.part_o, ws.part_lse, out);
+  kern<<<grid, CB_THREADS, smem, st>>>(s, static_cast<const T*>(w->w_uv), ws.tiles, ws.prefix,
+                                       ws.bounds, B, n_q, p, ws.part_o, ws.part_lse, out);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@
 #include <cmath>
 
 #include "device_common.cuh"
+#include "plan.cuh"
 #include "sm100_ptx.cuh"
 #include "tmap.h"
 
@@ -58,8 +59,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 __global__ void __launch_bounds__(CT_THREADS, 1)
 combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
-                  const int32_t* __restrict__ tiles, const int32_t* __restrict__ prefix, int B,
-                  int n_q, Partition p, const float* __restrict__ part_o,
+                  const int32_t* __restrict__ tiles, const int32_t* __restrict__ prefix,
+                  const long long* __restrict__ bounds, int B, int n_q, Partition p,
+                  const float* __restrict__ part_o,
                   const float* __restrict__ part_lse, float* __restrict__ out, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   CombSmem& sm = *reinterpret_cast<CombSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -94,7 +96,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   //    lse loads of a token are one round trip.
   const long long T_all = prefix[B];
   const long long N = T_all * p.G;
-  for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = N > 0 ? range_begin(c, N, p.C) : 0;
+  for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = N > 0 ? bounds[c] : 0;
   __syncthreads();
   float* wts = reinterpret_cast<float*>(rb + p.C + 1);  // [CT_TOK][C + 1] merge weights
   for (int t = warp; t < CT_TOK; t += CT_THREADS / 32) {
@@ -105,8 +107,8 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
       off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
       if (tiles[b] > 0) {
         const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
-        c0 = cta_of_item(first, N, p.C);
-        c1 = cta_of_item(last, N, p.C);
+        c0 = range_of_item(rb, p.C, first);
+        c1 = range_of_item(rb, p.C, last);
       }
     }
     float M = -INFINITY;
@@ -304,7 +306,8 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
     if (dev >= 0 && dev < 64) attr_bytes[dev] = static_cast<int>(smem);
   }
   dim3 grid(s.n_h, (Tq + CT_TOK - 1) / CT_TOK);
-  combine_tc_kernel<<<grid, CT_THREADS, smem, st>>>(tw, s.n_h, ws.tiles, ws.prefix, B, n_q, p,
+  combine_tc_kernel<<<grid, CT_THREADS, smem, st>>>(tw, s.n_h, ws.tiles, ws.prefix, ws.bounds, B,
+                                                     n_q, p,
                                                      ws.part_o, ws.part_lse, out, err);
   return cudaGetLastError();
 }

@@ -75,13 +75,4 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
-// The CTA that owns flat work item x when N items are split over C CTAs
-// as [c*N/C, (c+1)*N/C).
-__device__ __forceinline__ int cta_of_item(long long x, long long N, int C) {
-  return static_cast<int>(((x + 1) * C - 1) / N);
-}
-__device__ __forceinline__ long long range_begin(int c, long long N, int C) {
-  return (static_cast<long long>(c) * N) / C;
-}
-
 }  // namespace mla

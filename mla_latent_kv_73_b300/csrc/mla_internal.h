@@ -23,14 +23,17 @@ struct Shape {
 // The query rows of a sequence, r = i*n_h + h for query token i and head h,
 // are cut into G groups of RG rows. The cached tokens of sequence b form
 // tiles_b = ceil(L_b / TS) tiles. The attention grid splits the flat list of
-// work items (g, b, tile), ordered group-major, into C contiguous ranges of
-// near-equal length: one per CTA (CUDA-core kernel) or per 2-CTA cluster
-// (tensor-core kernel). One range therefore covers pieces of several (g, b)
-// pairs. The piece of range c on pair (g, b) writes its partial result to
-// slot c + g*B + b. The slots are unique, and slots = C + G*B bound their
+// work items (g, b, tile), ordered group-major, into C contiguous ranges:
+// one per CTA (CUDA-core kernel) or per 2-CTA cluster (tensor-core kernel).
+// A range costs its tiles plus K tiles for every (g, b) piece it starts
+// (the partial's epilogue and the next piece's query load), and the plan
+// writer cuts the item list so that these costs come out near-equal (K = 0
+// gives ranges of equal length). One range therefore covers pieces of several
+// (g, b) pairs. The piece of range c on pair (g, b) writes its partial result
+// to slot c + g*B + b. The slots are unique, and slots = C + G*B bound their
 // number.
 struct Partition {
-  int RG, G, TS, C, slots;
+  int RG, G, TS, C, K, slots;
 };
 
 // Pointers into the decode workspace.
@@ -38,12 +41,13 @@ struct WsView {
   void* qabs;         // [B*n_q*n_h, R] in the cache dtype: [q_lat | RoPE(q_rope)]
   int32_t* tiles;     // [B]    tiles per sequence (0 for an invalid length)
   int32_t* prefix;    // [B+1]  exclusive prefix sum of tiles
+  long long* bounds;  // [C+1]  first work item of each range (bounds[C] = all items)
   float* part_o;      // [slots, RG, d_c] normalised partial latent outputs
   float* part_lse;    // [slots, RG]      natural-log sum-exp of each partial
 };
 
 struct WsLayout {
-  size_t qabs, tiles, prefix, part_o, part_lse, total;
+  size_t qabs, tiles, prefix, bounds, part_o, part_lse, total;
 };
 
 WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p);

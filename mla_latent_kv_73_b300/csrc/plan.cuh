@@ -1,7 +1,17 @@
 // Split-KV plan, written by one CTA of the query-absorption kernel: the
-// number of 64-token tiles of each sequence and their exclusive prefix sum.
-// The attention and combine kernels read both. A sequence whose length is
-// below n_q or beyond its page table gets 0 tiles and sets MLA_DEVERR_SEQ_LEN.
+// number of 64-token tiles of each sequence, their exclusive prefix sum, and
+// the first work item of each of the C ranges. The attention and combine
+// kernels read all three. A sequence whose length is below n_q or beyond its
+// page table gets 0 tiles and sets MLA_DEVERR_SEQ_LEN.
+//
+// Range boundaries. Work items are (g, b, tile) in group-major order. Each
+// range is charged its tiles plus K for every (g, b) piece it contains; the
+// cumulative cost up to item (g, b, j) is taken as
+//   F(g, b, j) = g T + prefix[b] + j + K (g B + b)
+// (T tiles in all, one K per sequence start) and range c begins at the first
+// item whose F reaches c F_total / C. F is monotone in the item, so each
+// boundary is an independent binary search; with K = 0 the ranges have equal
+// length.
 #pragma once
 #include "device_common.cuh"
 
@@ -10,7 +20,8 @@ namespace mla {
 // Every thread of the block (NT threads) must call this.
 template <int NT>
 __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks,
-                           int bs, int TS, int32_t* tiles, int32_t* prefix, uint32_t* err) {
+                           int bs, int TS, int G, int C, int K, int32_t* tiles, int32_t* prefix,
+                           long long* bounds, uint32_t* err) {
   __shared__ int32_t warp_sums[NT / 32];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -45,6 +56,41 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
     __syncthreads();
   }
   if (threadIdx.x == 0) prefix[B] = carry;
+  __syncthreads();  // tiles and prefix are visible to the whole block
+  const long long T = carry;
+  const long long per_g = T + static_cast<long long>(K) * B;  // F of one whole group
+  const long long F_total = per_g * G;
+  for (int c = threadIdx.x; c <= C; c += NT) {
+    long long v = 0;
+    if (c == C) {
+      v = T * G;
+    } else if (c > 0 && F_total > 0) {
+      const long long Fc = (static_cast<long long>(c) * F_total) / C;
+      const int g = static_cast<int>(min(static_cast<long long>(G - 1), Fc / per_g));
+      const long long r = Fc - g * per_g;
+      int lo = 0, hi = B;  // largest b with prefix[b] + K b <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] + static_cast<long long>(K) * mid <= r) lo = mid; else hi = mid;
+      }
+      // past the end of sequence lo: cut at its end (the next sequence's start)
+      const long long j = min(r - prefix[lo] - static_cast<long long>(K) * lo,
+                              static_cast<long long>(tiles[lo]));
+      v = g * T + prefix[lo] + j;
+    }
+    bounds[c] = v;
+  }
+}
+
+// The range holding work item x: the largest c < C with rb[c] <= x, for
+// boundaries rb[0..C] and 0 <= x < rb[C]. Empty ranges are never returned.
+__device__ __forceinline__ int range_of_item(const long long* rb, int C, long long x) {
+  int lo = 0, hi = C;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (rb[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
 }
 
 
