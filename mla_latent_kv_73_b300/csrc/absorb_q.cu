@@ -31,7 +31,7 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
                 const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
                 int n_q, int max_blocks, int TS, int G, int C, int K, float out_scale,
                 T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
-                uint32_t* err) {
+                int32_t* first_b, uint32_t* err) {
   extern __shared__ __align__(16) float qn[];  // [d_nope][AQ_TOK], token fastest
   const int h = blockIdx.x;
   const int tok0 = blockIdx.y * AQ_TOK;
@@ -39,7 +39,7 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
   const int dq = s.d_nope + s.d_r, R = s.R();
   if (blockIdx.x == 0 && blockIdx.y == 0)
     write_plan<AQ_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
-                           err);
+                           first_b, err);
 
   const int ntok = min(AQ_TOK, Tq - tok0);
   for (int i = threadIdx.x; i < AQ_TOK * s.d_nope; i += AQ_THREADS) {
@@ -127,7 +127,7 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
   absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
       s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
       max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix,
-      ws.bounds, err);
+      ws.bounds, ws.first_b, err);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,7 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
                    int G, int C, int K, int n_tok_box, float out_scale,
                    __nv_bfloat16* __restrict__ qabs, int32_t* tiles, int32_t* prefix,
-                   long long* bounds, uint32_t* err) {
+                   long long* bounds, int32_t* first_b, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   AbsSmem& sm = *reinterpret_cast<AbsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -95,10 +95,13 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full_w[j]);
     }
   }
+  // The attention kernel may be scheduled now; it waits for this grid to
+  // complete before it reads the queries or the plan.
+  griddep_launch_dependents();
   // (after the loads are on their way, so the plan costs this block no time)
   if (blockIdx.x == 0 && blockIdx.y == 0)
     write_plan<AT_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
-                           err);
+                           first_b, err);
   if (warp < 4 && lane == 0) {
     // block j = warp of q_lat^T, as soon as its rows of W_uk[h] are in
     const int j = warp;
@@ -215,7 +218,7 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
   absorb_q_tc_kernel<<<grid, AT_THREADS, smem, st>>>(
       tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
       p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles,
-      ws.prefix, ws.bounds, err);
+      ws.prefix, ws.bounds, ws.first_b, err);
   return cudaGetLastError();
 }
 

@@ -168,6 +168,8 @@ WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partit
   off = align256(off + sizeof(int32_t) * (B + 1));
   l.bounds = off;
   off = align256(off + sizeof(long long) * (p.C + 1));
+  l.first_b = off;
+  off = align256(off + sizeof(int32_t) * p.C);
   l.part_o = off;
   off = align256(off + sizeof(float) * static_cast<size_t>(p.slots) * p.RG * s.d_c);
   l.part_lse = off;
@@ -183,6 +185,7 @@ WsView ws_view(void* base, const WsLayout& l) {
   v.tiles = reinterpret_cast<int32_t*>(b + l.tiles);
   v.prefix = reinterpret_cast<int32_t*>(b + l.prefix);
   v.bounds = reinterpret_cast<long long*>(b + l.bounds);
+  v.first_b = reinterpret_cast<int32_t*>(b + l.first_b);
   v.part_o = reinterpret_cast<float*>(b + l.part_o);
   v.part_lse = reinterpret_cast<float*>(b + l.part_lse);
   return v;

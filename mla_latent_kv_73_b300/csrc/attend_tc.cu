@@ -143,6 +143,7 @@ struct PairArgs {
   const int32_t* tiles;
   const int32_t* prefix;
   const long long* bounds;  // [P + 1] first work item of each pair's range
+  const int32_t* first_b;   // [P] sequence of each range's first work item
   float* part_o;
   float* part_lse;
   const __nv_bfloat16* qabs;  // [q_rows][576] absorbed queries (for the TMEM part of Q)
@@ -157,20 +158,22 @@ struct Piece {
   int g, b, t_first, n_tiles;
 };
 
-__device__ __forceinline__ Piece locate_piece(long long it, long long end, long long T_all,
-                                              const int32_t* prefix, const int32_t* tiles,
-                                              int B) {
+// The piece that starts at work item `it` of a range ending at `end`, found
+// by stepping forward from sequence b0 of group g0, which lies at or before
+// it (the plan's first sequence of the range, or the sequence after the
+// previous piece). Without empty sequences in between that is one round of
+// independent loads, not a search.
+__device__ __noinline__ Piece piece_at(long long it, long long end, long long T_all,
+                                      const PairArgs& a, int g0, int b0) {
   Piece pc;
   pc.g = static_cast<int>(it / T_all);
   const long long rem = it % T_all;
-  int lo = 0, hi = B;  // largest b with prefix[b] <= rem
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= rem) lo = mid; else hi = mid;
-  }
-  pc.b = lo;
-  pc.t_first = static_cast<int>(rem - prefix[lo]);
-  const long long stop = min(end, static_cast<long long>(pc.g) * T_all + prefix[lo] + tiles[lo]);
+  int b = pc.g == g0 ? min(b0, a.B - 1) : 0;
+  while (b + 1 < a.B && a.prefix[b + 1] <= rem) ++b;
+  pc.b = b;
+  pc.t_first = static_cast<int>(rem - a.prefix[b]);
+  const long long stop =
+      min(end, static_cast<long long>(pc.g) * T_all + a.prefix[b] + a.tiles[b]);
   pc.n_tiles = static_cast<int>(stop - it);
   return pc;
 }
@@ -184,13 +187,16 @@ struct TileCursor {
   Piece pc;
   int i, piece;
   uint32_t kv;
-  __device__ void init(long long b, long long e, const PairArgs& a) {
+  __device__ void init(long long b, long long e, const PairArgs& a, int pair) {
     it = b;
     left = static_cast<int>(e - b);
     i = 0;
     piece = 0;
     kv = 0;
-    if (left > 0) pc = locate_piece(it, e, a.prefix[a.B], a.prefix, a.tiles, a.B);
+    if (left > 0) {
+      const long long T_all = a.prefix[a.B];
+      pc = piece_at(it, e, T_all, a, static_cast<int>(it / T_all), a.first_b[pair]);
+    }
   }
   __device__ bool valid() const { return left > 0; }
   __device__ bool first() const { return i == 0; }
@@ -204,7 +210,7 @@ struct TileCursor {
     if (i == pc.n_tiles) {
       i = 0;
       ++piece;
-      if (left > 0) pc = locate_piece(it, it + left, a.prefix[a.B], a.prefix, a.tiles, a.B);
+      if (left > 0) pc = piece_at(it, it + left, a.prefix[a.B], a, pc.g, pc.b + 1);
     }
   }
 };
@@ -370,15 +376,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = static_cast<int>(cluster_id_x());
-  const long long T_all = a.prefix[a.B];
-  const long long N = T_all * a.G;
-  // Both CTAs of a pair see the same range, so they leave here together.
-  if (N == 0) return;
-  const long long it_begin = a.bounds[pair];
-  const long long it_end = a.bounds[pair + 1];
-  if (it_begin == it_end) return;
-  const int rows_total = a.n_q * a.n_h;
 
+  // Setup first: with programmatic dependent launch it overlaps the end of
+  // the query-absorption kernel, whose outputs are read only after the wait.
   if (threadIdx.x == 0) {
     for (int s = 0; s < TP_STAGES; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -410,8 +410,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   cluster_sync();  // both CTAs' barriers exist before either arrives remotely
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  griddep_wait();
+  griddep_launch_dependents();
+  const long long T_all = a.prefix[a.B];
+  const long long N = T_all * a.G;
+  // Both CTAs of a pair see the same range, so they skip the work together.
+  const long long it_begin = N > 0 ? a.bounds[pair] : 0;
+  const long long it_end = N > 0 ? a.bounds[pair + 1] : 0;
+  const int rows_total = a.n_q * a.n_h;
 
-  if (warp == 0) {
+  if (it_begin >= it_end) {
+    // empty range: straight to the final cluster barrier
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tmap_qc);
@@ -424,8 +434,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       int piece_idx = 0;
       uint32_t issued[TP_STAGES] = {};
       bool stop = false;
+      int prev_g = static_cast<int>(it_begin / T_all), next_b = a.first_b[pair];
       for (long long it = it_begin; it < it_end && !stop && !aborted(sm);) {
-        const Piece pc = locate_piece(it, it_end, T_all, a.prefix, a.tiles, a.B);
+        const Piece pc = piece_at(it, it_end, T_all, a, prev_g, next_b);
+        prev_g = pc.g;
+        next_b = pc.b + 1;
         if (piece_idx > 0 && !mbar_wait(&sm.q_empty, (piece_idx - 1) & 1, WAIT_LIMIT)) {
           note_timeout(sm, a.err);
           break;
@@ -484,7 +497,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       constexpr uint32_t kStageDesc = sizeof(PairSmem::Stage) >> 4;  // stage stride, 16-B units
       bool ok = true;
       TileCursor cur;
-      cur.init(it_begin, it_end, a);
+      cur.init(it_begin, it_end, a, pair);
       for (; cur.valid() && ok; cur.next(a)) {
         const uint32_t t = cur.kv;
         if (!mbar_wait(&sm.p_full[t & 1], (t >> 1) & 1, WAIT_LIMIT)) { ok = false; break; }
@@ -526,7 +539,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       const uint32_t dS = tmem + TM_S + 64 * half;
       bool ok = true;
       TileCursor cur;
-      cur.init(it_begin, it_end, a);
+      cur.init(it_begin, it_end, a, pair);
       while (cur.valid() && ok) {
         // one piece: wait for its Q, issue this parity's tiles, release Q
         if (!mbar_wait(&sm.q_full, cur.piece & 1, WAIT_LIMIT)) { ok = false; break; }
@@ -572,7 +585,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     const bool leader = warp == TP_SEND_WARP0 && lane == 0;
     bool bad = false;
     TileCursor cur;
-    cur.init(it_begin, it_end, a);
+    cur.init(it_begin, it_end, a, pair);
     // The four warps meet at named barriers inside send_tile, which merge
     // their timeout flags, so they leave the loop together.
     for (; cur.valid(); cur.next(a)) {
@@ -600,7 +613,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     const int row = 32 * qd + lane;
     const int gtid = sw * 32 + lane;            // 0..255
     TileCursor cur;
-    cur.init(it_begin, it_end, a);
+    cur.init(it_begin, it_end, a, pair);
     float l = 0.f, m = -INFINITY;
     int L = 0, rows_valid = 0, pos_q = 0;
     bool row_ok = false, bad = false;
@@ -921,6 +934,7 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   a.tiles = ws.tiles;
   a.prefix = ws.prefix;
   a.bounds = ws.bounds;
+  a.first_b = ws.first_b;
   a.part_o = ws.part_o;
   a.part_lse = ws.part_lse;
   a.qabs = static_cast<const __nv_bfloat16*>(ws.qabs);
@@ -939,13 +953,17 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   cfg.blockDim = dim3(TP_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes();
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel finishes (the kernel waits for it
+  // before reading anything)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tqc, tqr, tkc, tkr, a);
 }
 

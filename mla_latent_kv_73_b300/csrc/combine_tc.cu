@@ -85,8 +85,15 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // With programmatic dependent launch this CTA may start while the attention
+  // kernel still runs: pull W_uv[h] into L2 (coherent, so safe at any time),
+  // then wait for the attention kernel before loading anything into the SM.
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
+    for (int kc = 0; kc < 8; ++kc) tma_prefetch_2d(&tmap_w, 64 * kc, h * 128);
+  }
+  griddep_wait();
+  if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
     for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
   }
@@ -305,11 +312,23 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_bytes[dev] = static_cast<int>(smem);
   }
-  dim3 grid(s.n_h, (Tq + CT_TOK - 1) / CT_TOK);
-  combine_tc_kernel<<<grid, CT_THREADS, smem, st>>>(tw, s.n_h, ws.tiles, ws.prefix, ws.bounds, B,
-                                                     n_q, p,
-                                                     ws.part_o, ws.part_lse, out, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.n_h, (Tq + CT_TOK - 1) / CT_TOK, 1);
+  cfg.blockDim = dim3(CT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  // may start while the attention kernel finishes (see the kernel's wait)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_tc_kernel, tw, s.n_h,
+                            static_cast<const int32_t*>(ws.tiles),
+                            static_cast<const int32_t*>(ws.prefix),
+                            static_cast<const long long*>(ws.bounds), B, n_q, p,
+                            static_cast<const float*>(ws.part_o),
+                            static_cast<const float*>(ws.part_lse), out, err);
 }
 
 }  // namespace mla

@@ -42,12 +42,13 @@ struct WsView {
   int32_t* tiles;     // [B]    tiles per sequence (0 for an invalid length)
   int32_t* prefix;    // [B+1]  exclusive prefix sum of tiles
   long long* bounds;  // [C+1]  first work item of each range (bounds[C] = all items)
+  int32_t* first_b;   // [C]    sequence of each range's first work item
   float* part_o;      // [slots, RG, d_c] normalised partial latent outputs
   float* part_lse;    // [slots, RG]      natural-log sum-exp of each partial
 };
 
 struct WsLayout {
-  size_t qabs, tiles, prefix, bounds, part_o, part_lse, total;
+  size_t qabs, tiles, prefix, bounds, first_b, part_o, part_lse, total;
 };
 
 WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p);

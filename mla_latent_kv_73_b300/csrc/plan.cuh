@@ -11,7 +11,8 @@
 // (T tiles in all, one K per sequence start) and range c begins at the first
 // item whose F reaches c F_total / C. F is monotone in the item, so each
 // boundary is an independent binary search; with K = 0 the ranges have equal
-// length.
+// length. first_b[c] is the sequence of range c's first item (0 for an empty
+// range), so the attention kernel finds its first piece without a search.
 #pragma once
 #include "device_common.cuh"
 
@@ -21,7 +22,7 @@ namespace mla {
 template <int NT>
 __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks,
                            int bs, int TS, int G, int C, int K, int32_t* tiles, int32_t* prefix,
-                           long long* bounds, uint32_t* err) {
+                           long long* bounds, int32_t* first_b, uint32_t* err) {
   __shared__ int32_t warp_sums[NT / 32];
   __shared__ int32_t carry;
   if (threadIdx.x == 0) carry = 0;
@@ -79,6 +80,19 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
       v = g * T + prefix[lo] + j;
     }
     bounds[c] = v;
+    if (c < C) {
+      int b = 0;
+      if (T > 0 && v < T * G) {
+        const long long rem = v % T;
+        int lo = 0, hi = B;  // largest b with prefix[b] <= rem: the sequence holding item v
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (prefix[mid] <= rem) lo = mid; else hi = mid;
+        }
+        b = lo;
+      }
+      first_b[c] = b;
+    }
   }
 }
 

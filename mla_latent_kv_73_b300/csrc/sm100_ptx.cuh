@@ -88,6 +88,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Pulls a tile of a tensor into L2 (no shared-memory destination, no
+// completion signal). L2 is coherent, so this is safe before the data's
+// producer has finished; only the later load must wait.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m, int32_t x,
                                             int32_t y, int32_t z, uint64_t* bar) {
   asm volatile(
@@ -345,6 +355,16 @@ __device__ __forceinline__ const T* map_to_rank(const T* p, uint32_t rank) {
   uint64_t out;
   asm("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
   return reinterpret_cast<const T*>(out);
+}
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream still
+// runs; griddep_wait() returns once that kernel has completed and its memory
+// is visible. griddep_launch_dependents() lets the next such kernel start.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 // Whole-cluster barrier; every thread of every CTA in the cluster executes it.
 __device__ __forceinline__ void cluster_sync() {
