@@ -18,6 +18,11 @@
 
 namespace mla {
 
+// Sequences whose tiles and prefix sums the plan writer also keeps in shared
+// memory, so that its boundary searches are shared-memory reads rather than
+// dependent round trips to L2.
+constexpr int PLAN_SMEM_B = 1024;
+
 // Every thread of the block (NT threads) must call this.
 template <int NT>
 __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks,
@@ -25,6 +30,7 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
                            long long* bounds, int32_t* first_b, uint32_t* err) {
   __shared__ int32_t warp_sums[NT / 32];
   __shared__ int32_t carry;
+  __shared__ int32_t s_tiles[PLAN_SMEM_B], s_prefix[PLAN_SMEM_B + 1];
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
@@ -39,6 +45,7 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
         t = static_cast<int>((L + TS - 1) / TS);
       }
       tiles[b] = t;
+      if (b < PLAN_SMEM_B) s_tiles[b] = t;
     }
     // inclusive warp scan
     int v = t;
@@ -51,13 +58,22 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
     __syncthreads();
     int before = carry;
     for (int w = 0; w < warp; ++w) before += warp_sums[w];
-    if (b < B) prefix[b] = before + v - t;
+    if (b < B) {
+      prefix[b] = before + v - t;
+      if (b < PLAN_SMEM_B) s_prefix[b] = before + v - t;
+    }
     __syncthreads();
     if (threadIdx.x == NT - 1) carry = before + v;
     __syncthreads();
   }
-  if (threadIdx.x == 0) prefix[B] = carry;
+  if (threadIdx.x == 0) {
+    prefix[B] = carry;
+    if (B <= PLAN_SMEM_B) s_prefix[B] = carry;
+  }
   __syncthreads();  // tiles and prefix are visible to the whole block
+  const bool in_smem = B <= PLAN_SMEM_B;
+  const int32_t* P = in_smem ? s_prefix : prefix;
+  const int32_t* TL = in_smem ? s_tiles : tiles;
   const long long T = carry;
   const long long per_g = T + static_cast<long long>(K) * B;  // F of one whole group
   const long long F_total = per_g * G;
@@ -72,12 +88,12 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
       int lo = 0, hi = B;  // largest b with prefix[b] + K b <= r
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (prefix[mid] + static_cast<long long>(K) * mid <= r) lo = mid; else hi = mid;
+        if (P[mid] + static_cast<long long>(K) * mid <= r) lo = mid; else hi = mid;
       }
       // past the end of sequence lo: cut at its end (the next sequence's start)
-      const long long j = min(r - prefix[lo] - static_cast<long long>(K) * lo,
-                              static_cast<long long>(tiles[lo]));
-      v = g * T + prefix[lo] + j;
+      const long long j = min(r - P[lo] - static_cast<long long>(K) * lo,
+                              static_cast<long long>(TL[lo]));
+      v = g * T + P[lo] + j;
     }
     bounds[c] = v;
     if (c < C) {
@@ -87,7 +103,7 @@ __device__ void write_plan(const int32_t* __restrict__ seq_lens, int B, int n_q,
         int lo = 0, hi = B;  // largest b with prefix[b] <= rem: the sequence holding item v
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
-          if (prefix[mid] <= rem) lo = mid; else hi = mid;
+          if (P[mid] <= rem) lo = mid; else hi = mid;
         }
         b = lo;
       }
