@@ -84,9 +84,18 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   const uint32_t tmem = sm.tmem_base;
   bool ok = true;
 
+  // With programmatic dependent launch this CTA may start while the previous
+  // kernel (the append) still runs: pull W_uk[h] into L2 (coherent, so safe
+  // at any time), then wait for that kernel before loading anything into the
+  // SM or reading the queries.
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_q);
+    for (int j = 0; j < 4; ++j)
+      for (int kc = 0; kc < 2; ++kc) tma_prefetch_2d(&tmap_w, 64 * kc, h * 512 + 128 * j);
+  }
+  griddep_wait();
+  if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&sm.full_q, 2 * n_tok_box * 128);
     for (int kc = 0; kc < 2; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full_q);
     for (int j = 0; j < 4; ++j) {
@@ -214,12 +223,21 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  dim3 grid(s.n_h, (Tq + AT_TOK - 1) / AT_TOK);
-  absorb_q_tc_kernel<<<grid, AT_THREADS, smem, st>>>(
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.n_h, (Tq + AT_TOK - 1) / AT_TOK, 1);
+  cfg.blockDim = dim3(AT_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  // may start while the previous kernel finishes (see the kernel's wait)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, absorb_q_tc_kernel,
       tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
       p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles,
       ws.prefix, ws.bounds, ws.first_b, err);
-  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -376,11 +376,19 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  // With programmatic dependent launch this CTA may start while the previous
+  // kernel still runs: pull the weight slice into L2 (coherent, so safe at
+  // any time), then wait for that kernel before loading anything into the SM
+  // or touching the hidden states and the cache.
+  const int k0 = static_cast<int>(kc) * nkb * 64;
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_x);
+    for (int j = 0; j < nkb; ++j) tma_prefetch_2d(&tmap_w, k0 + 64 * j, mb * 128);
+  }
+  griddep_wait();
+  if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&full, nkb * (AT_WBOX + N * 128));
-    const int k0 = static_cast<int>(kc) * nkb * 64;
     for (int j = 0; j < nkb; ++j) {
       tma_load_2d(A + j * AT_WBOX, &tmap_w, k0 + 64 * j, mb * 128, &full);
       tma_load_2d(X + j * N * 128, &tmap_x, k0 + 64 * j, 0, &full);
@@ -398,6 +406,9 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     }
     mma_commit(&done);  // arrives once the MMAs (if any) are done
   }
+  // the next kernel (the query absorption) may be scheduled now; it waits
+  // for this grid before it reads anything this kernel writes
+  griddep_launch_dependents();
   // partial of this K slice: row (packed column) per lane, token per TMEM column
   const bool ok = mbar_wait(&done, 0, 2 * AT_WAIT);
   tc_fence_after();
@@ -553,13 +564,16 @@ bool launch_append_tc(const Shape& s, const Weights* w, const void* x, const App
   cfg.blockDim = dim3(AT_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kcn;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel finishes (see the kernel's wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   *err = cudaLaunchKernelEx(&cfg, append_tc_kernel, tw, tx, s, kcn, nkb, N, cols,
                             static_cast<__nv_bfloat16*>(cache), a);
   return true;
