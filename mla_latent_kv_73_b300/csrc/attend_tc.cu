@@ -59,13 +59,22 @@
 //               (one query row per lane, all 64 tokens), rounds the partial
 //               to fp16, writes the rounded values back to TMEM and the fp16
 //               words into the staging buffer, from which one thread copies
-//               them to the peer. They
-//               also put the TMEM part of Q in place at each piece.
+//               them to the peer. They also put the TMEM part of Q in place
+//               at each piece.
 //   warps 8..15 softmax: warp w reads lane quarter w % 4 and tokens
-//               [32h, 32h + 32), h = (w - 8) / 4. The two warps of a lane
-//               quarter meet at a 64-thread named barrier to agree on the
-//               row maximum. One set of warps handles every tile, so the
-//               running max and row sums live in registers.
+//               [32h, 32h + 32), h = (w - 8) / 4, and adds the peer's fp16
+//               partial to its own with one mixed-precision add per score.
+//               The two warps of a lane quarter meet at a 64-thread named
+//               barrier to agree on the row maximum. One set of warps handles
+//               every tile, so the running max and row sums live in
+//               registers.
+//
+// Work ranges. Each pair walks a contiguous range of (group, sequence, page)
+// items from the plan; ranges are balanced by pages plus a charge per
+// sequence piece (a piece change costs an epilogue and a Q load). The kernel
+// is launched with programmatic dependent launch: its setup overlaps the end
+// of the query-absorption kernel, and it reads nothing that kernel writes
+// before griddepcontrol.wait.
 //
 // Lazy rescale: a row's running max is only raised when the new max exceeds
 // it by more than 8 (log2 units). Otherwise P is computed against the stale

@@ -135,11 +135,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation: one full warp executes these.
@@ -288,34 +283,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
 }
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
 // Arrive (relaxed, cluster scope) on another CTA's mbarrier: orders nothing
 // before it, for signals whose prior accesses are loads already consumed.
 __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-// 16-byte store into another CTA's shared memory that counts its bytes
-// against that CTA's mbarrier (complete_tx).
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
-                                            float d, uint32_t cluster_mbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_mbar)
-      : "memory");
-}
-__device__ __forceinline__ void st_async_v4u(uint32_t cluster_addr, uint32_t a, uint32_t b,
-                                             uint32_t c, uint32_t d, uint32_t cluster_mbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_mbar)
-      : "memory");
 }
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into
 // another CTA's shared memory, counted on that CTA's mbarrier (complete_tx).
@@ -373,17 +345,6 @@ __device__ __forceinline__ void cluster_sync() {
 }
 constexpr uint32_t kSwizzle64B = 4;
 
-// Register rebalancing between warpgroups (all four warps of a warpgroup
-// execute these together). The counts must be multiples of 8, and the sum
-// over the block must stay within what the block was launched with.
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 // Named barrier over a subset of the block's warps.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
