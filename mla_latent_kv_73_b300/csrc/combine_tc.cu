@@ -99,48 +99,58 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   }
 
   // 1. per token: the CTAs holding its pieces and their merge weights
-  //    exp(lse_s - lse). One warp per token; the lanes take the pieces, so the
-  //    lse loads of a token are one round trip.
+  //    exp(lse_s - lse). The plan loads of all tokens go out together (the
+  //    range starts, and each token's tiles and prefix in one round trip);
+  //    then half a warp per token, its lanes taking the pieces, loads the
+  //    lse values, so two tokens per warp cost one more round trip.
   const long long T_all = prefix[B];
-  const long long N = T_all * p.G;
-  for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = N > 0 ? bounds[c] : 0;
+  for (int c = threadIdx.x; c <= p.C; c += CT_THREADS) rb[c] = bounds[c];  // all 0 without tiles
+  int my_tiles = 0, my_off = 0;
+  long long my_first = 0;
+  if (threadIdx.x < ntok) {
+    const int tok = t0 + threadIdx.x, b = tok / n_q, qi = tok % n_q;
+    const int r = qi * n_h + h, g = r / p.RG, rr = r % p.RG;
+    my_off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
+    my_tiles = tiles[b];
+    my_first = static_cast<long long>(g) * T_all + prefix[b];
+  }
+  __syncthreads();  // range starts in place
+  if (threadIdx.x < CT_TOK) {
+    int c0 = 0, c1 = -1;
+    if (my_tiles > 0) {
+      c0 = range_of_item(rb, p.C, my_first);
+      c1 = range_of_item(rb, p.C, my_first + my_tiles - 1);
+    }
+    sm.c_lo[threadIdx.x] = c0;
+    sm.c_hi[threadIdx.x] = c1;
+    sm.row_off[threadIdx.x] = my_off;
+  }
   __syncthreads();
   float* wts = reinterpret_cast<float*>(rb + p.C + 1);  // [CT_TOK][C + 1] merge weights
-  for (int t = warp; t < CT_TOK; t += CT_THREADS / 32) {
-    int c0 = 0, c1 = -1, off = 0;
-    if (t < ntok) {
-      const int tok = t0 + t, b = tok / n_q, qi = tok % n_q;
-      const int r = qi * n_h + h, g = r / p.RG, rr = r % p.RG;
-      off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
-      if (tiles[b] > 0) {
-        const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
-        c0 = range_of_item(rb, p.C, first);
-        c1 = range_of_item(rb, p.C, last);
-      }
-    }
+  for (int tb = 0; tb < ntok; tb += 2 * (CT_THREADS / 32)) {
+    const int t = tb + 2 * warp + (lane >> 4), hl = lane & 15;
+    const bool live = t < ntok;
+    const int c0 = live ? sm.c_lo[t] : 0, c1 = live ? sm.c_hi[t] : -1;
+    const int off = live ? sm.row_off[t] : 0;
     float M = -INFINITY;
-    for (int c = c0 + lane; c <= c1; c += 32) {
+    for (int c = c0 + hl; c <= c1; c += 16) {
       const float x = rb[c] != rb[c + 1] ? part_lse[static_cast<size_t>(c) * p.RG + off] : -INFINITY;
       wts[t * (p.C + 1) + (c - c0)] = x;
       M = fmaxf(M, x);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float den = 0.f;
-    for (int c = c0 + lane; c <= c1; c += 32) {
+    for (int c = c0 + hl; c <= c1; c += 16) {
       const float e = M == -INFINITY ? 0.f : expf(wts[t * (p.C + 1) + (c - c0)] - M);
       wts[t * (p.C + 1) + (c - c0)] = e;
       den += e;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int c = c0 + lane; c <= c1; c += 32) wts[t * (p.C + 1) + (c - c0)] *= inv;
-    if (lane == 0) {
-      sm.c_lo[t] = c0;
-      sm.c_hi[t] = (M == -INFINITY) ? -1 : c1;
-      sm.row_off[t] = off;
-    }
+    for (int c = c0 + hl; c <= c1; c += 16) wts[t * (p.C + 1) + (c - c0)] *= inv;
+    if (live && hl == 0 && M == -INFINITY) sm.c_hi[t] = -1;  // no piece holds a visible token
   }
   __syncthreads();
 
