@@ -346,3 +346,113 @@ def decode_head_absorbed(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
 def default_scale(d_nope, d_r):
     """Score scale 1/sqrt(d_nope + d_r). A head's query/key width is d_nope + d_r."""
     return 1.0 / math.sqrt(d_nope + d_r)
+
+
+# ---------------------------------------------------------------------------
+# One attention layer from the hidden state: x_q in, y out
+# ---------------------------------------------------------------------------
+
+
+def head_query_split(W_q, h, d_nope, d_r):
+    """(W_q,nope[h], W_qr[h]) of head h from W_q [d_model, n_h*(d_nope + d_r)].
+
+    Each head's query block is [q_nope | q_rope]; W_qr[h] is the matrix P1
+    calls ``W_qr`` in "The code" (``decoupled_score``).
+    """
+    W_q = np.asarray(W_q, dtype=np.float64)
+    dq = d_nope + d_r
+    return W_q[:, h * dq:h * dq + d_nope], W_q[:, h * dq + d_nope:(h + 1) * dq]
+
+
+def layer_output_materialised(x_q, seq_rows, seq_lens, W_q, W_uk, W_uv, W_o, d_c, d_nope,
+                              d_v, scale, base, tokens=None):
+    """Layer output y = concat_h(o_h) W_o, with every key and value materialised.
+
+    q = x_q W_q per head [P1 "The code", ``attention_via_latent``: the query
+    is the hidden state times W_q, cut into heads]; o_h is
+    :func:`decode_head_materialised`; the heads are concatenated and
+    projected by W_o [n_h*d_v, d_model] (reading: the pages list W_o among the
+    layer's weights, P1 "What it costs, said plainly", but print no output
+    projection; this is the usual one). Nothing is rounded: q is never
+    stored in this form.
+
+    x_q: [B, n_q, d_model]. ``tokens`` is None for every (b, i), or an
+    iterable of (b, i) pairs. Returns [B, n_q, d_model] (rows not computed
+    stay NaN) when tokens is None, else a dict keyed by (b, i).
+    """
+    x_q = np.asarray(x_q, dtype=np.float64)
+    B, n_q, _ = x_q.shape
+    W_q = np.asarray(W_q, dtype=np.float64)
+    W_o = np.asarray(W_o, dtype=np.float64)
+    n_h = W_o.shape[0] // d_v
+    d_r = W_q.shape[1] // n_h - d_nope
+    want = tokens if tokens is not None else [(b, i) for b in range(B) for i in range(n_q)]
+    res = {}
+    for (b, i) in want:
+        q = (x_q[b, i] @ W_q).reshape(n_h, d_nope + d_r)
+        L = int(seq_lens[b])
+        pos_q = L - n_q + i
+        o = np.concatenate([
+            decode_head_materialised(q[h], seq_rows[b][:L], pos_q, head_slice(W_uk, h, d_nope),
+                                     head_slice(W_uv, h, d_v), d_c, scale, base)
+            for h in range(n_h)])
+        res[(b, i)] = o @ W_o
+    if tokens is not None:
+        return res
+    out = np.full((B, n_q, W_o.shape[1]), np.nan)
+    for (b, i), v in res.items():
+        out[b, i] = v
+    return out
+
+
+def fold_value_output(W_uv_h, W_o_h):
+    """W_vo[h] = W_uv[h] W_o[h], shape (d_c, d_model), built once at load.
+
+    [P5] "The absorption trick and decoupled RoPE": the value-side
+    up-projection folds into the output projection the way W_uk folds into
+    the query side. W_o_h is the d_v rows of W_o that head h's output meets.
+    """
+    return np.asarray(W_uv_h, dtype=np.float64) @ np.asarray(W_o_h, dtype=np.float64)
+
+
+def layer_output_absorbed(x_q, seq_rows, seq_lens, W_q, W_uk, W_uv, W_o, d_c, d_nope, d_v,
+                          scale, base, tokens=None):
+    """:func:`layer_output_materialised` with both folds done first.
+
+    Per head: W_abs[h] = W_q,nope[h] W_uk[h]^T [P1 "Store the archive, not the
+    files" and "The code", ``absorb_q_into_latent``], W_vo[h] =
+    :func:`fold_value_output`. Then for each query token, content scores
+    (x_q W_abs[h]) c_j^T plus the decoupled part RoPE(x_q W_qr[h]) k_rope_j^T
+    [P1 "The code", ``decoupled_score``], softmax, o_lat = sum_j p_j c_j, and
+    y = sum_h o_lat[h] W_vo[h]. Used only to pin the algebra.
+    """
+    x_q = np.asarray(x_q, dtype=np.float64)
+    B, n_q, d_model = x_q.shape
+    W_o = np.asarray(W_o, dtype=np.float64)
+    n_h = W_o.shape[0] // d_v
+    d_r = np.asarray(W_q).shape[1] // n_h - d_nope
+    W_abs, W_qr, W_vo = [], [], []
+    for h in range(n_h):
+        wqn, wqr = head_query_split(W_q, h, d_nope, d_r)
+        W_abs.append(absorb_q_full(wqn, head_slice(W_uk, h, d_nope)))
+        W_qr.append(wqr)
+        W_vo.append(fold_value_output(head_slice(W_uv, h, d_v), W_o[h * d_v:(h + 1) * d_v]))
+    want = tokens if tokens is not None else [(b, i) for b in range(B) for i in range(n_q)]
+    res = {}
+    for (b, i) in want:
+        L = int(seq_lens[b])
+        pos_q = L - n_q + i
+        rows = np.asarray(seq_rows[b][:L], dtype=np.float64)
+        C, KR = rows[:, :d_c], rows[:, d_c:]
+        y = np.zeros(d_model)
+        for h in range(n_h):
+            s = (C @ (x_q[b, i] @ W_abs[h]) + KR @ apply_rope(x_q[b, i] @ W_qr[h], pos_q, base))
+            s = np.where(np.arange(L) <= pos_q, s * scale, -np.inf)
+            y += (softmax(s) @ C) @ W_vo[h]
+        res[(b, i)] = y
+    if tokens is not None:
+        return res
+    out = np.full((B, n_q, d_model), np.nan)
+    for (b, i), v in res.items():
+        out[b, i] = v
+    return out

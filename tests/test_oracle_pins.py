@@ -469,3 +469,121 @@ def test_planted_mistakes_are_caught(monkeypatch, target, idx):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"planted mistake in {target} went unnoticed"
+
+
+# ---------------------------------------------------------------------------
+# One layer from the hidden state: x_q in, y = concat_h(o_h) W_o out
+# ---------------------------------------------------------------------------
+
+
+def _layer(seed=7, n_h=3, d_model=24, d_c=16, d_r=4, d_nope=6, d_v=10, lens=(2, 9, 40), n_q=2):
+    g = np.random.default_rng(seed)
+    W_dkv = g.normal(0, d_model ** -0.5, (d_model, d_c))
+    W_kr = g.normal(0, d_model ** -0.5, (d_model, d_r))
+    W_q = g.normal(0, d_model ** -0.5, (d_model, n_h * (d_nope + d_r)))
+    W_uk = g.normal(0, d_c ** -0.5, (d_c, n_h * d_nope))
+    W_uv = g.normal(0, d_c ** -0.5, (d_c, n_h * d_v))
+    W_o = g.normal(0, (n_h * d_v) ** -0.5, (n_h * d_v, d_model))
+    rows = [O.latent_rows(g.normal(size=(L, d_model)), W_dkv, W_kr, np.arange(L), 1e4)
+            for L in lens]
+    x_q = g.normal(size=(len(lens), n_q, d_model))
+    return dict(W_q=W_q, W_uk=W_uk, W_uv=W_uv, W_o=W_o, rows=rows, lens=np.array(lens),
+                x_q=x_q, n_h=n_h, d_c=d_c, d_r=d_r, d_nope=d_nope, d_v=d_v,
+                scale=O.default_scale(d_nope, d_r))
+
+
+def _layer_args(t):
+    return (t["x_q"], t["rows"], t["lens"], t["W_q"], t["W_uk"], t["W_uv"], t["W_o"], t["d_c"],
+            t["d_nope"], t["d_v"], t["scale"], 1e4)
+
+
+def test_layer_output_under_permutation_weights():
+    """With W_q and W_o permutation matrices, the layer reduces to the
+    per-head outputs (pinned above against torch's attention) moved by index:
+    q[perm_q[j]] = x_q[j] and y[perm_o[j]] = concat_h(o_h)[j]."""
+    t = _layer(seed=8, d_v=10)  # d_model = n_h*(d_nope + d_r) = n_h*d_v = 30
+    n_h, dq = t["n_h"], t["d_nope"] + t["d_r"]
+    D = n_h * dq
+    g = np.random.default_rng(9)
+    perm_q, perm_o = g.permutation(D), g.permutation(D)
+    assert np.any(perm_q[perm_q] != np.arange(D)) and np.any(perm_o[perm_o] != np.arange(D))
+    P_q = np.zeros((D, D))
+    P_q[np.arange(D), perm_q] = 1.0
+    P_o = np.zeros((D, D))
+    P_o[np.arange(D), perm_o] = 1.0
+    x_q = g.normal(size=(len(t["lens"]), 2, D))
+    q = np.empty_like(x_q)
+    q[..., perm_q] = x_q
+    o = O.decode_materialised(q.reshape(len(t["lens"]), 2, n_h, dq), t["rows"], t["lens"],
+                              t["W_uk"], t["W_uv"], t["d_c"], t["d_nope"], t["d_v"], t["scale"], 1e4)
+    want = np.empty((len(t["lens"]), 2, D))
+    want[..., perm_o] = o.reshape(len(t["lens"]), 2, D)
+    got = O.layer_output_materialised(x_q, t["rows"], t["lens"], P_q, t["W_uk"], t["W_uv"], P_o,
+                                      t["d_c"], t["d_nope"], t["d_v"], t["scale"], 1e4)
+    assert np.max(np.abs(got - want)) <= 1e-12
+
+
+def test_layer_output_single_key_closed_form():
+    """One cached key gets all the weight, so every head's output is c W_uv[h]
+    and the layer output is c W_uv W_o whatever the query."""
+    t = _layer(seed=10, lens=(1,), n_q=1)
+    c = t["rows"][0][0, :t["d_c"]]
+    want = (c @ t["W_uv"]) @ t["W_o"]
+    for fn in (O.layer_output_materialised, O.layer_output_absorbed):
+        got = fn(*_layer_args(t))[0, 0]
+        assert np.max(np.abs(got - want)) <= 1e-12
+
+
+def test_layer_output_absorbed_equals_materialised():
+    """Both folds at once (P1's W_abs = W_q W_uk^T on the query side, P5's
+    W_uv W_o on the output side) change nothing but rounding."""
+    for seed in (11, 12):
+        t = _layer(seed=seed)
+        a = O.layer_output_absorbed(*_layer_args(t))
+        m = O.layer_output_materialised(*_layer_args(t))
+        assert np.all(np.isfinite(m))
+        assert np.max(np.abs(a - m)) <= gold("p1_params_macs.json")["float_noise_bound"]
+        # the sampled form returns the same rows
+        got = O.layer_output_materialised(*_layer_args(t), tokens=[(2, 1), (0, 0)])
+        assert np.array_equal(got[(2, 1)], m[2, 1]) and np.array_equal(got[(0, 0)], m[0, 0])
+
+
+def test_layer_output_absorbing_the_wrong_matrix():
+    """P1's "Now break it" row: folding W_uv where W_uk belongs keeps every
+    shape and changes the answer."""
+    t = _layer(seed=13, d_v=6)  # d_nope == d_v, so the swapped fold has the same shape
+    good = O.layer_output_absorbed(*_layer_args(t))
+    t2 = dict(t, W_uk=t["W_uv"])
+    bad = O.layer_output_absorbed(*_layer_args(t2))
+    assert bad.shape == good.shape and np.max(np.abs(bad - good)) > 1e-3
+
+
+def _layer_mutants():
+    def rope_block_first(W_q, h, d_nope, d_r):
+        W_q = np.asarray(W_q, dtype=np.float64)
+        dq = d_nope + d_r
+        return W_q[:, h * dq + d_r:(h + 1) * dq], W_q[:, h * dq:h * dq + d_r]
+
+    def reversed_latent(W_uv_h, W_o_h):
+        return np.asarray(W_uv_h, dtype=np.float64)[::-1] @ np.asarray(W_o_h, dtype=np.float64)
+
+    def no_transpose_fold(W_q_h, W_uk_h):
+        return np.asarray(W_q_h, dtype=np.float64) @ np.asarray(W_uk_h, dtype=np.float64)[:, ::-1].T
+
+    return {"head_query_split": [rope_block_first], "fold_value_output": [reversed_latent],
+            "absorb_q_full": [no_transpose_fold]}
+
+
+@pytest.mark.parametrize("target,idx",
+                         [(k, i) for k, v in _layer_mutants().items() for i in range(len(v))])
+def test_planted_layer_mistakes_are_caught(monkeypatch, target, idx):
+    monkeypatch.setattr(O, target, _layer_mutants()[target][idx])
+    failures = 0
+    for check in (test_layer_output_under_permutation_weights,
+                  test_layer_output_single_key_closed_form,
+                  test_layer_output_absorbed_equals_materialised):
+        try:
+            check()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"planted mistake in {target} went unnoticed"
