@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-heads", type=int, default=0,
                     help="(b, h) pairs in the oracle sample (0: about 10 s worth)")
+    ap.add_argument("--variant", choices=["per_head", "full_fold"], default="per_head",
+                    help="full_fold: time the folded layer (x_q in, y out) instead")
     return ap.parse_args()
 
 
@@ -451,6 +453,134 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
+def run_full_fold(args, world, rank, local):
+    """The full-fold layer: a step appends the new tokens and runs
+    mla_decode_full (hidden states in, layer output out). Every stage streams
+    from HBM, so the roofline is the whole call's algorithmic bytes (folded
+    fp32 weights, cache, activations) over its time. The per-head step on
+    the same inputs is timed beside it."""
+    import torch
+    from mla_latent_kv_73_b300 import _lib, synth
+    from mla_latent_kv_73_b300.device_inputs import DeviceWeights, config_for, to_device
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    _lib.load()
+    w = synth.WORKLOADS[args.workload]
+    lens = synth.seq_lens(w)
+    B, n_q = w.batch, w.n_q
+    Tq = B * n_q
+    cfg = config_for(w)
+    impl = _lib.mla_decode_impl(cfg)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pt_np, num_blocks = synth.page_table(w, lens)
+    cache_bytes, _ = algorithmic(w, lens)
+    wts = synth.weights(w)
+    raw = {k: to_device(v, w.dtype) for k, v in wts.raw.items()}
+    fw = _lib.mla_fold_full(cfg, raw["W_q"], raw["W_uk"], raw["W_uv"], raw["W_o"])
+    dw = DeviceWeights(w, wts, cfg)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2000 + rank)
+    cache = torch.randn((num_blocks, w.block_size, w.R), generator=gen, device="cuda").to(dt)
+    pt = to_device(pt_np, "i32")
+    x = torch.randn((Tq, w.d_model), generator=gen, device="cuda").to(dt)
+    q = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen, device="cuda").to(dt)
+    seq_lens = to_device(lens, "i32")
+    seq_idx = to_device(np.repeat(np.arange(B), n_q).astype(np.int32), "i32")
+    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32), "i32")
+    y = torch.empty((B, n_q, w.d_model), device="cuda")
+    out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
+    ws_f = torch.empty(_lib.mla_decode_full_workspace_size(cfg, B, n_q), dtype=torch.uint8,
+                       device="cuda")
+    ws_h = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q, int(lens.sum())),
+                       dtype=torch.uint8, device="cuda")
+
+    def full(st):
+        _lib.mla_append_kv(cfg, dw.handle, x, seq_idx, pos, pt, cache, st)
+        _lib.mla_decode_full(cfg, fw, x.view(B, n_q, w.d_model), cache, pt, seq_lens, y, ws_f, st)
+
+    def per_head(st):
+        _lib.mla_append_kv(cfg, dw.handle, x, seq_idx, pos, pt, cache, st)
+        _lib.mla_decode(cfg, dw.handle, q, cache, pt, seq_lens, out, ws_h, st)
+
+    stream = torch.cuda.current_stream()
+    graphs = {}
+    for name, fn in (("full", full), ("per_head", per_head)):
+        for _ in range(args.warmup):
+            fn(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        graphs[name] = g
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} after warm-up")
+    K = args.steps
+    times = {}
+    clocks = None
+    for name in ("per_head", "full"):
+        for _ in range(3):
+            graphs[name].replay()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            barrier(dist)
+            torch.cuda.synchronize()
+            wall0 = time.time()
+            t0.record()
+            for _ in range(K):
+                graphs[name].replay()
+            t1.record()
+            torch.cuda.synchronize()
+            barrier(dist)
+            wall1 = time.time()
+        if name == "full":
+            clocks = clk.summary(wall0, wall1)
+        times[name] = max_over_ranks(t0.elapsed_time(t1), dist, "cuda") / K
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+    ms = times["full"]
+    folded = 4 * (w.d_model * w.n_h * w.R + w.n_h * w.d_c * w.d_model)
+    step_bytes = folded + cache_bytes + (w.R * w.d_model) * w.elem_bytes  # + append's weights
+    hbm, _, _, src = measured_peaks()
+    achieved = step_bytes / (ms / 1e3) / 1e9
+    line = {
+        "metric": "full-fold layer tokens/s (hidden state in, layer output out)",
+        "variant": "full_fold",
+        "value": round(sum_over_ranks(Tq, dist, "cuda") / (ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) cache rows and hidden states; N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "batch": B, "n_q": n_q, "n_h": w.n_h,
+                   "d_model": w.d_model, "d_c": w.d_c, "d_r": w.d_r,
+                   "decode_kernel": "tensor_core" if impl == 2 else "cuda_core",
+                   "l2": f"one input set; {folded / 2**20:.0f} MiB of folded weights stream "
+                         f"through L2 every step"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
+                     "kernel": "mla_decode_full + append (all stages HBM-bound)",
+                     "bytes_per_step": step_bytes, "folded_weight_bytes": folded},
+        "per_head_ms_per_step": round(times["per_head"], 5),
+        "full_over_per_head": round(ms / times["per_head"], 2),
+        "clocks": clocks,
+    }
+    _lib.mla_full_weights_free(fw)
+    dw.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------------------
 # the oracle (CPU) arm
 # ---------------------------------------------------------------------------
@@ -541,6 +671,9 @@ def main():
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.variant == "full_fold":
+        run_full_fold(args, world, rank, local)
         return
     run_ours(args, world, rank, local)
 

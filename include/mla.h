@@ -38,10 +38,11 @@
  * Memory and streams. Every pointer argument is a DEVICE pointer to memory
  * the caller owns and keeps alive until the work queued on `stream` has
  * finished. The only exception is the out-parameters of the host-side query
- * functions (mla_decode_workspace_size, mla_get_last_device_error), which
- * are host pointers. All compute calls are asynchronous on `stream` and
- * return once the work is queued. The library allocates device memory only
- * inside mla_absorb_weights. It never allocates on the decode path.
+ * functions (mla_decode_workspace_size, mla_decode_full_workspace_size,
+ * mla_get_last_device_error), which are host pointers. All compute calls are
+ * asynchronous on `stream` and return once the work is queued. The library
+ * allocates device memory only inside mla_absorb_weights and mla_fold_full.
+ * It never allocates on the decode path.
  *
  * Errors. Each call checks its arguments on the host before queueing any
  * work. A failed check returns a status other than MLA_OK and queues
@@ -223,6 +224,70 @@ mla_status mla_decode_no_alloc(const mla_config* cfg, mla_weights w, const void*
                                const void* cache, int32_t num_blocks, const int32_t* page_table,
                                int32_t max_blocks, const int32_t* seq_lens, int32_t B,
                                int32_t n_q, float* out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Full-fold variant: one attention layer from the hidden state.
+ *
+ * Both up-projections are folded into the neighbouring projections once,
+ * at load, so the decode call takes the query token's hidden state x_q and
+ * returns the layer output y:
+ *     W_abs[h] = W_q,nope[h] W_uk[h]^T      (d_model x d_c)
+ *     W_vo[h]  = W_uv[h] W_o[h]             (d_c x d_model)
+ *     q_lat    = x_q W_abs[h],  q_pe = RoPE(x_q W_qr[h], pos_i)
+ *     o_lat    = the latent attention of mla_decode
+ *     y        = sum_h o_lat[h] W_vo[h]  =  concat_h(o_h) W_o
+ * Sources: "Multi-head Latent Attention: the KV cache, compressed", sections
+ * "Store the archive, not the files" (fold W_q and W_uk once, at load) and
+ * "The code" (absorb_q_into_latent; decoupled_score keeps the rotary query
+ * block W_qr out of the fold); "Multi-head Latent Attention and KV Cache
+ * Compression", section "The absorption trick and decoupled RoPE" (W_uv
+ * folds into the output projection).
+ * The first page's caveat applies: at DeepSeek-V2 widths the folded
+ * matrices are far larger than W_uk and W_uv (4.5x on the query side and
+ * 40x on the output side), so this form pays only at small widths. The
+ * per-head path above is the one for large models.
+ * ------------------------------------------------------------------------ */
+typedef struct mla_full_weights_s* mla_full_weights; /* opaque, library-owned */
+
+/* Build the folded matrices, once at load.
+ *   W_q  [d_model, n_h*(d_nope + d_r)] row-major, cfg->dtype; head h owns
+ *        columns [h*(d_nope+d_r), (h+1)*(d_nope+d_r)) as [q_nope | q_rope]
+ *   W_uk [d_c, n_h*d_nope], W_uv [d_c, n_h*d_v]  as in mla_absorb_weights
+ *   W_o  [n_h*d_v, d_model] row-major, cfg->dtype; head h's output meets
+ *        rows [h*d_v, (h+1)*d_v)
+ * The folded matrices are stored in fp32, d_model*n_h*(d_c+d_r) +
+ * n_h*d_c*d_model elements; the fold accumulates in fp64. Allocates them,
+ * queues the folding kernels on `stream` and returns the handle in *out.
+ * The caller's buffers may be freed once `stream` has passed this call.
+ * Release the handle with mla_full_weights_free. */
+mla_status mla_fold_full(const mla_config* cfg, const void* W_q, const void* W_uk,
+                         const void* W_uv, const void* W_o, cudaStream_t stream,
+                         mla_full_weights* out);
+
+/* Free a handle from mla_fold_full. Waits for the device to finish work
+ * that may still use it. NULL is accepted. */
+mla_status mla_full_weights_free(mla_full_weights w);
+
+/* Bytes of device workspace that mla_decode_full needs for B sequences with
+ * n_q query tokens each, on the current device. Writes the size to *bytes
+ * (a host pointer). */
+mla_status mla_decode_full_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                          size_t* bytes);
+
+/* The attention layer for B sequences with n_q new tokens each.
+ *   x_q        [B, n_q, d_model] cfg->dtype: hidden states of the query tokens
+ *   cache, num_blocks, page_table, max_blocks, seq_lens  as in mla_decode
+ *   y          [B, n_q, d_model] fp32 layer output
+ *   workspace  device buffer of at least mla_decode_full_workspace_size()
+ *              bytes, 256-byte aligned; its contents on entry do not matter
+ * The query projection and the output projection accumulate in fp32 (the
+ * projected query is rounded to cfg->dtype before the attention, like q in
+ * mla_decode). The decode kernel is chosen as in mla_decode. Errors as in
+ * mla_decode. */
+mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const void* x_q,
+                           const void* cache, int32_t num_blocks, const int32_t* page_table,
+                           int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                           float* y, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Which decode kernel mla_decode would run for this config on the current
  * device. Writes an mla_impl value other than MLA_IMPL_AUTO to *impl, a host

@@ -24,7 +24,9 @@ MLA_DEVERR_PAGE_RANGE, MLA_DEVERR_SEQ_LEN, MLA_DEVERR_APPEND_INDEX, MLA_DEVERR_T
 EXPORTS = ["mla_absorb_weights", "mla_weights_free", "mla_append_kv",
            "mla_decode_workspace_size", "mla_decode", "mla_decode_absorb_q",
            "mla_decode_attend", "mla_decode_combine", "mla_decode_impl",
-           "mla_get_last_device_error", "mla_status_string", "mla_decode_no_alloc"]
+           "mla_get_last_device_error", "mla_status_string", "mla_decode_no_alloc",
+           "mla_fold_full", "mla_full_weights_free", "mla_decode_full_workspace_size",
+           "mla_decode_full"]
 MLA_NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -61,6 +63,10 @@ def _declare(lib):
         "mla_decode_combine": [cfgp, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_decode_impl": [cfgp, ctypes.POINTER(_I)],
         "mla_decode_no_alloc": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P],
+        "mla_fold_full": [cfgp, _P, _P, _P, _P, _P, ctypes.POINTER(_P)],
+        "mla_full_weights_free": [_P],
+        "mla_decode_full_workspace_size": [cfgp, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
+        "mla_decode_full": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_get_last_device_error": [_P, ctypes.POINTER(ctypes.c_uint32)],
         "mla_status_string": [_I],
     }
@@ -185,6 +191,36 @@ def mla_decode_impl(cfg):
     v = _I()
     check("mla_decode_impl", load().mla_decode_impl(ctypes.byref(cfg), ctypes.byref(v)))
     return v.value
+
+
+def mla_fold_full(cfg, W_q, W_uk, W_uv, W_o, stream=None):
+    """Folded weights of the full-fold layer (see include/mla.h)."""
+    lib = load()
+    h = ctypes.c_void_p()
+    check("mla_fold_full", lib.mla_fold_full(
+        ctypes.byref(cfg), ptr(W_q), ptr(W_uk), ptr(W_uv), ptr(W_o), stream_handle(stream),
+        ctypes.byref(h)))
+    return h
+
+
+def mla_full_weights_free(h):
+    check("mla_full_weights_free", load().mla_full_weights_free(h))
+
+
+def mla_decode_full_workspace_size(cfg, B, n_q):
+    n = ctypes.c_size_t()
+    check("mla_decode_full_workspace_size", load().mla_decode_full_workspace_size(
+        ctypes.byref(cfg), B, n_q, ctypes.byref(n)))
+    return n.value
+
+
+def mla_decode_full(cfg, fw, x_q, cache, page_table, seq_lens, y, workspace, stream=None):
+    """y [B, n_q, d_model] from the hidden states x_q [B, n_q, d_model]."""
+    B, n_q = x_q.shape[0], x_q.shape[1]
+    check("mla_decode_full", load().mla_decode_full(
+        ctypes.byref(cfg), fw, ptr(x_q), ptr(cache), cache.shape[0], ptr(page_table),
+        page_table.shape[1], ptr(seq_lens), B, n_q, ptr(y), ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream)))
 
 
 def mla_get_last_device_error(stream=None):

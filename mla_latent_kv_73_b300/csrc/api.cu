@@ -198,6 +198,11 @@ struct mla_weights_s {
   mla_config cfg;
 };
 
+struct mla_full_weights_s {
+  mla::FullWeights w;
+  mla_config cfg;
+};
+
 using namespace mla;
 
 namespace {
@@ -229,6 +234,27 @@ mla_status prepare_decode(const mla_config* cfg, int B, int n_q, const void* cac
   if (ws_bytes < plan->lay.total) return MLA_ERR_WORKSPACE;
   *di_out = di;
   return MLA_OK;
+}
+
+// Device scratch of mla_decode_full beyond the per-head decode's workspace:
+// the fp32 query projection [B*n_q][n_h*R] (reused for o_lat, which is no
+// wider), then the split partials of the two x W products.
+struct FullExtra {
+  XwPlan q, o;
+  size_t proj, part, total;
+};
+
+FullExtra full_extra(const Shape& s, int B, int n_q, int sms) {
+  FullExtra f;
+  const int M = B * n_q;
+  f.q = xw_plan(M, s.d_model, s.n_h * s.R(), sms);
+  f.o = xw_plan(M, s.n_h * s.d_c, s.d_model, sms);
+  f.proj = align256(sizeof(float) * static_cast<size_t>(M) * s.n_h * s.R());
+  const size_t pq = xw_part_floats(M, s.n_h * s.R(), f.q);
+  const size_t po = xw_part_floats(M, s.d_model, f.o);
+  f.part = align256(sizeof(float) * (pq > po ? pq : po));
+  f.total = f.proj + f.part;
+  return f;
 }
 
 }  // namespace
@@ -459,6 +485,129 @@ mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const
                          workspace, ws_bytes, stream);
   if (st != MLA_OK) return st;
   return mla_decode_combine(&c2, w, seq_lens, B, n_q, out, workspace, ws_bytes, stream);
+}
+
+mla_status mla_fold_full(const mla_config* cfg, const void* W_q, const void* W_uk,
+                         const void* W_uv, const void* W_o, cudaStream_t stream,
+                         mla_full_weights* out) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (!W_q || !W_uk || !W_uv || !W_o) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  const int dev = current_device();
+  const Shape s = shape_of(cfg);
+  const size_t n_qf = sizeof(float) * static_cast<size_t>(s.d_model) * s.n_h * s.R();
+  const size_t n_vo = sizeof(float) * static_cast<size_t>(s.n_h) * s.d_c * s.d_model;
+  const int half = s.d_r / 2;
+  mla_full_weights_s* h = new (std::nothrow) mla_full_weights_s();
+  if (!h) return MLA_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->w.shape = s;
+  h->w.dtype = cfg->dtype;
+  h->w.device = dev;
+  auto release = [h]() {
+    cudaFree(h->w.w_qf);
+    cudaFree(h->w.w_vo);
+    cudaFree(h->w.inv_freq);
+    delete h;
+  };
+  if (cudaMalloc(&h->w.w_qf, n_qf) != cudaSuccess || cudaMalloc(&h->w.w_vo, n_vo) != cudaSuccess ||
+      cudaMalloc(&h->w.inv_freq, sizeof(double) * half) != cudaSuccess) {
+    cudaGetLastError();
+    release();
+    return MLA_ERR_CUDA;
+  }
+  double inv[512];
+  for (int i = 0; i < half; ++i)
+    inv[i] = std::pow(static_cast<double>(cfg->rope_base), -2.0 * i / s.d_r);
+  cudaError_t e = cudaMemcpyAsync(h->w.inv_freq, inv, sizeof(double) * half,
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess)
+    e = launch_fold_full(s, cfg->dtype, W_q, W_uk, W_uv, W_o, &h->w, di->sms, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaStreamSynchronize(stream);
+    release();
+    return MLA_ERR_CUDA;
+  }
+  *out = h;
+  return MLA_OK;
+}
+
+mla_status mla_full_weights_free(mla_full_weights w) {
+  if (!w) return MLA_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(w->w.device);
+  cudaDeviceSynchronize();
+  cudaFree(w->w.w_qf);
+  cudaFree(w->w.w_vo);
+  cudaFree(w->w.inv_freq);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete w;
+  return MLA_OK;
+}
+
+mla_status mla_decode_full_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                          size_t* bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = 0;
+  size_t base = 0;
+  mla_status st = mla_decode_workspace_size(cfg, B, n_q, 0, &base);
+  if (st != MLA_OK) return st;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  *bytes = base + full_extra(shape_of(cfg), B, n_q, di->sms).total;
+  return MLA_OK;
+}
+
+mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const void* x_q,
+                           const void* cache, int32_t num_blocks, const int32_t* page_table,
+                           int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                           float* y, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!fw || !x_q || !cache || !page_table || !seq_lens || !y) return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di, true);
+  if (st != MLA_OK) return st;
+  if (!same_shape(cfg, &fw->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != fw->w.device) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * cfg->block_size > (1LL << 31) - 1) return MLA_ERR_SHAPE;
+  const FullExtra fx = full_extra(p.s, B, n_q, di->sms);
+  if (ws_bytes < p.lay.total + fx.total) return MLA_ERR_WORKSPACE;
+  const WsView v = ws_view(workspace, p.lay);
+  float* proj = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.lay.total);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.lay.total + fx.proj);
+  const int M = B * n_q;
+  // 1. x_q [W_abs[h] | W_qr[h]] for every head, then RoPE, scale, rounding and the plan
+  cudaError_t e = launch_xw(cfg->dtype, x_q, M, p.s.d_model, fw->w.w_qf, p.s.n_h * p.s.R(), proj,
+                            part, fx.q, stream);
+  const float out_scale =
+      p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
+  if (e == cudaSuccess)
+    e = launch_q_finish(p.s, cfg->dtype, fw->w.inv_freq, proj, seq_lens, max_blocks, B, n_q,
+                        p.part, v, out_scale, di->err, stream);
+  // 2. split-KV latent attention, the same kernels as mla_decode
+  if (e == cudaSuccess) {
+    if (p.impl == MLA_IMPL_TENSOR_CORE)
+      e = launch_attend_tc(p.s, cache, num_blocks, page_table, max_blocks, B, n_q, p.part, v,
+                           seq_lens, di->err, stream);
+    else
+      e = launch_attend_simt(p.s, cfg->dtype, cache, num_blocks, page_table, max_blocks, B, n_q,
+                             p.part, v, seq_lens, di->err, stream);
+  }
+  // 3. merge the splits into o_lat (over the projection, which is spent)
+  if (e == cudaSuccess) e = launch_combine_latent(p.s, B, n_q, p.part, v, proj, stream);
+  // 4. y = sum_h o_lat[h] W_vo[h]
+  if (e == cudaSuccess)
+    e = launch_xw(MLA_F32, proj, M, p.s.n_h * p.s.d_c, fw->w.w_vo, p.s.d_model, y, part, fx.o,
+                  stream);
+  return from_cuda(e);
 }
 
 mla_status mla_get_last_device_error(cudaStream_t stream, uint32_t* code) {

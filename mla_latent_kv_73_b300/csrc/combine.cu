@@ -13,7 +13,8 @@
 //
 // One CTA per (head, tile of 16 query tokens). It streams that head's
 // [d_v x d_c] slice of W_uv once with 16-byte loads and reuses each element
-// for all 16 tokens.
+// for all 16 tokens. In latent mode (the full-fold layer, whose output
+// projection has W_uv folded in) it writes o_lat instead and stops there.
 #include <cmath>
 
 #include "device_common.cuh"
@@ -33,7 +34,7 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
                const int32_t* __restrict__ prefix, const long long* __restrict__ bounds, int B,
                int n_q, Partition p,
                const float* __restrict__ part_o, const float* __restrict__ part_lse,
-               float* __restrict__ out) {
+               float* __restrict__ out, float* __restrict__ olat_out) {
   extern __shared__ __align__(16) float sm[];
   float* olat = sm;                                   // [d_c][CB_TOK]
   float* half_out = olat + s.d_c * CB_TOK;            // [2][CB_TOK][d_v]
@@ -89,6 +90,13 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
     }
   }
   __syncthreads();
+  if (olat_out) {  // latent mode: o_lat [B*n_q][n_h*d_c], no up-projection
+    for (int i = threadIdx.x; i < ntok * s.d_c; i += CB_THREADS) {
+      const int t = i / s.d_c, dc = i % s.d_c;
+      olat_out[(static_cast<size_t>(tok0 + t) * s.n_h + h) * s.d_c + dc] = olat[dc * CB_TOK + t];
+    }
+    return;
+  }
 
   // 3. out = o_lat W_uv[h]: W_uv is packed [h][d_v][d_c]. A thread owns one
   // output column for all 16 tokens and half of the d_c reduction.
@@ -140,8 +148,8 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
 }
 
 template <typename T>
-cudaError_t combine_t(const Shape& s, const Weights* w, int B, int n_q, const Partition& p,
-                      const WsView& ws, float* out, cudaStream_t st) {
+cudaError_t combine_t(const Shape& s, const T* w_uv, int B, int n_q, const Partition& p,
+                      const WsView& ws, float* out, float* olat, cudaStream_t st) {
   const int Tq = B * n_q;
   dim3 grid(s.n_h, (Tq + CB_TOK - 1) / CB_TOK);
   const size_t smem = sizeof(float) * (CB_TOK * s.d_c + 2 * CB_TOK * s.d_v) +
@@ -152,8 +160,8 @@ cudaError_t combine_t(const Shape& s, const Weights* w, int B, int n_q, const Pa
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, CB_THREADS, smem, st>>>(s, static_cast<const T*>(w->w_uv), ws.tiles, ws.prefix,
-                                       ws.bounds, B, n_q, p, ws.part_o, ws.part_lse, out);
+  kern<<<grid, CB_THREADS, smem, st>>>(s, w_uv, ws.tiles, ws.prefix, ws.bounds, B, n_q, p,
+                                       ws.part_o, ws.part_lse, out, olat);
   return cudaGetLastError();
 }
 
@@ -163,8 +171,16 @@ cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
                            const WsView& ws, float* out, cudaStream_t st) {
   (void)seq_lens;
-  if (dt == MLA_F32) return combine_t<float>(s, w, B, n_q, p, ws, out, st);
-  return combine_t<__nv_bfloat16>(s, w, B, n_q, p, ws, out, st);
+  if (dt == MLA_F32)
+    return combine_t<float>(s, static_cast<const float*>(w->w_uv), B, n_q, p, ws, out, nullptr,
+                            st);
+  return combine_t<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(w->w_uv), B, n_q, p, ws,
+                                  out, nullptr, st);
+}
+
+cudaError_t launch_combine_latent(const Shape& s, int B, int n_q, const Partition& p,
+                                  const WsView& ws, float* olat, cudaStream_t st) {
+  return combine_t<float>(s, nullptr, B, n_q, p, ws, nullptr, olat, st);
 }
 
 }  // namespace mla

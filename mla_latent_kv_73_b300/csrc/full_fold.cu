@@ -1,0 +1,303 @@
+// Full-fold variant of the decode layer: the hidden state x_q goes in and the
+// layer output y comes out, with both up-projections folded into the
+// neighbouring projections once, at load:
+//
+//   W_abs[h] = W_q,nope[h] W_uk[h]^T     (d_model x d_c)  query side
+//   W_vo[h]  = W_uv[h] W_o[h]            (d_c x d_model)  output side
+//
+//   q_lat[t, h] = x_q[t] W_abs[h],   q_pe[t, h] = RoPE(x_q[t] W_qr[h], pos_t)
+//   o_lat[t, h] = latent attention over the cache (the same kernels as the
+//                 per-head path)
+//   y[t]        = sum_h o_lat[t, h] W_vo[h]
+//
+// Sources: "Multi-head Latent Attention: the KV cache, compressed", sections
+// "Store the archive, not the files" (W_abs = W_q W_uk^T, built once at
+// load) and "The code" (absorb_q_into_latent; decoupled_score keeps the
+// rotary block W_qr apart and rotates x_q W_qr at the query position);
+// "Multi-head Latent Attention and KV Cache Compression", section "The
+// absorption trick and decoupled RoPE" (the value up-projection folds into
+// the output projection the same way).
+//
+// The first page warns that at DeepSeek's ratios the fold costs more than
+// it saves ("Absorption: the part that makes it free"): W_abs is d_model x d_c
+// per head where W_q,nope is d_model x d_nope, so the folded weights stream
+// R/d_nope = 4.5x (query side) and d_model/d_v = 40x (output side) more bytes
+// per step at DeepSeek-V2 shapes. It pays at small model widths.
+//
+// Folded weights are kept in fp32 (the product of two rounded matrices is
+// not a value of the input dtype); the fold accumulates in fp64. The two
+// x W products are HBM-bound weight streams: a CTA owns 1024 output columns
+// (4 per thread, 16-byte loads) and 16 query rows, and K is split across
+// CTAs until the grid covers the SMs twice. The split partials are summed in
+// a fixed order by a second kernel, so results are deterministic.
+#include "device_common.cuh"
+#include "plan.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int XW_THREADS = 256;
+constexpr int XW_VEC = 4;                      // output columns per thread
+constexpr int XW_COLS = XW_THREADS * XW_VEC;   // output columns per CTA
+constexpr int XW_ROWS = 16;                    // rows of A (query tokens) per CTA
+constexpr int XW_KC = 64;                      // K chunk staged in shared memory
+constexpr int QF_THREADS = 256;
+constexpr int FOLD_THREADS = 256;
+
+// out[z][m][n] = sum over k in split z of A[m][k] W[k][n], fp32 accumulation
+// in k order. W is fp32 row-major [K][N]; A is [M][K] in TA.
+template <typename TA>
+__global__ void __launch_bounds__(XW_THREADS)
+xw_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, int N,
+          int k_split, float* __restrict__ out) {
+  __shared__ __align__(16) float a_s[XW_KC][XW_ROWS];  // row index fastest
+  const int n0 = blockIdx.x * XW_COLS + threadIdx.x * XW_VEC;
+  const int m0 = blockIdx.y * XW_ROWS, mt = min(XW_ROWS, M - m0);
+  const int kb = blockIdx.z * k_split, ke = min(K, kb + k_split);
+  const bool vec = (N % XW_VEC == 0) && n0 + XW_VEC <= N;
+  float acc[XW_ROWS][XW_VEC];
+#pragma unroll
+  for (int t = 0; t < XW_ROWS; ++t)
+#pragma unroll
+    for (int j = 0; j < XW_VEC; ++j) acc[t][j] = 0.f;
+
+  for (int k0 = kb; k0 < ke; k0 += XW_KC) {
+    const int kc = min(XW_KC, ke - k0);
+    __syncthreads();  // the previous chunk is consumed
+    for (int i = threadIdx.x; i < XW_KC * XW_ROWS; i += XW_THREADS) {
+      const int t = i / XW_KC, k = i % XW_KC;  // consecutive threads walk k: coalesced in A
+      a_s[k][t] = (t < mt && k < kc) ? to_f32<TA>(A[static_cast<size_t>(m0 + t) * K + k0 + k])
+                                     : 0.f;
+    }
+    __syncthreads();
+    if (n0 < N) {
+#pragma unroll 4
+      for (int k = 0; k < kc; ++k) {
+        const float* wp = W + static_cast<size_t>(k0 + k) * N + n0;
+        float w[XW_VEC];
+        if (vec) {
+          const float4 v = *reinterpret_cast<const float4*>(wp);
+          w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < XW_VEC; ++j) w[j] = n0 + j < N ? wp[j] : 0.f;
+        }
+        const float4* av = reinterpret_cast<const float4*>(a_s[k]);
+#pragma unroll
+        for (int u = 0; u < XW_ROWS / 4; ++u) {
+          const float4 a = av[u];
+#pragma unroll
+          for (int j = 0; j < XW_VEC; ++j) {
+            acc[4 * u + 0][j] = fmaf(a.x, w[j], acc[4 * u + 0][j]);
+            acc[4 * u + 1][j] = fmaf(a.y, w[j], acc[4 * u + 1][j]);
+            acc[4 * u + 2][j] = fmaf(a.z, w[j], acc[4 * u + 2][j]);
+            acc[4 * u + 3][j] = fmaf(a.w, w[j], acc[4 * u + 3][j]);
+          }
+        }
+      }
+    }
+  }
+  if (n0 >= N) return;
+  float* o = out + static_cast<size_t>(blockIdx.z) * M * N;
+  // rows start at multiples of 4 floats when N % 4 == 0: 16-byte stores need
+  // only an aligned base (the caller's y may be any float pointer)
+  const bool vec_out = vec && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+#pragma unroll
+  for (int t = 0; t < XW_ROWS; ++t) {
+    if (t >= mt) break;
+    float* orow = o + static_cast<size_t>(m0 + t) * N + n0;
+    if (vec_out) {
+      *reinterpret_cast<float4*>(orow) = make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < XW_VEC; ++j)
+        if (n0 + j < N) orow[j] = acc[t][j];
+    }
+  }
+}
+
+// out[i] = sum_z part[z][i], z in increasing order.
+__global__ void __launch_bounds__(256)
+sum_splits_kernel(const float* __restrict__ part, int S, size_t n, float* __restrict__ out) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < S; ++z) s += part[static_cast<size_t>(z) * n + i];
+    out[i] = s;
+  }
+}
+
+// qabs[t, h] = out_scale * [q_lat | RoPE(q_rope, pos_t)] in T, from the fp32
+// projection qpre[t][h*R + n]. Block 0 also writes the split-KV plan.
+template <typename T>
+__global__ void __launch_bounds__(QF_THREADS)
+q_finish_kernel(Shape s, const float* __restrict__ qpre, const double* __restrict__ inv_freq,
+                const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
+                int G, int C, int K, float out_scale, T* __restrict__ qabs, int32_t* tiles,
+                int32_t* prefix, long long* bounds, int32_t* first_b, uint32_t* err) {
+  if (blockIdx.x == 0)
+    write_plan<QF_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
+                           first_b, err);
+  const int tok = blockIdx.x, b = tok / n_q, qi = tok % n_q;
+  const int R = s.R(), half = s.d_r / 2, per_head = s.d_c + half;
+  const int pos = seq_lens[b] - n_q + qi;
+  const float* src = qpre + static_cast<size_t>(tok) * s.n_h * R;
+  T* dst = qabs + static_cast<size_t>(tok) * s.n_h * R;
+  for (int i = threadIdx.x; i < s.n_h * per_head; i += QF_THREADS) {
+    const int h = i / per_head, n = i % per_head;
+    const float* sh = src + static_cast<size_t>(h) * R;
+    T* dh = dst + static_cast<size_t>(h) * R;
+    if (n < s.d_c) {
+      dh[n] = from_f32<T>(sh[n] * out_scale);
+    } else {
+      const int k = n - s.d_c;
+      const float x1 = sh[s.d_c + k], x2 = sh[s.d_c + k + half];
+      float c, sn;
+      rope_cos_sin(pos, inv_freq[k], &c, &sn);
+      dh[s.d_c + k] = from_f32<T>((x1 * c - x2 * sn) * out_scale);
+      dh[s.d_c + k + half] = from_f32<T>((x1 * sn + x2 * c) * out_scale);
+    }
+  }
+}
+
+// w_qf[m][h*R + n]: W_abs[h][m][n] = sum_k W_q[m][h*dq + k] W_uk[n][h*d_nope + k]
+// for n < d_c, and the rotary query columns W_q[m][h*dq + d_nope + n - d_c]
+// unchanged for n >= d_c.
+template <typename T>
+__global__ void __launch_bounds__(FOLD_THREADS)
+fold_q_kernel(Shape s, const T* __restrict__ W_q, const T* __restrict__ W_uk,
+              float* __restrict__ w_qf) {
+  const int R = s.R(), dq = s.d_nope + s.d_r;
+  const size_t NC = static_cast<size_t>(s.n_h) * R;
+  const size_t total = static_cast<size_t>(s.d_model) * NC;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(idx / NC), col = static_cast<int>(idx % NC);
+    const int h = col / R, n = col % R;
+    const T* q = W_q + static_cast<size_t>(m) * s.n_h * dq + static_cast<size_t>(h) * dq;
+    float v;
+    if (n < s.d_c) {
+      const T* u = W_uk + static_cast<size_t>(n) * s.n_h * s.d_nope + static_cast<size_t>(h) * s.d_nope;
+      double acc = 0.0;
+      for (int k = 0; k < s.d_nope; ++k)
+        acc = fma(static_cast<double>(to_f32<T>(q[k])), static_cast<double>(to_f32<T>(u[k])), acc);
+      v = static_cast<float>(acc);
+    } else {
+      v = to_f32<T>(q[s.d_nope + n - s.d_c]);
+    }
+    w_qf[idx] = v;
+  }
+}
+
+// w_vo[h*d_c + c][m] = sum_k W_uv[c][h*d_v + k] W_o[h*d_v + k][m]
+template <typename T>
+__global__ void __launch_bounds__(FOLD_THREADS)
+fold_o_kernel(Shape s, const T* __restrict__ W_uv, const T* __restrict__ W_o,
+              float* __restrict__ w_vo) {
+  const size_t total = static_cast<size_t>(s.n_h) * s.d_c * s.d_model;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(idx / s.d_model), m = static_cast<int>(idx % s.d_model);
+    const int h = row / s.d_c, c = row % s.d_c;
+    const T* u = W_uv + static_cast<size_t>(c) * s.n_h * s.d_v + static_cast<size_t>(h) * s.d_v;
+    const T* o = W_o + static_cast<size_t>(h) * s.d_v * s.d_model + m;
+    double acc = 0.0;
+    for (int k = 0; k < s.d_v; ++k)
+      acc = fma(static_cast<double>(to_f32<T>(u[k])),
+                static_cast<double>(to_f32<T>(o[static_cast<size_t>(k) * s.d_model])), acc);
+    w_vo[idx] = static_cast<float>(acc);
+  }
+}
+
+int grid_for(size_t work, int sms) {
+  const size_t blocks = (work + 255) / 256;
+  return static_cast<int>(blocks < static_cast<size_t>(sms) * 16 ? (blocks ? blocks : 1)
+                                                                 : static_cast<size_t>(sms) * 16);
+}
+
+template <typename T>
+cudaError_t fold_t(const Shape& s, const void* W_q, const void* W_uk, const void* W_uv,
+                   const void* W_o, FullWeights* w, int sms, cudaStream_t st) {
+  const size_t nq = static_cast<size_t>(s.d_model) * s.n_h * s.R();
+  const size_t no = static_cast<size_t>(s.n_h) * s.d_c * s.d_model;
+  fold_q_kernel<T><<<grid_for(nq, sms), FOLD_THREADS, 0, st>>>(
+      s, static_cast<const T*>(W_q), static_cast<const T*>(W_uk), w->w_qf);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  fold_o_kernel<T><<<grid_for(no, sms), FOLD_THREADS, 0, st>>>(
+      s, static_cast<const T*>(W_uv), static_cast<const T*>(W_o), w->w_vo);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t q_finish_t(const Shape& s, const double* inv_freq, const float* qpre,
+                       const int32_t* seq_lens, int max_blocks, int B, int n_q, const Partition& p,
+                       const WsView& ws, float out_scale, uint32_t* err, cudaStream_t st) {
+  q_finish_kernel<T><<<B * n_q, QF_THREADS, 0, st>>>(
+      s, qpre, inv_freq, seq_lens, B, n_q, max_blocks, p.TS, p.G, p.C, p.K, out_scale,
+      static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, ws.bounds, ws.first_b, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+XwPlan xw_plan(int M, int K, int N, int sms) {
+  XwPlan p;
+  const long long tiles = static_cast<long long>((N + XW_COLS - 1) / XW_COLS) *
+                          ((M + XW_ROWS - 1) / XW_ROWS);
+  const int chunks = (K + XW_KC - 1) / XW_KC;
+  long long S = (2LL * sms + tiles - 1) / tiles;
+  if (S > chunks) S = chunks;
+  if (S < 1) S = 1;
+  if (S > 65535) S = 65535;
+  const int per = (chunks + static_cast<int>(S) - 1) / static_cast<int>(S);
+  p.k_split = per * XW_KC;
+  p.S = (K + p.k_split - 1) / p.k_split;
+  if (p.S < 1) p.S = 1;
+  return p;
+}
+
+size_t xw_part_floats(int M, int N, const XwPlan& p) {
+  return p.S > 1 ? static_cast<size_t>(p.S) * M * N : 0;
+}
+
+cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
+                      float* out, float* part, const XwPlan& p, cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  if (M > 65535 * XW_ROWS) return cudaErrorInvalidValue;
+  dim3 grid((N + XW_COLS - 1) / XW_COLS, (M + XW_ROWS - 1) / XW_ROWS, p.S);
+  float* dst = p.S > 1 ? part : out;
+  if (a_dt == MLA_F32)
+    xw_kernel<float><<<grid, XW_THREADS, 0, st>>>(static_cast<const float*>(A), M, K, W, N,
+                                                  p.k_split, dst);
+  else
+    xw_kernel<__nv_bfloat16><<<grid, XW_THREADS, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(A), M, K, W, N, p.k_split, dst);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.S == 1) return e;
+  const size_t n = static_cast<size_t>(M) * N;
+  const size_t blocks = (n + 255) / 256;
+  sum_splits_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(part, p.S, n,
+                                                                                       out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, const void* W_uk,
+                             const void* W_uv, const void* W_o, FullWeights* w, int sms,
+                             cudaStream_t st) {
+  if (dt == MLA_F32) return fold_t<float>(s, W_q, W_uk, W_uv, W_o, w, sms, st);
+  return fold_t<__nv_bfloat16>(s, W_q, W_uk, W_uv, W_o, w, sms, st);
+}
+
+cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
+                            const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
+                            int n_q, const Partition& p, const WsView& ws, float out_scale,
+                            uint32_t* err, cudaStream_t st) {
+  if (dt == MLA_F32)
+    return q_finish_t<float>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws, out_scale,
+                             err, st);
+  return q_finish_t<__nv_bfloat16>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws,
+                                   out_scale, err, st);
+}
+
+}  // namespace mla

@@ -67,6 +67,21 @@ struct Weights {
   double* inv_freq;  // [d_r/2] rope_base^(-2i/d_r), computed on the host in fp64
 };
 
+// Library-owned weights of the full-fold variant (x_q in, y out).
+struct FullWeights {
+  Shape shape;
+  mla_dtype dtype;
+  int device;
+  float* w_qf;       // [d_model][n_h*R]: per head [W_abs[h] | W_qr[h]] (fp32)
+  float* w_vo;       // [n_h*d_c][d_model]: row h*d_c + c of W_uv[h] W_o[h] (fp32)
+  double* inv_freq;  // [d_r/2] rope_base^(-2i/d_r), computed on the host in fp64
+};
+
+// Split of K across CTAs for one x W product: S splits of k_split each.
+struct XwPlan {
+  int S, k_split;
+};
+
 // ---------------------------------------------------------------- launchers
 // Each returns the cudaError_t of its launch.
 cudaError_t launch_pack_weights(const Shape& s, mla_dtype dt, const void* W_dkv, const void* W_kr,
@@ -114,6 +129,28 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
 cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
                            const WsView& ws, float* out, cudaStream_t st);
+
+// Full-fold variant. launch_fold_full builds FullWeights' matrices from the
+// caller's W_q, W_uk, W_uv and W_o (all in dt). launch_xw computes
+// out[M][N] = A[M][K] W[K][N] (A in a_dt, W and out fp32) with the split-K
+// plan from xw_plan; part holds xw_part_floats() floats of split partials.
+// launch_q_finish turns the fp32 query projection [B*n_q][n_h*R] into the
+// workspace's qabs (RoPE on the rotary block, times out_scale, rounded to
+// dt) and writes the split-KV plan. launch_combine_latent merges the splits
+// into o_lat [B*n_q][n_h*d_c] fp32 without the W_uv up-projection.
+cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, const void* W_uk,
+                             const void* W_uv, const void* W_o, FullWeights* w, int sms,
+                             cudaStream_t st);
+XwPlan xw_plan(int M, int K, int N, int sms);
+size_t xw_part_floats(int M, int N, const XwPlan& p);
+cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
+                      float* out, float* part, const XwPlan& p, cudaStream_t st);
+cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
+                            const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
+                            int n_q, const Partition& p, const WsView& ws, float out_scale,
+                            uint32_t* err, cudaStream_t st);
+cudaError_t launch_combine_latent(const Shape& s, int B, int n_q, const Partition& p,
+                                  const WsView& ws, float* olat, cudaStream_t st);
 
 // Partition parameters for each attention kernel.
 // tc_pairs: CTA pairs resident at once for the tensor-core attention kernel.

@@ -79,6 +79,19 @@ def test_null_and_count_checks(lib):
                           0, None) == 1
     assert lib.mla_weights_free(None) == 0
     assert lib.mla_decode_impl(ctypes.byref(cfg), None) == 1
+    # the full-fold calls check their arguments the same way
+    assert lib.mla_fold_full(ctypes.byref(cfg), None, None, None, None, None,
+                             ctypes.byref(h)) == 1
+    assert lib.mla_fold_full(ctypes.byref(cfg), None, None, None, None, None, None) == 1
+    bad = good_cfg()
+    bad.d_c = 3
+    assert lib.mla_fold_full(ctypes.byref(bad), None, None, None, None, None,
+                             ctypes.byref(h)) == 2
+    assert lib.mla_full_weights_free(None) == 0
+    assert lib.mla_decode_full_workspace_size(ctypes.byref(cfg), 0, 1, ctypes.byref(n)) == 2
+    assert lib.mla_decode_full_workspace_size(ctypes.byref(cfg), 4, 1, None) == 1
+    assert lib.mla_decode_full(ctypes.byref(cfg), None, None, None, 1, None, 1, None, 1, 1, None,
+                               None, 0, None) == 1
     assert lib.mla_get_last_device_error(None, None) == 1
 
 
@@ -92,3 +105,4 @@ def test_no_gpu_means_a_loud_cuda_error(lib):
     assert lib.mla_decode_workspace_size(ctypes.byref(cfg), 4, 1, 0, ctypes.byref(n)) == 6
     v = ctypes.c_int32()
     assert lib.mla_decode_impl(ctypes.byref(cfg), ctypes.byref(v)) == 6
+    assert lib.mla_decode_full_workspace_size(ctypes.byref(cfg), 4, 1, ctypes.byref(n)) == 6
