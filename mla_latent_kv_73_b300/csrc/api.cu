@@ -586,7 +586,7 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   const int M = B * n_q;
   // 1. x_q [W_abs[h] | W_qr[h]] for every head, then RoPE, scale, rounding and the plan
   cudaError_t e = launch_xw(cfg->dtype, x_q, M, p.s.d_model, fw->w.w_qf, p.s.n_h * p.s.R(), proj,
-                            part, fx.q, stream);
+                            part, fx.q, di->err, stream);
   const float out_scale =
       p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (e == cudaSuccess)
@@ -606,7 +606,7 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   // 4. y = sum_h o_lat[h] W_vo[h]
   if (e == cudaSuccess)
     e = launch_xw(MLA_F32, proj, M, p.s.n_h * p.s.d_c, fw->w.w_vo, p.s.d_model, y, part, fx.o,
-                  stream);
+                  di->err, stream);
   return from_cuda(e);
 }
 

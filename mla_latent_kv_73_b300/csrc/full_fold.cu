@@ -32,9 +32,12 @@
 // a fixed order by a second kernel, so results are deterministic.
 #include "device_common.cuh"
 #include "plan.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 namespace {
+
+using namespace mla_ptx;
 
 constexpr int XW_THREADS = 256;
 constexpr int XW_VEC = 4;                      // output columns per thread
@@ -43,6 +46,22 @@ constexpr int XW_ROWS = 16;                    // rows of A (query tokens) per C
 constexpr int XW_KC = 64;                      // K chunk staged in shared memory
 constexpr int QF_THREADS = 256;
 constexpr int FOLD_THREADS = 256;
+
+// TMA-ring form of the x W product (W rows 16-byte aligned: N % 4 == 0).
+constexpr int XR_CONSUMERS = 256;               // 8 warps, 4 columns per thread
+constexpr int XR_THREADS = XR_CONSUMERS + 32;   // + one producer warp
+constexpr int XR_COLS = 4 * XR_CONSUMERS;       // output columns per CTA
+constexpr int XR_RS = 8;                        // W rows per ring stage
+constexpr int XR_NST = 3;                       // ring stages
+constexpr int XR_KA = 192;                      // rows of A^T staged at a time (multiple of XR_RS)
+constexpr long long XR_WAIT = 2000000000LL;     // about 1 s at 2 GHz
+static_assert(XR_KA % XR_RS == 0, "a stage never straddles two A chunks");
+
+struct XrSmem {
+  float w[XR_NST][XR_RS][XR_COLS];  // 96 KB ring of W row segments
+  float a[XR_KA][XW_ROWS];          // A^T chunk, row index fastest
+  uint64_t full[XR_NST], empty[XR_NST];
+};
 
 // out[z][m][n] = sum over k in split z of A[m][k] W[k][n], fp32 accumulation
 // in k order. W is fp32 row-major [K][N]; A is [M][K] in TA.
@@ -112,6 +131,137 @@ xw_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, i
 #pragma unroll
       for (int j = 0; j < XW_VEC; ++j)
         if (n0 + j < N) orow[j] = acc[t][j];
+    }
+  }
+}
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(XR_CONSUMERS) : "memory");
+}
+
+// The same product as xw_kernel, with W streamed by the bulk-copy engine.
+// One producer thread copies, per stage, XR_RS rows of the CTA's 4 KB W
+// segment into a 3-stage shared-memory ring; two CTAs per SM keep up to
+// 192 KB of W in flight per SM without holding it in registers. The 256
+// consumer threads read their 16 bytes of each row from shared memory and
+// the 16 A values as four broadcast reads, and accumulate pairs of rows with
+// the packed fp32x2 FMA (one IEEE fma per lane, so the sums are those of
+// fmaf in the same order). Every wait is bounded: a timeout sets
+// MLA_DEVERR_TIMEOUT, the consumers stop waiting, and the producer waits
+// (bounded) for the copies it issued before the CTA exits.
+template <typename TA>
+__global__ void __launch_bounds__(XR_THREADS, 2)
+xw_ring_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, int N,
+               int k_split, float* __restrict__ out, uint32_t* err) {
+  extern __shared__ uint8_t xr_raw[];
+  XrSmem& sm = *reinterpret_cast<XrSmem*>((reinterpret_cast<uintptr_t>(xr_raw) + 127) &
+                                          ~static_cast<uintptr_t>(127));
+  const int c0 = blockIdx.x * XR_COLS;
+  const int m0 = blockIdx.y * XW_ROWS, mt = min(XW_ROWS, M - m0);
+  const int kb = blockIdx.z * k_split, ke = min(K, kb + k_split);
+  const int n_it = ke > kb ? (ke - kb + XR_RS - 1) / XR_RS : 0;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < XR_NST; ++st) {
+      mbar_init(&sm.full[st], 1);
+      mbar_init(&sm.empty[st], XR_CONSUMERS / 32);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  if (warp == XR_CONSUMERS / 32) {  // producer
+    if (lane != 0) return;
+    const uint32_t seg = static_cast<uint32_t>(min(XR_COLS, N - c0)) * 4u;
+    int it = 0;
+    for (; it < n_it; ++it) {
+      const int st = it % XR_NST;
+      if (it >= XR_NST && !mbar_wait(&sm.empty[st], ((it / XR_NST) - 1) & 1, XR_WAIT)) {
+        set_error(err, MLA_DEVERR_TIMEOUT);
+        break;
+      }
+      const int k = kb + it * XR_RS, rows = min(XR_RS, ke - k);
+      mbar_arrive_expect_tx(&sm.full[st], static_cast<uint32_t>(rows) * seg);
+      for (int r = 0; r < rows; ++r)
+        bulk_load(sm.w[st][r], W + static_cast<size_t>(k + r) * N + c0, seg, &sm.full[st]);
+    }
+    // the copies issued last land before this thread (and so the CTA) exits
+    for (int j = it > XR_NST ? it - XR_NST : 0; j < it; ++j)
+      mbar_wait(&sm.full[j % XR_NST], (j / XR_NST) & 1, XR_WAIT);
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  const int n0 = c0 + 4 * tid;
+  const bool live = n0 < N;  // N % 4 == 0: all four columns are in range
+  float2 acc[XW_ROWS / 2][4];  // acc[p][j]: rows 2p and 2p+1 of column n0 + j
+#pragma unroll
+  for (int p = 0; p < XW_ROWS / 2; ++p)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[p][j] = make_float2(0.f, 0.f);
+  bool ok = true;
+  int a_base = kb - XR_KA;
+  for (int it = 0; it < n_it; ++it) {
+    const int k = kb + it * XR_RS;
+    if (k >= a_base + XR_KA) {  // the same decision in every consumer
+      a_base = k;
+      consumer_bar();  // the previous chunk is consumed
+      const int ka = min(XR_KA, ke - k);
+      for (int i = tid; i < XR_KA * XW_ROWS; i += XR_CONSUMERS) {
+        const int t = i / XR_KA, kk = i % XR_KA;
+        sm.a[kk][t] = (t < mt && kk < ka)
+                          ? to_f32<TA>(A[static_cast<size_t>(m0 + t) * K + k + kk])
+                          : 0.f;
+      }
+      consumer_bar();
+    }
+    const int st = it % XR_NST;
+    if (ok) ok = mbar_wait(&sm.full[st], (it / XR_NST) & 1, XR_WAIT);
+    const int rows = min(XR_RS, ke - k);
+    if (live) {
+#pragma unroll
+      for (int r = 0; r < XR_RS; ++r) {
+        if (r < rows) {
+          const float4 w = *reinterpret_cast<const float4*>(&sm.w[st][r][4 * tid]);
+          const float2 w0 = make_float2(w.x, w.x), w1 = make_float2(w.y, w.y);
+          const float2 w2 = make_float2(w.z, w.z), w3 = make_float2(w.w, w.w);
+          const float4* av = reinterpret_cast<const float4*>(sm.a[k - a_base + r]);
+#pragma unroll
+          for (int u = 0; u < XW_ROWS / 4; ++u) {
+            const float4 a = av[u];
+            const float2 lo = make_float2(a.x, a.y), hi = make_float2(a.z, a.w);
+            acc[2 * u][0] = __ffma2_rn(lo, w0, acc[2 * u][0]);
+            acc[2 * u][1] = __ffma2_rn(lo, w1, acc[2 * u][1]);
+            acc[2 * u][2] = __ffma2_rn(lo, w2, acc[2 * u][2]);
+            acc[2 * u][3] = __ffma2_rn(lo, w3, acc[2 * u][3]);
+            acc[2 * u + 1][0] = __ffma2_rn(hi, w0, acc[2 * u + 1][0]);
+            acc[2 * u + 1][1] = __ffma2_rn(hi, w1, acc[2 * u + 1][1]);
+            acc[2 * u + 1][2] = __ffma2_rn(hi, w2, acc[2 * u + 1][2]);
+            acc[2 * u + 1][3] = __ffma2_rn(hi, w3, acc[2 * u + 1][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[st]);
+  }
+  if (!ok && lane == 0) set_error(err, MLA_DEVERR_TIMEOUT);
+  if (!live) return;
+  float* o = out + static_cast<size_t>(blockIdx.z) * M * N;
+  const bool vec_out = reinterpret_cast<uintptr_t>(out) % 16 == 0;
+#pragma unroll
+  for (int t = 0; t < XW_ROWS; ++t) {
+    if (t >= mt) break;
+    const int p = t / 2;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = (t & 1) ? acc[p][j].y : acc[p][j].x;
+    float* orow = o + static_cast<size_t>(m0 + t) * N + n0;
+    if (vec_out) {
+      *reinterpret_cast<float4*>(orow) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) orow[j] = v[j];
     }
   }
 }
@@ -241,17 +391,20 @@ cudaError_t q_finish_t(const Shape& s, const double* inv_freq, const float* qpre
 
 }  // namespace
 
+// K is split so that the grid fills the two CTAs per SM that the ring kernel
+// holds in one wave (tiles * S <= 2 * sms) without leaving most SMs idle:
+// S = floor(2 sms / tiles), at least 1, in whole stages of XR_RS rows.
 XwPlan xw_plan(int M, int K, int N, int sms) {
   XwPlan p;
   const long long tiles = static_cast<long long>((N + XW_COLS - 1) / XW_COLS) *
                           ((M + XW_ROWS - 1) / XW_ROWS);
-  const int chunks = (K + XW_KC - 1) / XW_KC;
-  long long S = (2LL * sms + tiles - 1) / tiles;
-  if (S > chunks) S = chunks;
+  const int stages = (K + XR_RS - 1) / XR_RS;
+  long long S = tiles > 0 ? (2LL * sms) / tiles : 1;
+  if (S > stages) S = stages;
   if (S < 1) S = 1;
   if (S > 65535) S = 65535;
-  const int per = (chunks + static_cast<int>(S) - 1) / static_cast<int>(S);
-  p.k_split = per * XW_KC;
+  const int per = (stages + static_cast<int>(S) - 1) / static_cast<int>(S);
+  p.k_split = per * XR_RS;
   p.S = (K + p.k_split - 1) / p.k_split;
   if (p.S < 1) p.S = 1;
   return p;
@@ -261,19 +414,41 @@ size_t xw_part_floats(int M, int N, const XwPlan& p) {
   return p.S > 1 ? static_cast<size_t>(p.S) * M * N : 0;
 }
 
+template <typename TA>
+cudaError_t xw_ring_t(const TA* A, int M, int K, const float* W, int N, int k_split, float* dst,
+                      uint32_t* err, dim3 grid, cudaStream_t st) {
+  const int smem = static_cast<int>(sizeof(XrSmem)) + 128;
+  cudaError_t e = cudaFuncSetAttribute(xw_ring_kernel<TA>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  xw_ring_kernel<TA><<<grid, XR_THREADS, smem, st>>>(A, M, K, W, N, k_split, dst, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
-                      float* out, float* part, const XwPlan& p, cudaStream_t st) {
+                      float* out, float* part, const XwPlan& p, uint32_t* err, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (M > 65535 * XW_ROWS) return cudaErrorInvalidValue;
+  static_assert(XR_COLS == XW_COLS, "both forms tile the columns alike");
   dim3 grid((N + XW_COLS - 1) / XW_COLS, (M + XW_ROWS - 1) / XW_ROWS, p.S);
   float* dst = p.S > 1 ? part : out;
-  if (a_dt == MLA_F32)
+  // the bulk copies need 16-byte aligned W rows
+  const bool ring = N % 4 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0;
+  cudaError_t e;
+  if (ring && a_dt == MLA_F32)
+    e = xw_ring_t<float>(static_cast<const float*>(A), M, K, W, N, p.k_split, dst, err, grid, st);
+  else if (ring)
+    e = xw_ring_t<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(A), M, K, W, N, p.k_split,
+                                 dst, err, grid, st);
+  else if (a_dt == MLA_F32) {
     xw_kernel<float><<<grid, XW_THREADS, 0, st>>>(static_cast<const float*>(A), M, K, W, N,
                                                   p.k_split, dst);
-  else
+    e = cudaGetLastError();
+  } else {
     xw_kernel<__nv_bfloat16><<<grid, XW_THREADS, 0, st>>>(
         static_cast<const __nv_bfloat16*>(A), M, K, W, N, p.k_split, dst);
-  cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || p.S == 1) return e;
   const size_t n = static_cast<size_t>(M) * N;
   const size_t blocks = (n + 255) / 256;

@@ -144,7 +144,7 @@ cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, cons
 XwPlan xw_plan(int M, int K, int N, int sms);
 size_t xw_part_floats(int M, int N, const XwPlan& p);
 cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
-                      float* out, float* part, const XwPlan& p, cudaStream_t st);
+                      float* out, float* part, const XwPlan& p, uint32_t* err, cudaStream_t st);
 cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,

@@ -142,3 +142,12 @@ def test_full_fold_deterministic_and_checks_workspace():
         _lib.mla_decode_full(r.cfg, r.fw, r.x, r.cache, r.pt, r.sl, r.y, small)
     assert e.value.status == 5  # MLA_ERR_WORKSPACE
     r.free()
+
+
+def test_full_fold_rows_not_16_byte_aligned():
+    """n_h*(d_c + d_r) = 114 and d_model = 70 are not multiples of 4 floats, so
+    the bulk-copy ring cannot take the folded rows; the register form runs."""
+    w, lens = workload(3, 70, 32, 6, 16, 16, (5, 77, 130), 2, "f32", seed=26)
+    r = FullRun(w, lens)
+    check("f32", r.decode(), r.oracle(), "unaligned rows")
+    r.free()
