@@ -27,7 +27,8 @@ constexpr int CB_TOK = 16, CB_THREADS = 256;
 
 // Dynamic shared memory: o_lat [d_c][CB_TOK] (token fastest), then the
 // partial outputs of the two d_c halves [2][CB_TOK][d_v], then the range
-// table rb[0..C] of the attention partition.
+// table rb[0..C] of the attention partition, then the merge weights
+// [CB_TOK][C + 1].
 template <typename T>
 __global__ void __launch_bounds__(CB_THREADS)
 combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ tiles,
@@ -39,64 +40,102 @@ combine_kernel(Shape s, const T* __restrict__ w_uv, const int32_t* __restrict__ 
   float* olat = sm;                                   // [d_c][CB_TOK]
   float* half_out = olat + s.d_c * CB_TOK;            // [2][CB_TOK][d_v]
   long long* rb = reinterpret_cast<long long*>(half_out + 2 * CB_TOK * s.d_v);  // [C+1]
+  float* wts = reinterpret_cast<float*>(rb + p.C + 1);  // [CB_TOK][C+1]
   __shared__ int c_lo[CB_TOK], c_hi[CB_TOK], row_off[CB_TOK];
-  __shared__ float m_max[CB_TOK], inv_den[CB_TOK];
   const int h = blockIdx.x, tok0 = blockIdx.y * CB_TOK;
   const int Tq = B * n_q, ntok = min(CB_TOK, Tq - tok0);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // 1. per token: the ranges holding its pieces and their merge weights
+  //    exp(lse_s - lse). The plan loads of all tokens go out together; then
+  //    half a warp per token, its lanes taking the pieces, loads the lse
+  //    values.
   const long long T_all = prefix[B];
-  const long long N = T_all * p.G;
-
-  for (int c = threadIdx.x; c <= p.C; c += CB_THREADS) rb[c] = N > 0 ? bounds[c] : 0;
-  __syncthreads();
-
-  // 1. per token: the CTAs holding its pieces, the max lse and the normaliser
+  for (int c = threadIdx.x; c <= p.C; c += CB_THREADS) rb[c] = bounds[c];  // all 0 without tiles
+  int my_tiles = 0, my_off = 0;
+  long long my_first = 0;
+  if (threadIdx.x < ntok) {
+    const int tok = tok0 + threadIdx.x, b = tok / n_q, qi = tok % n_q;
+    const int r = qi * s.n_h + h, g = r / p.RG, rr = r % p.RG;
+    my_off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
+    my_tiles = tiles[b];
+    my_first = static_cast<long long>(g) * T_all + prefix[b];
+  }
+  __syncthreads();  // range starts in place
   if (threadIdx.x < CB_TOK) {
-    const int t = threadIdx.x;
-    int c0 = 0, c1 = -1, off = 0;
-    float M = -INFINITY, den = 0.f;
-    if (t < ntok) {
-      const int tok = tok0 + t, b = tok / n_q, qi = tok % n_q;
-      const int r = qi * s.n_h + h, g = r / p.RG, rr = r % p.RG;
-      off = (g * B + b) * p.RG + rr;  // row of slot (c + g*B + b) is c*RG + off
-      if (tiles[b] > 0) {
-        const long long first = g * T_all + prefix[b], last = first + tiles[b] - 1;
-        c0 = range_of_item(rb, p.C, first);
-        c1 = range_of_item(rb, p.C, last);
-        for (int c = c0; c <= c1; ++c)
-          if (rb[c] != rb[c + 1]) M = fmaxf(M, part_lse[static_cast<size_t>(c) * p.RG + off]);
-        if (M != -INFINITY)
-          for (int c = c0; c <= c1; ++c)
-            if (rb[c] != rb[c + 1]) den += expf(part_lse[static_cast<size_t>(c) * p.RG + off] - M);
-      }
+    int c0 = 0, c1 = -1;
+    if (my_tiles > 0) {
+      c0 = range_of_item(rb, p.C, my_first);
+      c1 = range_of_item(rb, p.C, my_first + my_tiles - 1);
     }
-    c_lo[t] = c0;
-    c_hi[t] = (M == -INFINITY) ? -1 : c1;
-    row_off[t] = off;
-    m_max[t] = M;
-    inv_den[t] = den > 0.f ? 1.f / den : 0.f;
+    c_lo[threadIdx.x] = c0;
+    c_hi[threadIdx.x] = c1;
+    row_off[threadIdx.x] = my_off;
+  }
+  __syncthreads();
+  for (int tb = 0; tb < ntok; tb += 2 * (CB_THREADS / 32)) {
+    const int t = tb + 2 * warp + (lane >> 4), hl = lane & 15;
+    const bool live = t < ntok;
+    const int c0 = live ? c_lo[t] : 0, c1 = live ? c_hi[t] : -1;
+    const int off = live ? row_off[t] : 0;
+    float M = -INFINITY;
+    for (int c = c0 + hl; c <= c1; c += 16) {
+      const float x = rb[c] != rb[c + 1] ? part_lse[static_cast<size_t>(c) * p.RG + off] : -INFINITY;
+      wts[t * (p.C + 1) + (c - c0)] = x;
+      M = fmaxf(M, x);
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float den = 0.f;
+    for (int c = c0 + hl; c <= c1; c += 16) {
+      const float e = M == -INFINITY ? 0.f : expf(wts[t * (p.C + 1) + (c - c0)] - M);
+      wts[t * (p.C + 1) + (c - c0)] = e;
+      den += e;
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = c0 + hl; c <= c1; c += 16) wts[t * (p.C + 1) + (c - c0)] *= inv;
+    if (live && hl == 0 && M == -INFINITY) c_hi[t] = -1;  // no piece holds a visible token
   }
   __syncthreads();
 
-  // 2. o_lat = weighted sum of the normalised partials (coalesced over d_c)
-  for (int t = 0; t < CB_TOK; ++t) {
-    for (int dc = threadIdx.x; dc < s.d_c; dc += CB_THREADS) {
-      float acc = 0.f;
-      for (int c = c_lo[t]; c <= c_hi[t]; ++c) {
-        if (rb[c] == rb[c + 1]) continue;
-        const size_t row = static_cast<size_t>(c) * p.RG + row_off[t];
-        acc = fmaf(expf(part_lse[row] - m_max[t]) * inv_den[t], part_o[row * s.d_c + dc], acc);
+  // 2. o_lat = weighted sum of the normalised partials. A thread owns four
+  //    latent dims (one 16-byte load per piece) of several tokens; pieces of
+  //    empty ranges carry weight 0 and are not read.
+  const int d4 = s.d_c / 4;  // d_c % 4 == 0
+  for (int i = threadIdx.x; i < CB_TOK * d4; i += CB_THREADS) {
+    const int t = i / d4, dc = 4 * (i % d4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < ntok) {
+      const int c0 = c_lo[t], c1 = c_hi[t];
+      const float* w = wts + t * (p.C + 1) - c0;
+#pragma unroll 4
+      for (int c = c0; c <= c1; ++c) {
+        const float wc = w[c];
+        if (wc == 0.f) continue;
+        const float4 v = *reinterpret_cast<const float4*>(
+            part_o + (static_cast<size_t>(c) * p.RG + row_off[t]) * s.d_c + dc);
+        acc.x = fmaf(wc, v.x, acc.x);
+        acc.y = fmaf(wc, v.y, acc.y);
+        acc.z = fmaf(wc, v.z, acc.z);
+        acc.w = fmaf(wc, v.w, acc.w);
       }
-      olat[dc * CB_TOK + t] = acc;
+      if (olat_out) {  // latent mode: o_lat [B*n_q][n_h*d_c], no up-projection
+        *reinterpret_cast<float4*>(olat_out + (static_cast<size_t>(tok0 + t) * s.n_h + h) * s.d_c +
+                                   dc) = acc;
+        continue;
+      }
+    }
+    if (!olat_out) {
+      olat[(dc + 0) * CB_TOK + t] = acc.x;
+      olat[(dc + 1) * CB_TOK + t] = acc.y;
+      olat[(dc + 2) * CB_TOK + t] = acc.z;
+      olat[(dc + 3) * CB_TOK + t] = acc.w;
     }
   }
+  if (olat_out) return;
   __syncthreads();
-  if (olat_out) {  // latent mode: o_lat [B*n_q][n_h*d_c], no up-projection
-    for (int i = threadIdx.x; i < ntok * s.d_c; i += CB_THREADS) {
-      const int t = i / s.d_c, dc = i % s.d_c;
-      olat_out[(static_cast<size_t>(tok0 + t) * s.n_h + h) * s.d_c + dc] = olat[dc * CB_TOK + t];
-    }
-    return;
-  }
 
   // 3. out = o_lat W_uv[h]: W_uv is packed [h][d_v][d_c]. A thread owns one
   // output column for all 16 tokens and half of the d_c reduction.
@@ -153,7 +192,7 @@ cudaError_t combine_t(const Shape& s, const T* w_uv, int B, int n_q, const Parti
   const int Tq = B * n_q;
   dim3 grid(s.n_h, (Tq + CB_TOK - 1) / CB_TOK);
   const size_t smem = sizeof(float) * (CB_TOK * s.d_c + 2 * CB_TOK * s.d_v) +
-                      sizeof(long long) * (p.C + 1);
+                      sizeof(long long) * (p.C + 1) + sizeof(float) * CB_TOK * (p.C + 1);
   auto kern = combine_kernel<T>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

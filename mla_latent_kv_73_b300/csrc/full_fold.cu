@@ -278,7 +278,11 @@ sum_splits_kernel(const float* __restrict__ part, int S, size_t n, float* __rest
 }
 
 // qabs[t, h] = out_scale * [q_lat | RoPE(q_rope, pos_t)] in T, from the fp32
-// projection qpre[t][h*R + n]. Block 0 also writes the split-KV plan.
+// projection qpre[t][h*R + n]. One block per (token, QF_HEADS heads), so
+// that each thread has only a few elements and the grid covers the SMs.
+// Block 0 also writes the split-KV plan.
+constexpr int QF_HEADS = 2;
+
 template <typename T>
 __global__ void __launch_bounds__(QF_THREADS)
 q_finish_kernel(Shape s, const float* __restrict__ qpre, const double* __restrict__ inv_freq,
@@ -288,12 +292,15 @@ q_finish_kernel(Shape s, const float* __restrict__ qpre, const double* __restric
   if (blockIdx.x == 0)
     write_plan<QF_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
                            first_b, err);
-  const int tok = blockIdx.x, b = tok / n_q, qi = tok % n_q;
+  const int hg_n = (s.n_h + QF_HEADS - 1) / QF_HEADS;
+  const int tok = blockIdx.x / hg_n, h0 = (blockIdx.x % hg_n) * QF_HEADS;
+  const int nh = min(QF_HEADS, s.n_h - h0);
+  const int b = tok / n_q, qi = tok % n_q;
   const int R = s.R(), half = s.d_r / 2, per_head = s.d_c + half;
   const int pos = seq_lens[b] - n_q + qi;
-  const float* src = qpre + static_cast<size_t>(tok) * s.n_h * R;
-  T* dst = qabs + static_cast<size_t>(tok) * s.n_h * R;
-  for (int i = threadIdx.x; i < s.n_h * per_head; i += QF_THREADS) {
+  const float* src = qpre + (static_cast<size_t>(tok) * s.n_h + h0) * R;
+  T* dst = qabs + (static_cast<size_t>(tok) * s.n_h + h0) * R;
+  for (int i = threadIdx.x; i < nh * per_head; i += QF_THREADS) {
     const int h = i / per_head, n = i % per_head;
     const float* sh = src + static_cast<size_t>(h) * R;
     T* dh = dst + static_cast<size_t>(h) * R;
@@ -383,7 +390,10 @@ template <typename T>
 cudaError_t q_finish_t(const Shape& s, const double* inv_freq, const float* qpre,
                        const int32_t* seq_lens, int max_blocks, int B, int n_q, const Partition& p,
                        const WsView& ws, float out_scale, uint32_t* err, cudaStream_t st) {
-  q_finish_kernel<T><<<B * n_q, QF_THREADS, 0, st>>>(
+  const long long blocks =
+      static_cast<long long>(B) * n_q * ((s.n_h + QF_HEADS - 1) / QF_HEADS);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  q_finish_kernel<T><<<static_cast<unsigned>(blocks), QF_THREADS, 0, st>>>(
       s, qpre, inv_freq, seq_lens, B, n_q, max_blocks, p.TS, p.G, p.C, p.K, out_scale,
       static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, ws.bounds, ws.first_b, err);
   return cudaGetLastError();
