@@ -103,6 +103,9 @@ typedef struct {
   mla_dtype dtype;        /* dtype of cache, weights, x and q; outputs are fp32 */
   int32_t impl;           /* an mla_impl value */
 } mla_config;
+/* Supported shapes: n_h, d_model, d_nope, d_v, block_size >= 1; d_c a multiple
+ * of 4 in [4, 512]; d_r even and >= 2; d_c + d_r <= 1024; d_nope <= 1024;
+ * d_v <= 1024. Any other shape returns MLA_ERR_SHAPE before device work. */
 
 typedef struct mla_weights_s* mla_weights; /* opaque, library-owned */
 

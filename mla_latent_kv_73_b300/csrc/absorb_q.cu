@@ -123,7 +123,13 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
                        float out_scale, uint32_t* err, cudaStream_t st) {
   const int Tq = B * n_q;
   dim3 grid(s.n_h, (Tq + AQ_TOK - 1) / AQ_TOK);
-  const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;
+  const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;  // up to 64 KB (d_nope <= 1024)
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(absorb_q_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
   absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
       s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
       max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix,

@@ -66,7 +66,10 @@ mla_status check_config(const mla_config* c) {
     return MLA_ERR_SHAPE;
   if (c->d_c < 4 || c->d_c > 512 || c->d_c % 4 != 0) return MLA_ERR_SHAPE;
   if (c->d_r < 2 || c->d_r % 2 != 0 || c->d_c + c->d_r > 1024) return MLA_ERR_SHAPE;
-  if (c->d_nope > 1024 || c->d_v > 4096) return MLA_ERR_SHAPE;
+  // d_v: the CUDA-core combine keeps [2][16][d_v] fp32 partial outputs in
+  // shared memory beside o_lat and the merge weights (about 191 KB at
+  // d_c = 512, d_v = 1024 on 148 SMs, under the 227 KB a block may use).
+  if (c->d_nope > 1024 || c->d_v > 1024) return MLA_ERR_SHAPE;
   return MLA_OK;
 }
 

@@ -49,6 +49,7 @@ def good_cfg(**kw):
 
 @pytest.mark.parametrize("field,value,status", [
     ("d_r", 3, 2), ("d_r", 0, 2), ("d_c", 513, 2), ("d_c", 1024, 2), ("n_h", 0, 2),
+    ("d_v", 1025, 2), ("d_nope", 1025, 2),
     ("block_size", 0, 2), ("dtype", 7, 1), ("impl", 5, 1), ("rope_base", 0.0, 1),
     ("softmax_scale", -1.0, 1),
 ])

@@ -237,6 +237,16 @@ def test_decode_small_fp32_shapes():
     r.dw.free()
 
 
+def test_decode_widest_heads_fp32():
+    """d_nope = 800 (the query absorption stages 51 KB of queries in shared
+    memory) and d_v = 1024, the widest head the config accepts."""
+    w, lens = small_workload(n_h=2, d_model=32, d_c=32, d_r=8, d_nope=800, d_v=1024,
+                             lens=(3, 70), n_q=1, dtype="f32")
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO)
+    check_f32(r.decode(), r.oracle(), "widest heads fp32")
+    r.dw.free()
+
+
 def test_kernels_agree_and_steps_equal_fused():
     w, lens = small_workload(lens=(5, 128, 129, 700), n_q=2, seed=3)
     a = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
