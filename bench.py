@@ -92,6 +92,13 @@ def barrier(dist):
         dist.barrier()
 
 
+def whole_job_rate(units, ms, dist, device="cpu"):
+    """(units of all ranks per second over the slowest rank's time, that time
+    in ms). Every rank gets the same pair."""
+    ms_max = max_over_ranks(ms, dist, device)
+    return sum_over_ranks(units, dist, device) / (ms_max / 1e3), ms_max
+
+
 # ---------------------------------------------------------------------------
 # accounting
 # ---------------------------------------------------------------------------
@@ -329,10 +336,8 @@ def run_ours(args, world, rank, local):
     st, code = _lib.mla_get_last_device_error(stream)
     if code:
         raise RuntimeError(f"device error word {code:#x} in the timed region")
-    total_ms_max = max_over_ranks(total_ms, dist, "cuda")
+    value, total_ms_max = whole_job_rate(Tq * K, total_ms, dist, "cuda")
     ms_per_step = total_ms_max / K
-    tokens = sum_over_ranks(Tq * K, dist, "cuda")
-    value = tokens / (total_ms_max / 1e3)
 
     # the attention kernel, launch by launch (each launch on a cold input set)
     Ka = min(K, 2000)
