@@ -456,3 +456,18 @@ def layer_output_absorbed(x_q, seq_rows, seq_lens, W_q, W_uk, W_uv, W_o, d_c, d_
     for (b, i), v in res.items():
         out[b, i] = v
     return out
+
+
+def layer_step_materialised(q, seq_rows, seq_lens, W_uk, W_uv, W_o, d_c, d_nope, d_v, scale,
+                            base):
+    """One layer's decode step from the projected queries: every head's
+    materialised attention (:func:`decode_materialised`), the heads
+    concatenated, then the output projection y = concat_h(o_h) W_o.
+
+    q: [B, n_q, n_h, d_nope + d_r] before RoPE. W_o: [n_h*d_v, d_model] (the
+    reading of :func:`layer_output_materialised`). Returns y [B, n_q, d_model].
+    The query projection stays with the caller, as for the decode step.
+    """
+    o = decode_materialised(q, seq_rows, seq_lens, W_uk, W_uv, d_c, d_nope, d_v, scale, base)
+    B, n_q, n_h, _ = o.shape
+    return o.reshape(B, n_q, n_h * d_v) @ np.asarray(W_o, dtype=np.float64)

@@ -558,6 +558,37 @@ def test_layer_output_absorbing_the_wrong_matrix():
     assert bad.shape == good.shape and np.max(np.abs(bad - good)) > 1e-3
 
 
+def test_layer_step_under_permutation_output_weights():
+    """With W_o a permutation, the step's output is the per-head outputs
+    (pinned above) moved by index: y[perm[j]] = concat_h(o_h)[j]."""
+    t = _layer(seed=14)
+    n_h, d_v = t["n_h"], t["d_v"]
+    D = n_h * d_v
+    g = np.random.default_rng(15)
+    perm = g.permutation(D)
+    P = np.zeros((D, D))
+    P[np.arange(D), perm] = 1.0
+    q = g.normal(size=(len(t["lens"]), 2, n_h, t["d_nope"] + t["d_r"]))
+    o = O.decode_materialised(q, t["rows"], t["lens"], t["W_uk"], t["W_uv"], t["d_c"],
+                              t["d_nope"], d_v, t["scale"], 1e4)
+    want = np.empty((len(t["lens"]), 2, D))
+    want[..., perm] = o.reshape(len(t["lens"]), 2, D)
+    got = O.layer_step_materialised(q, t["rows"], t["lens"], t["W_uk"], t["W_uv"], P, t["d_c"],
+                                    t["d_nope"], d_v, t["scale"], 1e4)
+    assert np.max(np.abs(got - want)) <= 1e-12
+
+
+def test_layer_step_equals_layer_from_hidden_state():
+    """Fed q = x_q W_q, the step gives the layer output from x_q."""
+    t = _layer(seed=16)
+    B, n_q = t["x_q"].shape[:2]
+    q = (t["x_q"] @ t["W_q"]).reshape(B, n_q, t["n_h"], t["d_nope"] + t["d_r"])
+    a = O.layer_step_materialised(q, t["rows"], t["lens"], t["W_uk"], t["W_uv"], t["W_o"],
+                                  t["d_c"], t["d_nope"], t["d_v"], t["scale"], 1e4)
+    b = O.layer_output_materialised(*_layer_args(t))
+    assert np.max(np.abs(a - b)) <= 1e-12
+
+
 def _layer_mutants():
     def rope_block_first(W_q, h, d_nope, d_r):
         W_q = np.asarray(W_q, dtype=np.float64)
