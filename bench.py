@@ -45,8 +45,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-heads", type=int, default=0,
                     help="(b, h) pairs in the oracle sample (0: about 10 s worth)")
-    ap.add_argument("--variant", choices=["per_head", "full_fold"], default="per_head",
-                    help="full_fold: time the folded layer (x_q in, y out) instead")
+    ap.add_argument("--variant", choices=["per_head", "full_fold", "layer"], default="per_head",
+                    help="full_fold: time the folded layer (x_q in, y out); layer: time "
+                         "append + decode + W_o (mla_decode_layer)")
     return ap.parse_args()
 
 
@@ -651,6 +652,136 @@ def run_full_fold(args, world, rank, local):
         dist.destroy_process_group()
 
 
+def run_layer_step(args, world, rank, local):
+    """One layer's decode step (mla_decode_layer: append, decode, W_o
+    projection) as a per-layer latency, beside the per-head step (append +
+    decode) on the same inputs. Every stage streams from HBM; the roofline is
+    the call's algorithmic bytes over its time. W_o (168 MB at DeepSeek-V2
+    widths) is larger than L2, so the step's inputs do not stay in L2."""
+    import torch
+    from mla_latent_kv_73_b300 import _lib, synth
+    from mla_latent_kv_73_b300.device_inputs import DeviceWeights, config_for, to_device
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    _lib.load()
+    w = synth.WORKLOADS[args.workload]
+    lens = synth.seq_lens(w)
+    B, n_q = w.batch, w.n_q
+    Tq = B * n_q
+    cfg = config_for(w)
+    impl = _lib.mla_decode_impl(cfg)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pt_np, num_blocks = synth.page_table(w, lens)
+    cache_bytes, _ = algorithmic(w, lens)
+    wts = synth.weights(w)
+    dw = DeviceWeights(w, wts, cfg)
+    W_o = to_device(wts.raw["W_o"], w.dtype)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3000 + rank)
+    cache = torch.randn((num_blocks, w.block_size, w.R), generator=gen, device="cuda").to(dt)
+    pt = to_device(pt_np, "i32")
+    x = torch.randn((Tq, w.d_model), generator=gen, device="cuda").to(dt)
+    q = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen, device="cuda").to(dt)
+    seq_lens = to_device(lens, "i32")
+    seq_idx = to_device(np.repeat(np.arange(B), n_q).astype(np.int32), "i32")
+    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32), "i32")
+    out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
+    y = torch.empty((B, n_q, w.d_model), device="cuda")
+    ws_l = torch.empty(_lib.mla_decode_layer_workspace_size(cfg, B, n_q), dtype=torch.uint8,
+                       device="cuda")
+    ws_h = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q, int(lens.sum())),
+                       dtype=torch.uint8, device="cuda")
+
+    def layer(st):
+        _lib.mla_decode_layer(cfg, dw.handle, W_o, x, seq_idx, pos, q, cache, pt, seq_lens, out,
+                              y, ws_l, st)
+
+    def per_head(st):
+        _lib.mla_append_kv(cfg, dw.handle, x, seq_idx, pos, pt, cache, st)
+        _lib.mla_decode(cfg, dw.handle, q, cache, pt, seq_lens, out, ws_h, st)
+
+    stream = torch.cuda.current_stream()
+    graphs = {}
+    for name, fn in (("layer", layer), ("per_head", per_head)):
+        for _ in range(args.warmup):
+            fn(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        graphs[name] = g
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} after warm-up")
+    K = args.steps
+    times, clocks = {}, None
+    for name in ("per_head", "layer"):
+        for _ in range(3):
+            graphs[name].replay()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            barrier(dist)
+            torch.cuda.synchronize()
+            wall0 = time.time()
+            t0.record()
+            for _ in range(K):
+                graphs[name].replay()
+            t1.record()
+            torch.cuda.synchronize()
+            barrier(dist)
+            wall1 = time.time()
+        if name == "layer":
+            clocks = clk.summary(wall0, wall1)
+        times[name] = max_over_ranks(t0.elapsed_time(t1), dist, "cuda") / K
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+    ms = times["layer"]
+    eb = w.elem_bytes
+    weight_bytes = (w.R * w.d_model + 2 * w.n_h * w.d_c * w.d_nope
+                    + w.n_h * w.d_v * w.d_model) * eb
+    step_bytes = cache_bytes + weight_bytes
+    hbm, _, _, src = measured_peaks()
+    achieved = step_bytes / (ms / 1e3) / 1e9
+    value, _ = whole_job_rate(Tq, ms, dist, "cuda")
+    line = {
+        "metric": "per-layer decode latency (append + decode + W_o)",
+        "variant": "layer",
+        "value": round(1e3 * ms, 2),
+        "unit": "us per layer step",
+        "tokens_per_s": round(value, 1),
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) cache rows, hidden states and queries; "
+                "N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "batch": B, "n_q": n_q, "n_h": w.n_h,
+                   "d_model": w.d_model, "d_c": w.d_c, "d_r": w.d_r,
+                   "decode_kernel": "tensor_core" if impl == 2 else "cuda_core",
+                   "l2": f"one input set; W_o alone is {w.n_h * w.d_v * w.d_model * eb / 2**20:.0f}"
+                         f" MiB, above L2"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
+                     "kernel": "mla_decode_layer (all stages HBM-bound)",
+                     "bytes_per_step": step_bytes},
+        "per_head_step_us": round(1e3 * times["per_head"], 2),
+        "w_o_projection_us": round(1e3 * (ms - times["per_head"]), 2),
+        "clocks": clocks,
+    }
+    dw.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------------------
 # the oracle (CPU) arm
 # ---------------------------------------------------------------------------
@@ -744,6 +875,9 @@ def main():
         return
     if args.variant == "full_fold":
         run_full_fold(args, world, rank, local)
+        return
+    if args.variant == "layer":
+        run_layer_step(args, world, rank, local)
         return
     run_ours(args, world, rank, local)
 

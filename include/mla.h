@@ -39,7 +39,8 @@
  * the caller owns and keeps alive until the work queued on `stream` has
  * finished. The only exception is the out-parameters of the host-side query
  * functions (mla_decode_workspace_size, mla_decode_full_workspace_size,
- * mla_get_last_device_error), which are host pointers. All compute calls are
+ * mla_decode_layer_workspace_size, mla_get_last_device_error), which are
+ * host pointers. All compute calls are
  * asynchronous on `stream` and return once the work is queued. The library
  * allocates device memory only inside mla_absorb_weights and mla_fold_full.
  * It never allocates on the decode path.
@@ -291,6 +292,47 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
                            const void* cache, int32_t num_blocks, const int32_t* page_table,
                            int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
                            float* y, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * One layer's decode step: append, decode and the output projection.
+ *
+ * The per-head path leaves the output projection W_o with the caller. This
+ * call runs the whole step of one attention layer for the new tokens on
+ * `stream`: mla_append_kv of their hidden states, mla_decode of their
+ * queries, then y = concat_h(o_h) W_o. The kernels are chained with
+ * programmatic dependent launch: each one's constant-weight prologue overlaps
+ * the kernel before it, and the projection streams W_o while the combine
+ * still runs. Source for the projection's place in the layer: "Multi-head
+ * Latent Attention: the KV cache, compressed", section "What it costs, said
+ * plainly" (W_o [n_h*head_dim -> d_model] among the layer's weights).
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace that mla_decode_layer needs (the decode's plus
+ * the projection's split partials). Writes the size to *bytes (a host
+ * pointer). */
+mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                           size_t* bytes);
+
+/* One decode step of one layer for B sequences with n_q new tokens each.
+ *   W_o        [n_h*d_v, d_model] row-major, cfg->dtype, caller-owned; head
+ *              h's output meets rows [h*d_v, (h+1)*d_v)
+ *   x          [B*n_q, d_model] cfg->dtype: hidden states of the new tokens
+ *   seq_idx, pos [B*n_q] int32: their sequences and positions (as in
+ *              mla_append_kv; normally pos = seq_lens[b] - n_q + i)
+ *   q          [B, n_q, n_h, d_nope + d_r] cfg->dtype, RoPE not yet applied
+ *   cache      updated in place with the new rows, then read
+ *   out        [B, n_q, n_h, d_v] fp32: the per-head outputs (also returned)
+ *   y          [B, n_q, d_model] fp32: the layer output
+ *   workspace  at least mla_decode_layer_workspace_size() bytes, 256-byte
+ *              aligned
+ * The projection accumulates in fp32. Errors as in mla_append_kv and
+ * mla_decode. */
+mla_status mla_decode_layer(const mla_config* cfg, mla_weights w, const void* W_o, const void* x,
+                            const int32_t* seq_idx, const int32_t* pos, const void* q,
+                            void* cache, int32_t num_blocks, const int32_t* page_table,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                            float* out, float* y, void* workspace, size_t ws_bytes,
+                            cudaStream_t stream);
 
 /* Which decode kernel mla_decode would run for this config on the current
  * device. Writes an mla_impl value other than MLA_IMPL_AUTO to *impl, a host

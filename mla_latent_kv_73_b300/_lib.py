@@ -26,7 +26,7 @@ EXPORTS = ["mla_absorb_weights", "mla_weights_free", "mla_append_kv",
            "mla_decode_attend", "mla_decode_combine", "mla_decode_impl",
            "mla_get_last_device_error", "mla_status_string", "mla_decode_no_alloc",
            "mla_fold_full", "mla_full_weights_free", "mla_decode_full_workspace_size",
-           "mla_decode_full"]
+           "mla_decode_full", "mla_decode_layer_workspace_size", "mla_decode_layer"]
 MLA_NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -67,6 +67,9 @@ def _declare(lib):
         "mla_full_weights_free": [_P],
         "mla_decode_full_workspace_size": [cfgp, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
         "mla_decode_full": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
+        "mla_decode_layer_workspace_size": [cfgp, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
+        "mla_decode_layer": [cfgp, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P,
+                             ctypes.c_size_t, _P],
         "mla_get_last_device_error": [_P, ctypes.POINTER(ctypes.c_uint32)],
         "mla_status_string": [_I],
     }
@@ -221,6 +224,24 @@ def mla_decode_full(cfg, fw, x_q, cache, page_table, seq_lens, y, workspace, str
         ctypes.byref(cfg), fw, ptr(x_q), ptr(cache), cache.shape[0], ptr(page_table),
         page_table.shape[1], ptr(seq_lens), B, n_q, ptr(y), ptr(workspace),
         workspace.numel() * workspace.element_size(), stream_handle(stream)))
+
+
+def mla_decode_layer_workspace_size(cfg, B, n_q):
+    n = ctypes.c_size_t()
+    check("mla_decode_layer_workspace_size", load().mla_decode_layer_workspace_size(
+        ctypes.byref(cfg), B, n_q, ctypes.byref(n)))
+    return n.value
+
+
+def mla_decode_layer(cfg, w, W_o, x, seq_idx, pos, q, cache, page_table, seq_lens, out, y,
+                     workspace, stream=None):
+    """Append, decode and output projection of one layer (see include/mla.h)."""
+    B, n_q = q.shape[0], q.shape[1]
+    check("mla_decode_layer", load().mla_decode_layer(
+        ctypes.byref(cfg), w, ptr(W_o), ptr(x), ptr(seq_idx), ptr(pos), ptr(q), ptr(cache),
+        cache.shape[0], ptr(page_table), page_table.shape[1], ptr(seq_lens), B, n_q, ptr(out),
+        ptr(y), ptr(workspace), workspace.numel() * workspace.element_size(),
+        stream_handle(stream)))
 
 
 def mla_get_last_device_error(stream=None):

@@ -588,8 +588,8 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.lay.total + fx.proj);
   const int M = B * n_q;
   // 1. x_q [W_abs[h] | W_qr[h]] for every head, then RoPE, scale, rounding and the plan
-  cudaError_t e = launch_xw(cfg->dtype, x_q, M, p.s.d_model, fw->w.w_qf, p.s.n_h * p.s.R(), proj,
-                            part, fx.q, di->err, stream);
+  cudaError_t e = launch_xw(cfg->dtype, x_q, M, p.s.d_model, MLA_F32, fw->w.w_qf,
+                            p.s.n_h * p.s.R(), proj, part, fx.q, di->err, false, stream);
   const float out_scale =
       p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (e == cudaSuccess)
@@ -608,9 +608,56 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   if (e == cudaSuccess) e = launch_combine_latent(p.s, B, n_q, p.part, v, proj, stream);
   // 4. y = sum_h o_lat[h] W_vo[h]
   if (e == cudaSuccess)
-    e = launch_xw(MLA_F32, proj, M, p.s.n_h * p.s.d_c, fw->w.w_vo, p.s.d_model, y, part, fx.o,
-                  di->err, stream);
+    e = launch_xw(MLA_F32, proj, M, p.s.n_h * p.s.d_c, MLA_F32, fw->w.w_vo, p.s.d_model, y,
+                  part, fx.o, di->err, false, stream);
   return from_cuda(e);
+}
+
+mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
+                                           size_t* bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = 0;
+  size_t base = 0;
+  mla_status st = mla_decode_workspace_size(cfg, B, n_q, 0, &base);
+  if (st != MLA_OK) return st;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  const XwPlan po = xw_plan(B * n_q, cfg->n_h * cfg->d_v, cfg->d_model, di->sms);
+  *bytes = base + align256(sizeof(float) * xw_part_floats(B * n_q, cfg->d_model, po));
+  return MLA_OK;
+}
+
+mla_status mla_decode_layer(const mla_config* cfg, mla_weights w, const void* W_o, const void* x,
+                            const int32_t* seq_idx, const int32_t* pos, const void* q,
+                            void* cache, int32_t num_blocks, const int32_t* page_table,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                            float* out, float* y, void* workspace, size_t ws_bytes,
+                            cudaStream_t stream) {
+  if (!w || !W_o || !x || !seq_idx || !pos || !q || !cache || !page_table || !seq_lens || !out ||
+      !y)
+    return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di, true);
+  if (st != MLA_OK) return st;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  const int M = B * n_q;
+  const XwPlan po = xw_plan(M, p.s.n_h * p.s.d_v, p.s.d_model, di->sms);
+  const size_t part_bytes = align256(sizeof(float) * xw_part_floats(M, p.s.d_model, po));
+  if (ws_bytes < p.lay.total + part_bytes) return MLA_ERR_WORKSPACE;
+  // The new tokens go into the cache first, then the decode reads them.
+  st = mla_append_kv(cfg, w, x, seq_idx, pos, page_table, B, max_blocks, cache, num_blocks, M,
+                     stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode(cfg, w, q, cache, num_blocks, page_table, max_blocks, seq_lens, B, n_q, out,
+                  workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  // y = concat_h(o_h) W_o, launched early: its W_o stream overlaps the combine
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.lay.total);
+  return from_cuda(launch_xw(MLA_F32, out, M, p.s.n_h * p.s.d_v, cfg->dtype, W_o, p.s.d_model, y,
+                             part, po, di->err, true, stream));
 }
 
 mla_status mla_get_last_device_error(cudaStream_t stream, uint32_t* code) {

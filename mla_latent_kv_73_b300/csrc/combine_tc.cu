@@ -93,6 +93,9 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
     for (int kc = 0; kc < 8; ++kc) tma_prefetch_2d(&tmap_w, 64 * kc, h * 128);
   }
   griddep_wait();
+  // the next kernel (its weights are constant) may start its prologue now;
+  // it waits for this one to finish before it reads anything this one writes
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
     for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);

@@ -47,33 +47,53 @@ constexpr int XW_KC = 64;                      // K chunk staged in shared memor
 constexpr int QF_THREADS = 256;
 constexpr int FOLD_THREADS = 256;
 
-// TMA-ring form of the x W product (W rows 16-byte aligned: N % 4 == 0).
+// Bulk-copy-ring form of the x W product (W rows 16-byte aligned).
 constexpr int XR_CONSUMERS = 256;               // 8 warps, 4 columns per thread
 constexpr int XR_THREADS = XR_CONSUMERS + 32;   // + one producer warp
 constexpr int XR_COLS = 4 * XR_CONSUMERS;       // output columns per CTA
 constexpr int XR_RS = 8;                        // W rows per ring stage
-constexpr int XR_NST = 3;                       // ring stages
 constexpr int XR_KA = 192;                      // rows of A^T staged at a time (multiple of XR_RS)
 constexpr long long XR_WAIT = 2000000000LL;     // about 1 s at 2 GHz
 static_assert(XR_KA % XR_RS == 0, "a stage never straddles two A chunks");
 
-struct XrSmem {
-  float w[XR_NST][XR_RS][XR_COLS];  // 96 KB ring of W row segments
-  float a[XR_KA][XW_ROWS];          // A^T chunk, row index fastest
-  uint64_t full[XR_NST], empty[XR_NST];
+// The ring holds 96 KB of W whatever its type: 3 stages of fp32, 6 of bf16.
+template <typename TW>
+struct XrRing {
+  static constexpr int NST = 12 / static_cast<int>(sizeof(TW));
 };
 
+template <typename TW>
+struct XrSmem {
+  TW w[XrRing<TW>::NST][XR_RS][XR_COLS];  // ring of W row segments
+  float a[XR_KA][XW_ROWS];                // A^T chunk, row index fastest
+  uint64_t full[XrRing<TW>::NST], empty[XrRing<TW>::NST];
+};
+
+// Four consecutive W elements of a row, widened to fp32.
+__device__ __forceinline__ float4 load_w4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load_w4(const __nv_bfloat16* p) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                     __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u));
+}
+
 // out[z][m][n] = sum over k in split z of A[m][k] W[k][n], fp32 accumulation
-// in k order. W is fp32 row-major [K][N]; A is [M][K] in TA.
-template <typename TA>
+// in k order. W is row-major [K][N] in TW; A is [M][K] in TA.
+template <typename TA, typename TW>
 __global__ void __launch_bounds__(XW_THREADS)
-xw_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, int N,
+xw_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W, int N,
           int k_split, float* __restrict__ out) {
+  griddep_wait();  // A comes from the previous kernel (a no-op without programmatic launch)
   __shared__ __align__(16) float a_s[XW_KC][XW_ROWS];  // row index fastest
   const int n0 = blockIdx.x * XW_COLS + threadIdx.x * XW_VEC;
   const int m0 = blockIdx.y * XW_ROWS, mt = min(XW_ROWS, M - m0);
   const int kb = blockIdx.z * k_split, ke = min(K, kb + k_split);
-  const bool vec = (N % XW_VEC == 0) && n0 + XW_VEC <= N;
+  // one load of 4 consecutive W elements: rows must start at multiples of 4
+  // elements (N % 4 == 0) from a base aligned to 4 elements
+  const bool vec = (N % XW_VEC == 0) && n0 + XW_VEC <= N &&
+                   reinterpret_cast<uintptr_t>(W) % (XW_VEC * sizeof(TW)) == 0;
   float acc[XW_ROWS][XW_VEC];
 #pragma unroll
   for (int t = 0; t < XW_ROWS; ++t)
@@ -92,14 +112,14 @@ xw_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, i
     if (n0 < N) {
 #pragma unroll 4
       for (int k = 0; k < kc; ++k) {
-        const float* wp = W + static_cast<size_t>(k0 + k) * N + n0;
+        const TW* wp = W + static_cast<size_t>(k0 + k) * N + n0;
         float w[XW_VEC];
         if (vec) {
-          const float4 v = *reinterpret_cast<const float4*>(wp);
+          const float4 v = load_w4(wp);
           w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
         } else {
 #pragma unroll
-          for (int j = 0; j < XW_VEC; ++j) w[j] = n0 + j < N ? wp[j] : 0.f;
+          for (int j = 0; j < XW_VEC; ++j) w[j] = n0 + j < N ? to_f32<TW>(wp[j]) : 0.f;
         }
         const float4* av = reinterpret_cast<const float4*>(a_s[k]);
 #pragma unroll
@@ -149,13 +169,14 @@ __device__ __forceinline__ void consumer_bar() {
 // fmaf in the same order). Every wait is bounded: a timeout sets
 // MLA_DEVERR_TIMEOUT, the consumers stop waiting, and the producer waits
 // (bounded) for the copies it issued before the CTA exits.
-template <typename TA>
+template <typename TA, typename TW>
 __global__ void __launch_bounds__(XR_THREADS, 2)
-xw_ring_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__ W, int N,
+xw_ring_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W, int N,
                int k_split, float* __restrict__ out, uint32_t* err) {
+  constexpr int XR_NST = XrRing<TW>::NST;
   extern __shared__ uint8_t xr_raw[];
-  XrSmem& sm = *reinterpret_cast<XrSmem*>((reinterpret_cast<uintptr_t>(xr_raw) + 127) &
-                                          ~static_cast<uintptr_t>(127));
+  XrSmem<TW>& sm = *reinterpret_cast<XrSmem<TW>*>(
+      (reinterpret_cast<uintptr_t>(xr_raw) + 127) & ~static_cast<uintptr_t>(127));
   const int c0 = blockIdx.x * XR_COLS;
   const int m0 = blockIdx.y * XW_ROWS, mt = min(XW_ROWS, M - m0);
   const int kb = blockIdx.z * k_split, ke = min(K, kb + k_split);
@@ -172,7 +193,9 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__
 
   if (warp == XR_CONSUMERS / 32) {  // producer
     if (lane != 0) return;
-    const uint32_t seg = static_cast<uint32_t>(min(XR_COLS, N - c0)) * 4u;
+    // W is constant: the producer streams it without waiting for the
+    // previous kernel (programmatic launch lets this overlap that kernel)
+    const uint32_t seg = static_cast<uint32_t>(min(XR_COLS, N - c0)) * sizeof(TW);
     int it = 0;
     for (; it < n_it; ++it) {
       const int st = it % XR_NST;
@@ -191,6 +214,7 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__
     return;
   }
 
+  griddep_wait();  // A comes from the previous kernel (a no-op without programmatic launch)
   const int tid = threadIdx.x;
   const int n0 = c0 + 4 * tid;
   const bool live = n0 < N;  // N % 4 == 0: all four columns are in range
@@ -222,7 +246,7 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const float* __restrict__
 #pragma unroll
       for (int r = 0; r < XR_RS; ++r) {
         if (r < rows) {
-          const float4 w = *reinterpret_cast<const float4*>(&sm.w[st][r][4 * tid]);
+          const float4 w = load_w4(&sm.w[st][r][4 * tid]);
           const float2 w0 = make_float2(w.x, w.x), w1 = make_float2(w.y, w.y);
           const float2 w2 = make_float2(w.z, w.z), w3 = make_float2(w.w, w.w);
           const float4* av = reinterpret_cast<const float4*>(sm.a[k - a_base + r]);
@@ -424,41 +448,57 @@ size_t xw_part_floats(int M, int N, const XwPlan& p) {
   return p.S > 1 ? static_cast<size_t>(p.S) * M * N : 0;
 }
 
-template <typename TA>
-cudaError_t xw_ring_t(const TA* A, int M, int K, const float* W, int N, int k_split, float* dst,
-                      uint32_t* err, dim3 grid, cudaStream_t st) {
-  const int smem = static_cast<int>(sizeof(XrSmem)) + 128;
-  cudaError_t e = cudaFuncSetAttribute(xw_ring_kernel<TA>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  xw_ring_kernel<TA><<<grid, XR_THREADS, smem, st>>>(A, M, K, W, N, k_split, dst, err);
-  return cudaGetLastError();
+// Launches one of the two forms, with programmatic dependent launch when
+// pdl is set (the kernel's prologue and its W stream may then overlap the
+// previous kernel; its reads of A wait for that kernel).
+template <typename TA, typename TW>
+cudaError_t xw_t(const void* A_, int M, int K, const void* W_, int N, int k_split, float* dst,
+                 uint32_t* err, dim3 grid, bool pdl, cudaStream_t st) {
+  const TA* A = static_cast<const TA*>(A_);
+  const TW* W = static_cast<const TW*>(W_);
+  // the bulk copies need 16-byte aligned W rows
+  const bool ring = (static_cast<size_t>(N) * sizeof(TW)) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(W) % 16 == 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (ring) {
+    const int smem = static_cast<int>(sizeof(XrSmem<TW>)) + 128;
+    cudaError_t e = cudaFuncSetAttribute(xw_ring_kernel<TA, TW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cfg.blockDim = dim3(XR_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, xw_ring_kernel<TA, TW>, A, M, K, W, N, k_split, dst, err);
+  }
+  cfg.blockDim = dim3(XW_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, xw_kernel<TA, TW>, A, M, K, W, N, k_split, dst);
 }
 
-cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
-                      float* out, float* part, const XwPlan& p, uint32_t* err, cudaStream_t st) {
+cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, mla_dtype w_dt,
+                      const void* W, int N, float* out, float* part, const XwPlan& p,
+                      uint32_t* err, bool pdl, cudaStream_t st) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (M > 65535 * XW_ROWS) return cudaErrorInvalidValue;
   static_assert(XR_COLS == XW_COLS, "both forms tile the columns alike");
   dim3 grid((N + XW_COLS - 1) / XW_COLS, (M + XW_ROWS - 1) / XW_ROWS, p.S);
   float* dst = p.S > 1 ? part : out;
-  // the bulk copies need 16-byte aligned W rows
-  const bool ring = N % 4 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0;
+  using bf16 = __nv_bfloat16;
   cudaError_t e;
-  if (ring && a_dt == MLA_F32)
-    e = xw_ring_t<float>(static_cast<const float*>(A), M, K, W, N, p.k_split, dst, err, grid, st);
-  else if (ring)
-    e = xw_ring_t<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(A), M, K, W, N, p.k_split,
-                                 dst, err, grid, st);
-  else if (a_dt == MLA_F32) {
-    xw_kernel<float><<<grid, XW_THREADS, 0, st>>>(static_cast<const float*>(A), M, K, W, N,
-                                                  p.k_split, dst);
-    e = cudaGetLastError();
-  } else {
-    xw_kernel<__nv_bfloat16><<<grid, XW_THREADS, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(A), M, K, W, N, p.k_split, dst);
-    e = cudaGetLastError();
-  }
+  if (a_dt == MLA_F32 && w_dt == MLA_F32)
+    e = xw_t<float, float>(A, M, K, W, N, p.k_split, dst, err, grid, pdl, st);
+  else if (a_dt == MLA_F32)
+    e = xw_t<float, bf16>(A, M, K, W, N, p.k_split, dst, err, grid, pdl, st);
+  else if (w_dt == MLA_F32)
+    e = xw_t<bf16, float>(A, M, K, W, N, p.k_split, dst, err, grid, pdl, st);
+  else
+    e = xw_t<bf16, bf16>(A, M, K, W, N, p.k_split, dst, err, grid, pdl, st);
   if (e != cudaSuccess || p.S == 1) return e;
   const size_t n = static_cast<size_t>(M) * N;
   const size_t blocks = (n + 255) / 256;

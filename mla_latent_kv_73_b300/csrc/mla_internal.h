@@ -130,10 +130,12 @@ cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
                            const WsView& ws, float* out, cudaStream_t st);
 
-// Full-fold variant. launch_fold_full builds FullWeights' matrices from the
-// caller's W_q, W_uk, W_uv and W_o (all in dt). launch_xw computes
-// out[M][N] = A[M][K] W[K][N] (A in a_dt, W and out fp32) with the split-K
-// plan from xw_plan; part holds xw_part_floats() floats of split partials.
+// Full-fold variant and output projection. launch_fold_full builds
+// FullWeights' matrices from the caller's W_q, W_uk, W_uv and W_o (all in
+// dt). launch_xw computes out[M][N] = A[M][K] W[K][N] (A in a_dt, W in w_dt,
+// out fp32) with the split-K plan from xw_plan; part holds xw_part_floats()
+// floats of split partials; pdl launches it with programmatic dependent
+// launch (its W stream may overlap the previous kernel).
 // launch_q_finish turns the fp32 query projection [B*n_q][n_h*R] into the
 // workspace's qabs (RoPE on the rotary block, times out_scale, rounded to
 // dt) and writes the split-KV plan. launch_combine_latent merges the splits
@@ -143,8 +145,9 @@ cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, cons
                              cudaStream_t st);
 XwPlan xw_plan(int M, int K, int N, int sms);
 size_t xw_part_floats(int M, int N, const XwPlan& p);
-cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, const float* W, int N,
-                      float* out, float* part, const XwPlan& p, uint32_t* err, cudaStream_t st);
+cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, mla_dtype w_dt,
+                      const void* W, int N, float* out, float* part, const XwPlan& p,
+                      uint32_t* err, bool pdl, cudaStream_t st);
 cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,

@@ -93,6 +93,10 @@ def test_null_and_count_checks(lib):
     assert lib.mla_decode_full_workspace_size(ctypes.byref(cfg), 4, 1, None) == 1
     assert lib.mla_decode_full(ctypes.byref(cfg), None, None, None, 1, None, 1, None, 1, 1, None,
                                None, 0, None) == 1
+    assert lib.mla_decode_layer_workspace_size(ctypes.byref(cfg), 4, 0, ctypes.byref(n)) == 2
+    assert lib.mla_decode_layer_workspace_size(ctypes.byref(cfg), 4, 1, None) == 1
+    assert lib.mla_decode_layer(ctypes.byref(cfg), None, None, None, None, None, None, None, 1,
+                                None, 1, None, 1, 1, None, None, None, 0, None) == 1
     assert lib.mla_get_last_device_error(None, None) == 1
 
 
