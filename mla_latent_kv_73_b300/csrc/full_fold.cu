@@ -27,12 +27,13 @@
 // Folded weights are kept in fp32 (the product of two rounded matrices is
 // not a value of the input dtype); the fold accumulates in fp64. The two
 // x W products are HBM-bound weight streams: a CTA owns 1024 output columns
-// (4 per thread, 16-byte loads) and 16 query rows, and K is split across
+// (4 per thread) and 16 query rows, W arrives by TMA, and K is split across
 // CTAs until the grid covers the SMs twice. The split partials are summed in
 // a fixed order by a second kernel, so results are deterministic.
 #include "device_common.cuh"
 #include "plan.cuh"
 #include "sm100_ptx.cuh"
+#include "tmap.h"
 
 namespace mla {
 namespace {
@@ -47,26 +48,33 @@ constexpr int XW_KC = 64;                      // K chunk staged in shared memor
 constexpr int QF_THREADS = 256;
 constexpr int FOLD_THREADS = 256;
 
-// Bulk-copy-ring form of the x W product (W rows 16-byte aligned).
+// TMA-ring form of the x W product (W rows 16-byte aligned). W arrives in
+// 2-D tensor-map boxes of XR_BOXC columns x RS rows: four boxes cover a
+// CTA's 1024 columns, and a stage is 32 KB whatever W's type (8 rows of
+// fp32, 16 of bf16), so each request moves 8 KB. (One 1-D bulk copy per row,
+// 2-4 KB each, left the copy engine request-bound.)
 constexpr int XR_CONSUMERS = 256;               // 8 warps, 4 columns per thread
 constexpr int XR_THREADS = XR_CONSUMERS + 32;   // + one producer warp
 constexpr int XR_COLS = 4 * XR_CONSUMERS;       // output columns per CTA
-constexpr int XR_RS = 8;                        // W rows per ring stage
-constexpr int XR_KA = 192;                      // rows of A^T staged at a time (multiple of XR_RS)
+constexpr int XR_BOXC = 256;                    // columns per tensor-map box
+constexpr int XR_NBOX = XR_COLS / XR_BOXC;      // boxes per stage
+constexpr int XR_NST = 3;                       // ring stages
+constexpr int XR_KGRAN = 16;                    // K splits are multiples of every RS
+constexpr int XR_KA = 192;                      // rows of A^T staged at a time
 constexpr long long XR_WAIT = 2000000000LL;     // about 1 s at 2 GHz
-static_assert(XR_KA % XR_RS == 0, "a stage never straddles two A chunks");
 
-// The ring holds 96 KB of W whatever its type: 3 stages of fp32, 6 of bf16.
 template <typename TW>
 struct XrRing {
-  static constexpr int NST = 12 / static_cast<int>(sizeof(TW));
+  static constexpr int RS = 32 / static_cast<int>(sizeof(TW));  // W rows per stage
+  static_assert(XR_KA % RS == 0, "a stage never straddles two A chunks");
+  static_assert(XR_KGRAN % RS == 0, "splits hold whole stages");
 };
 
 template <typename TW>
 struct XrSmem {
-  TW w[XrRing<TW>::NST][XR_RS][XR_COLS];  // ring of W row segments
-  float a[XR_KA][XW_ROWS];                // A^T chunk, row index fastest
-  uint64_t full[XrRing<TW>::NST], empty[XrRing<TW>::NST];
+  TW w[XR_NST][XR_NBOX][XrRing<TW>::RS][XR_BOXC];  // ring of W boxes (32 KB per stage)
+  float a[XR_KA][XW_ROWS];                          // A^T chunk, row index fastest
+  uint64_t full[XR_NST], empty[XR_NST];
 };
 
 // Four consecutive W elements of a row, widened to fp32.
@@ -159,21 +167,21 @@ __device__ __forceinline__ void consumer_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(XR_CONSUMERS) : "memory");
 }
 
-// The same product as xw_kernel, with W streamed by the bulk-copy engine.
-// One producer thread copies, per stage, XR_RS rows of the CTA's 4 KB W
-// segment into a 3-stage shared-memory ring; two CTAs per SM keep up to
-// 192 KB of W in flight per SM without holding it in registers. The 256
-// consumer threads read their 16 bytes of each row from shared memory and
-// the 16 A values as four broadcast reads, and accumulate pairs of rows with
+// The same product as xw_kernel, with W streamed by TMA. One producer thread
+// loads, per stage, four boxes (RS rows x 256 columns) of the CTA's columns
+// into a 3-stage shared-memory ring; two CTAs per SM keep up to 192 KB of W
+// in flight per SM without holding it in registers. The 256 consumer
+// threads read their 4 elements of each row from shared memory and the 16 A
+// values as four broadcast reads, and accumulate pairs of rows with
 // the packed fp32x2 FMA (one IEEE fma per lane, so the sums are those of
 // fmaf in the same order). Every wait is bounded: a timeout sets
 // MLA_DEVERR_TIMEOUT, the consumers stop waiting, and the producer waits
 // (bounded) for the copies it issued before the CTA exits.
 template <typename TA, typename TW>
 __global__ void __launch_bounds__(XR_THREADS, 2)
-xw_ring_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W, int N,
-               int k_split, float* __restrict__ out, uint32_t* err) {
-  constexpr int XR_NST = XrRing<TW>::NST;
+xw_ring_kernel(const __grid_constant__ CUtensorMap tmap_w, const TA* __restrict__ A, int M,
+               int K, int N, int k_split, float* __restrict__ out, uint32_t* err) {
+  constexpr int XR_RS = XrRing<TW>::RS;
   extern __shared__ uint8_t xr_raw[];
   XrSmem<TW>& sm = *reinterpret_cast<XrSmem<TW>*>(
       (reinterpret_cast<uintptr_t>(xr_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -194,8 +202,12 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W,
   if (warp == XR_CONSUMERS / 32) {  // producer
     if (lane != 0) return;
     // W is constant: the producer streams it without waiting for the
-    // previous kernel (programmatic launch lets this overlap that kernel)
-    const uint32_t seg = static_cast<uint32_t>(min(XR_COLS, N - c0)) * sizeof(TW);
+    // previous kernel (programmatic launch lets this overlap that kernel).
+    // Boxes past N are not loaded; a box's columns past N and rows past K
+    // arrive as zeros and still count their bytes.
+    prefetch_tmap(&tmap_w);
+    const int nbox = min(XR_NBOX, (N - c0 + XR_BOXC - 1) / XR_BOXC);
+    const uint32_t stage_bytes = static_cast<uint32_t>(nbox * XR_RS * XR_BOXC * sizeof(TW));
     int it = 0;
     for (; it < n_it; ++it) {
       const int st = it % XR_NST;
@@ -203,10 +215,10 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W,
         set_error(err, MLA_DEVERR_TIMEOUT);
         break;
       }
-      const int k = kb + it * XR_RS, rows = min(XR_RS, ke - k);
-      mbar_arrive_expect_tx(&sm.full[st], static_cast<uint32_t>(rows) * seg);
-      for (int r = 0; r < rows; ++r)
-        bulk_load(sm.w[st][r], W + static_cast<size_t>(k + r) * N + c0, seg, &sm.full[st]);
+      const int k = kb + it * XR_RS;
+      mbar_arrive_expect_tx(&sm.full[st], stage_bytes);
+      for (int j = 0; j < nbox; ++j)
+        tma_load_2d(sm.w[st][j], &tmap_w, c0 + j * XR_BOXC, k, &sm.full[st]);
     }
     // the copies issued last land before this thread (and so the CTA) exits
     for (int j = it > XR_NST ? it - XR_NST : 0; j < it; ++j)
@@ -246,7 +258,7 @@ xw_ring_kernel(const TA* __restrict__ A, int M, int K, const TW* __restrict__ W,
 #pragma unroll
       for (int r = 0; r < XR_RS; ++r) {
         if (r < rows) {
-          const float4 w = load_w4(&sm.w[st][r][4 * tid]);
+          const float4 w = load_w4(&sm.w[st][tid / 64][r][4 * (tid % 64)]);
           const float2 w0 = make_float2(w.x, w.x), w1 = make_float2(w.y, w.y);
           const float2 w2 = make_float2(w.z, w.z), w3 = make_float2(w.w, w.w);
           const float4* av = reinterpret_cast<const float4*>(sm.a[k - a_base + r]);
@@ -427,18 +439,18 @@ cudaError_t q_finish_t(const Shape& s, const double* inv_freq, const float* qpre
 
 // K is split so that the grid fills the two CTAs per SM that the ring kernel
 // holds in one wave (tiles * S <= 2 * sms) without leaving most SMs idle:
-// S = floor(2 sms / tiles), at least 1, in whole stages of XR_RS rows.
+// S = floor(2 sms / tiles), at least 1, in whole groups of XR_KGRAN rows.
 XwPlan xw_plan(int M, int K, int N, int sms) {
   XwPlan p;
   const long long tiles = static_cast<long long>((N + XW_COLS - 1) / XW_COLS) *
                           ((M + XW_ROWS - 1) / XW_ROWS);
-  const int stages = (K + XR_RS - 1) / XR_RS;
+  const int stages = (K + XR_KGRAN - 1) / XR_KGRAN;
   long long S = tiles > 0 ? (2LL * sms) / tiles : 1;
   if (S > stages) S = stages;
   if (S < 1) S = 1;
   if (S > 65535) S = 65535;
   const int per = (stages + static_cast<int>(S) - 1) / static_cast<int>(S);
-  p.k_split = per * XR_RS;
+  p.k_split = per * XR_KGRAN;
   p.S = (K + p.k_split - 1) / p.k_split;
   if (p.S < 1) p.S = 1;
   return p;
@@ -456,8 +468,8 @@ cudaError_t xw_t(const void* A_, int M, int K, const void* W_, int N, int k_spli
                  uint32_t* err, dim3 grid, bool pdl, cudaStream_t st) {
   const TA* A = static_cast<const TA*>(A_);
   const TW* W = static_cast<const TW*>(W_);
-  // the bulk copies need 16-byte aligned W rows
-  const bool ring = (static_cast<size_t>(N) * sizeof(TW)) % 16 == 0 &&
+  // the tensor map needs a 16-byte aligned base and row stride
+  bool ring = (static_cast<size_t>(N) * sizeof(TW)) % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(W) % 16 == 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -467,6 +479,20 @@ cudaError_t xw_t(const void* A_, int M, int K, const void* W_, int N, int k_spli
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  CUtensorMap tm;
+  if (ring) {
+    TmapSpec spec = {};
+    spec.dtype = sizeof(TW) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    spec.rank = 2;
+    spec.base = W;
+    spec.dims[0] = static_cast<uint64_t>(N);
+    spec.dims[1] = static_cast<uint64_t>(K);
+    spec.strides[0] = static_cast<uint64_t>(N) * sizeof(TW);
+    spec.box[0] = XR_BOXC;
+    spec.box[1] = XrRing<TW>::RS;
+    spec.swizzle = CU_TENSOR_MAP_SWIZZLE_NONE;
+    ring = get_tmap(spec, &tm);  // the register form takes what the encoder refuses
+  }
   if (ring) {
     const int smem = static_cast<int>(sizeof(XrSmem<TW>)) + 128;
     cudaError_t e = cudaFuncSetAttribute(xw_ring_kernel<TA, TW>,
@@ -474,7 +500,7 @@ cudaError_t xw_t(const void* A_, int M, int K, const void* W_, int N, int k_spli
     if (e != cudaSuccess) return e;
     cfg.blockDim = dim3(XR_THREADS);
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, xw_ring_kernel<TA, TW>, A, M, K, W, N, k_split, dst, err);
+    return cudaLaunchKernelEx(&cfg, xw_ring_kernel<TA, TW>, tm, A, M, K, N, k_split, dst, err);
   }
   cfg.blockDim = dim3(XW_THREADS);
   cfg.dynamicSmemBytes = 0;

@@ -110,9 +110,10 @@ def test_full_fold_bf16_dsv2_latent(impl, n_q):
 
 
 def test_full_fold_unaligned_output_written_directly():
-    """n_h*d_c = 64 is one K chunk, so the output projection writes y itself,
-    here at a 4-byte offset from a 16-byte boundary."""
-    w, lens = workload(2, 64, 32, 8, 16, 16, (3, 90), 1, "f32", seed=23)
+    """n_h*d_c = 16 rows of W_vo are one K split, so the output projection
+    writes y itself (no split partials), here at a 4-byte offset from a
+    16-byte boundary."""
+    w, lens = workload(2, 64, 8, 2, 4, 4, (3, 90), 1, "f32", seed=23)
     r = FullRun(w, lens, y_offset=1)
     assert r.y.data_ptr() % 16 == 4
     check("f32", r.decode(), r.oracle(), "unaligned y")
