@@ -152,12 +152,16 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples go to MLA_CLOCKS_CSV if set (to keep them), else to
+        # a temporary file; the JSON line carries their summary either way
+        self.path = os.environ.get("MLA_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), f"mla_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
