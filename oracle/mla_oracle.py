@@ -471,3 +471,54 @@ def layer_step_materialised(q, seq_rows, seq_lens, W_uk, W_uv, W_o, d_c, d_nope,
     o = decode_materialised(q, seq_rows, seq_lens, W_uk, W_uv, d_c, d_nope, d_v, scale, base)
     B, n_q, n_h, _ = o.shape
     return o.reshape(B, n_q, n_h * d_v) @ np.asarray(W_o, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) latent cache with one scale per row
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0  # 1.75 * 2^8, the largest finite e4m3 value
+
+
+def e4m3_round(x):
+    """Nearest e4m3 value of each element (ties to even), in fp64.
+
+    The e4m3 format ("fn" variant): 1 sign bit, 4 exponent bits with bias 7,
+    3 mantissa bits; below 2^-6 the values are subnormal, in steps of 2^-9;
+    the largest finite value is 448 and there are no infinities. A magnitude
+    above 448 saturates to 448 (reading: the row quantiser scales every row
+    so that none does).
+
+    The pages quantise the latent vector only in passing [P5 "Moving a
+    trained MHA model over": quantisation on top of the latent cache, and its
+    error passing through the up-projection]; they fix neither the format
+    nor the scale granularity.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, E = np.frexp(a)                    # a = m * 2^E with m in [0.5, 1)
+    e = np.maximum(E - 1, -6)             # binade exponent; subnormals share 2^-6's step
+    step = np.ldexp(1.0, e - 3)           # 3 mantissa bits
+    q = np.minimum(np.rint(a / step) * step, E4M3_MAX)  # rint: ties to even
+    return np.copysign(q, x)
+
+
+def quantize_rows_fp8(rows, dtype=np.float64):
+    """One cache row -> (e4m3 values, one scale), row by row.
+
+    scale = max|row| / 448 and code = e4m3_round(row / scale), so each row's
+    largest element becomes +-448 exactly. A row of zeros gets scale 1.
+    ``dtype`` is the precision the scale and the division are computed in
+    (np.float32 mirrors a kernel that quantises fp32 accumulators).
+    Returns (codes [..., R] fp64 holding e4m3 values, scales [...] fp64).
+    """
+    r = np.asarray(rows, dtype=dtype)
+    amax = np.max(np.abs(r), axis=-1)
+    scale = np.where(amax > 0, amax / dtype(E4M3_MAX), dtype(1.0)).astype(dtype)
+    codes = e4m3_round((r / scale[..., None]).astype(dtype))
+    return codes, scale.astype(np.float64)
+
+
+def dequantize_rows_fp8(codes, scales):
+    """Cache rows back from e4m3 values and their row scales: code * scale."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[..., None]

@@ -618,3 +618,112 @@ def test_planted_layer_mistakes_are_caught(monkeypatch, target, idx):
         except AssertionError:
             failures += 1
     assert failures >= 1, f"planted mistake in {target} went unnoticed"
+
+
+# ---------------------------------------------------------------------------
+# fp8 (e4m3) latent cache: the format against torch's float8_e4m3fn
+# ---------------------------------------------------------------------------
+
+
+def _e4m3_values():
+    """Every finite e4m3 value, decoded by torch from its byte (254 of 256)."""
+    v = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return v[np.isfinite(v)]
+
+
+def test_e4m3_code_points_are_fixed_points():
+    v = _e4m3_values()
+    assert len(v) == 254 and v.max() == 448.0 and v.min() == -448.0
+    assert np.array_equal(O.e4m3_round(v), v)
+
+
+def test_e4m3_rounding_matches_torch():
+    """Random values, every midpoint between neighbouring codes (the ties),
+    their fp32 neighbours, and the subnormal range: the same value as
+    torch's float32 -> float8_e4m3fn conversion."""
+    g = np.random.default_rng(17)
+    pos = np.unique(np.abs(_e4m3_values()))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    x = np.concatenate([
+        g.uniform(-448, 448, 20000).astype(np.float32),
+        (g.standard_normal(20000) * 4).astype(np.float32),
+        g.uniform(-2.0 ** -5, 2.0 ** -5, 5000).astype(np.float32),
+        mids, -mids,
+        np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+    ])
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3_round(x.astype(np.float64)), want)
+
+
+def test_e4m3_saturates_past_448():
+    x = np.array([448.0, 450.0, 464.0, 470.0, 1e4, -1e6])
+    assert np.array_equal(O.e4m3_round(x), [448, 448, 448, 448, 448, -448])
+
+
+@pytest.mark.parametrize("dtype", [np.float64, np.float32])
+def test_fp8_row_quantiser(dtype):
+    g = np.random.default_rng(18)
+    rows = g.standard_normal((64, 576))
+    rows[3] = 0.0
+    codes, scales = O.quantize_rows_fp8(rows, dtype=dtype)
+    assert np.array_equal(O.e4m3_round(codes), codes)  # only e4m3 values
+    live = np.arange(64) != 3
+    assert np.all(np.max(np.abs(codes[live]), axis=1) == 448.0)
+    assert scales[3] == 1.0 and np.all(codes[3] == 0)
+    assert np.array_equal(scales.astype(dtype).astype(np.float64), scales)
+    r = rows.astype(dtype).astype(np.float64)
+    deq = O.dequantize_rows_fp8(codes, scales)
+    u = np.abs(r) / scales[:, None]  # magnitude in code units
+    err = np.abs(deq - r) / scales[:, None]
+    tol = np.where(u >= 2.0 ** -6, 2.0 ** -4 * u, 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(err <= tol + (1e-6 if dtype == np.float32 else 0))
+
+
+def test_fp8_cache_error_reaches_the_output():
+    """Attention over dequantised rows: the quantisation error passes through
+    to the output (P5 "Moving a trained MHA model over"), small but not
+    zero."""
+    t = _tiny(seed=19, L=200)
+    codes, scales = O.quantize_rows_fp8(t["rows"])
+    t8 = dict(t, rows=O.dequantize_rows_fp8(codes, scales))
+    a, b = _oracle_out(t, 1), _oracle_out(t8, 1)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 1e-4 < rel < 5e-2
+
+
+def _fp8_mutants():
+    def truncating(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        _, E = np.frexp(a)
+        step = np.ldexp(1.0, np.maximum(E - 1, -6) - 3)
+        return np.copysign(np.minimum(np.floor(a / step) * step, 448.0), x)
+
+    def no_subnormals(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        _, E = np.frexp(a)
+        step = np.ldexp(1.0, np.maximum(E - 1, -9) - 3)
+        return np.copysign(np.minimum(np.rint(a / step) * step, 448.0), x)
+
+    def two_mantissa_bits(x):
+        x = np.asarray(x, dtype=np.float64)
+        a = np.abs(x)
+        _, E = np.frexp(a)
+        step = np.ldexp(1.0, np.maximum(E - 1, -6) - 2)
+        return np.copysign(np.minimum(np.rint(a / step) * step, 448.0), x)
+
+    return [truncating, no_subnormals, two_mantissa_bits]
+
+
+@pytest.mark.parametrize("idx", range(3))
+def test_planted_fp8_mistakes_are_caught(monkeypatch, idx):
+    monkeypatch.setattr(O, "e4m3_round", _fp8_mutants()[idx])
+    failures = 0
+    for check in (test_e4m3_code_points_are_fixed_points, test_e4m3_rounding_matches_torch):
+        try:
+            check()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1
