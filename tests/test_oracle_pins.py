@@ -727,3 +727,33 @@ def test_planted_fp8_mistakes_are_caught(monkeypatch, idx):
         except AssertionError:
             failures += 1
     assert failures >= 1
+
+
+def test_prefill_chunk_matches_library_attention():
+    """A 24-token chunk at the end of a 40-token sequence (a prefill step):
+    each chunk token sees the earlier tokens and itself. Checked against
+    torch's attention with the same causal pattern, keys and values built
+    per head."""
+    g = np.random.default_rng(20)
+    n_h, d_model, d_c, d_r, d_nope, d_v, L, n_q = 3, 24, 16, 4, 6, 5, 40, 24
+    W_dkv = g.normal(0, d_model ** -0.5, (d_model, d_c))
+    W_kr = g.normal(0, d_model ** -0.5, (d_model, d_r))
+    W_uk = g.normal(0, d_c ** -0.5, (d_c, n_h * d_nope))
+    W_uv = g.normal(0, d_c ** -0.5, (d_c, n_h * d_v))
+    rows = O.latent_rows(g.normal(size=(L, d_model)), W_dkv, W_kr, np.arange(L), 1e4)
+    q = g.normal(size=(1, n_q, n_h, d_nope + d_r))
+    scale = O.default_scale(d_nope, d_r)
+    got = O.decode_materialised(q, [rows], [L], W_uk, W_uv, d_c, d_nope, d_v, scale, 1e4)[0]
+    C, KR = rows[:, :d_c], rows[:, d_c:]
+    pos = L - n_q + np.arange(n_q)
+    mask = torch.tensor(np.arange(L)[None, :] <= pos[:, None])
+    for h in range(n_h):
+        K = np.concatenate([C @ W_uk[:, h * d_nope:(h + 1) * d_nope], KR], axis=1)
+        V = C @ W_uv[:, h * d_v:(h + 1) * d_v]
+        Q = np.stack([np.concatenate([q[0, i, h, :d_nope],
+                                      O.apply_rope(q[0, i, h, d_nope:], pos[i], 1e4)])
+                      for i in range(n_q)])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(Q)[None], torch.tensor(K)[None], torch.tensor(V)[None],
+            attn_mask=mask[None], scale=scale)[0].numpy()
+        assert np.max(np.abs(got[:, h] - ref)) < 1e-12
