@@ -211,7 +211,7 @@ def _tiny(seed=0, n_h=4, d_model=32, d_c=16, d_r=8, d_nope=8, d_v=8, L=37):
                 n_h=n_h, d_c=d_c, d_r=d_r, d_nope=d_nope, d_v=d_v, L=L)
 
 
-def _sdpa_reference(t, n_q):
+def _sdpa_reference(t, n_q, default_scale=False):
     """Textbook attention via torch's scaled_dot_product_attention.
 
     Keys and values are built explicitly per head: k = [c W_uk_h | k_rope],
@@ -232,7 +232,8 @@ def _sdpa_reference(t, n_q):
         mask = torch.tensor(np.arange(L)[None, :] <= (L - n_q + np.arange(n_q))[:, None])
         o = torch.nn.functional.scaled_dot_product_attention(
             Q, torch.tensor(K)[None, None], torch.tensor(V)[None, None],
-            attn_mask=mask[None, None], scale=O.default_scale(d_nope, t["d_r"]))
+            attn_mask=mask[None, None],
+            scale=None if default_scale else O.default_scale(d_nope, t["d_r"]))
         out[:, h] = o[0, 0].numpy()
     return out
 
@@ -359,6 +360,73 @@ def test_two_queries_are_causal():
     assert np.max(np.abs(both2[1] - both[1])) > 1e-6
 
 
+def test_default_scale_is_torch_attention_default():
+    """The score scale over the full query/key width d_nope + d_r.
+
+    Two anchors outside the oracle: the DeepSeek-V2-shape workload states its
+    scale as 1/sqrt(192) (d_nope 128 + d_r 64), and torch's
+    scaled_dot_product_attention, called with no scale, divides by the square
+    root of the query width, here [q_nope | RoPE(q_rope)]. A scale over
+    d_nope alone (P1's toy has no RoPE block, so its 1/sqrt(head_dim) does not
+    tell the two apart) fails both.
+    """
+    assert O.default_scale(128, 64) == 1.0 / math.sqrt(192.0)
+    assert O.default_scale(16, 8) == 1.0 / math.sqrt(24.0)
+    assert O.default_scale(8, 0) == 1.0 / math.sqrt(8.0)
+    for seed, d_nope, d_r in ((21, 8, 8), (22, 16, 4)):
+        t = _tiny(seed=seed, d_nope=d_nope, d_r=d_r, L=29)
+        got = _oracle_out(t, 2)
+        ref = _sdpa_reference(t, 2, default_scale=True)
+        assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def _self_score(x, W_kr, pos):
+    """RoPE part of the score of a query whose unrotated rope vector is the
+    key's own x W_kr, both at position pos."""
+    kr = O.latent_rows(x[None], np.zeros((x.shape[0], 1)), W_kr, np.array([pos]), 1e4)[0, 1:]
+    return O.apply_rope(x @ W_kr, pos, 1e4) @ kr
+
+
+def test_latent_rows_rotate_each_key_by_its_own_position():
+    """Pins the position latent_rows rotates each key by.
+
+    [P1 "RoPE, and why the explanations stop here"]: k_rope is computed the
+    ordinary way, rotated by its token's position and cached already rotated;
+    the query is rotated by its own position at decode time.
+      * A key at position 0 is not rotated: its rope block is x W_kr.
+      * A query and key at the same position with the same unrotated vector
+        score |x W_kr|^2, whatever the position (both rotations cancel).
+      * Shifting every key position and the query position by the same
+        offset leaves the decode output unchanged (RoPE's relative-position
+        property), while shifting the keys alone changes it.
+    A key rotated by pos + 1, by -pos, or not at all fails one of these.
+    """
+    g = np.random.default_rng(23)
+    d_model, d_r = 12, 8
+    W_kr = g.normal(0, d_model ** -0.5, (d_model, d_r))
+    X = g.normal(size=(6, d_model))
+    r0 = O.latent_rows(X, np.zeros((d_model, 3)), W_kr, np.zeros(6, dtype=np.int64), 1e4)
+    assert np.max(np.abs(r0[:, 3:] - X @ W_kr)) == 0.0
+    for pos in (0, 1, 7, 4095, 131071):
+        u = X[pos % 6] @ W_kr
+        assert abs(_self_score(X[pos % 6], W_kr, pos) - u @ u) < 1e-9 * (1 + u @ u)
+    # the whole decode: keys at positions delta .. delta + L - 1, query at the last one
+    t = _tiny(seed=24, L=33)
+    scale = O.default_scale(t["d_nope"], t["d_r"])
+    wuk, wuv = O.head_slice(t["W_uk"], 2, t["d_nope"]), O.head_slice(t["W_uv"], 2, t["d_v"])
+    outs = []
+    for delta in (0, 5, 1000, 131038):
+        rows = O.latent_rows(t["X"], t["W_dkv"], t["W_kr"], np.arange(t["L"]) + delta, 1e4)
+        outs.append(O.decode_head_materialised(t["q"][0, 0, 2], rows, t["L"] - 1 + delta,
+                                               wuk, wuv, t["d_c"], scale, 1e4))
+    for o in outs[1:]:
+        assert np.max(np.abs(o - outs[0])) < 1e-12
+    rows = O.latent_rows(t["X"], t["W_dkv"], t["W_kr"], np.arange(t["L"]) + 5, 1e4)
+    moved = O.decode_head_materialised(t["q"][0, 0, 2], rows, t["L"] - 1, wuk, wuv, t["d_c"],
+                                       scale, 1e4)
+    assert np.max(np.abs(moved - outs[0])) > 1e-6
+
+
 # ---------------------------------------------------------------------------
 # Paged layout and append
 # ---------------------------------------------------------------------------
@@ -464,6 +532,43 @@ def test_planted_mistakes_are_caught(monkeypatch, target, idx):
     for check in (lambda: test_materialised_matches_library_attention(2),
                   test_rope_matches_explicit_rotation_and_preserves_norm,
                   test_softmax_rows_sum_to_one_and_match_library):
+        try:
+            check()
+        except AssertionError:
+            failures += 1
+    assert failures >= 1, f"planted mistake in {target} went unnoticed"
+
+
+ORIG_LATENT_ROWS = O.latent_rows
+
+
+def _position_mutants():
+    def scale_without_rope_width(d_nope, d_r):
+        return 1.0 / math.sqrt(d_nope)
+
+    def scale_over_head_count(d_nope, d_r):
+        return 1.0 / (d_nope + d_r)
+
+    def keys_rotated_one_late(x, W_dkv, W_kr, pos, base):
+        return ORIG_LATENT_ROWS(x, W_dkv, W_kr, np.asarray(pos) + 1, base)
+
+    def keys_unrotated(x, W_dkv, W_kr, pos, base):
+        return ORIG_LATENT_ROWS(x, W_dkv, W_kr, np.zeros_like(np.asarray(pos)), base)
+
+    def keys_rotated_backwards(x, W_dkv, W_kr, pos, base):
+        return ORIG_LATENT_ROWS(x, W_dkv, W_kr, -np.asarray(pos), base)
+
+    return {"default_scale": [scale_without_rope_width, scale_over_head_count],
+            "latent_rows": [keys_rotated_one_late, keys_unrotated, keys_rotated_backwards]}
+
+
+@pytest.mark.parametrize("target,idx",
+                         [(k, i) for k, v in _position_mutants().items() for i in range(len(v))])
+def test_planted_scale_and_position_mistakes_are_caught(monkeypatch, target, idx):
+    monkeypatch.setattr(O, target, _position_mutants()[target][idx])
+    failures = 0
+    for check in (test_default_scale_is_torch_attention_default,
+                  test_latent_rows_rotate_each_key_by_its_own_position):
         try:
             check()
         except AssertionError:
