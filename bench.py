@@ -4,19 +4,31 @@
 A step is one pass of the whole hot path over one batch: compress-and-append
 the B*n_q new tokens (mla_append_kv), then decode (absorb q, split-KV
 attention over the paged latent cache, log-sum-exp combine, W_uv
-up-projection). It runs on the DeepSeek-V2-shaped workload: batch 16, 4096
-cached tokens per sequence, 1 query token, bf16 cache.
+up-projection).
+
+The JSON line is headed by the DeepSeek-V2-shape ragged workload (batch 64,
+cached lengths uniform in [512, 32768], 1 query token, bf16 cache), the
+largest DeepSeek-V2-shape decode workload on one GPU. The same run times the
+other bf16 workloads (batch 16 x 4096; batch 4 x 131072 with 2 query tokens;
+16 heads, batch 256 x [1024, 8192]) and reports each under ``per_config``:
+tokens/s, cache GB/s, the attention kernel's roofline fraction and the whole
+step's roofline fraction.
 
 L2 hygiene: the timed steps cycle through several layer-sized input sets
 (cache, page table, weights, queries, hidden states). Their total is more
 than 3x the L2 size, so no step finds its inputs in L2.
 
+``--gpus N`` without a torchrun environment starts N local processes
+through torch.distributed.run, one replica per GPU (sequences shard across
+replicas with no collective on the data path).
+
 Prints one JSON line. --impl reference times the fp64 CPU oracle on a
-bounded sample of the same workload instead.
+bounded sample of the headline workload instead.
 """
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -32,7 +44,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode tokens/s and latent-cache GB/s at 1 B300, % of roofline"
-DEFAULT_WORKLOAD = "dsv2_b16_l4096"
+# The largest DeepSeek-V2-shape workload that fits one GPU heads the line;
+# the other bf16 workloads are timed in the same run (per_config).
+DEFAULT_WORKLOAD = "dsv2_b64_ragged"
+PER_CONFIG = ["dsv2_b64_ragged", "dsv2_b16_l4096", "dsv2_b4_l131072_nq2", "nh16_b256_ragged"]
 
 
 def parse():
@@ -43,6 +58,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="time the --workload alone (no per_config rows for the others)")
     ap.add_argument("--cpu-sample-heads", type=int, default=0,
                     help="(b, h) pairs in the oracle sample (0: about 10 s worth)")
     ap.add_argument("--variant", choices=["per_head", "full_fold", "layer"], default="per_head",
@@ -209,15 +226,53 @@ class ClockSampler:
 # the CUDA arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, world, rank, local):
+def step_algorithmic(w, lens):
+    """Bytes and FLOPs of one whole step (append of the B*n_q new tokens, then
+    the decode), counting each input once and each output once.
+
+    Bytes: the cache, the append's packed W_dkv||W_kr, W_uk and W_uv, the new
+    tokens' hidden states and cache rows, the queries and the fp32 output.
+    FLOPs: the attention's, plus the append (d_model x R per token), the
+    query absorption (d_c x d_nope per head and token) and the value
+    up-projection (d_c x d_v per head and token).
+    """
+    cache_bytes, attn_flops = algorithmic(w, lens)
+    eb = w.elem_bytes
+    Tq = w.batch * w.n_q
+    weight_bytes = (w.R * w.d_model + w.n_h * w.d_c * (w.d_nope + w.d_v)) * eb
+    act_bytes = Tq * (w.d_model + w.R + w.n_h * (w.d_nope + w.d_r)) * eb + Tq * w.n_h * w.d_v * 4
+    flops = attn_flops + 2.0 * Tq * (w.d_model * w.R + w.n_h * w.d_c * (w.d_nope + w.d_v))
+    return cache_bytes + weight_bytes + act_bytes, flops
+
+
+def roofline_entry(nbytes, flops, ms, hbm, tflops):
+    """Roofline of work that moves nbytes and does flops in ms: the slower of
+    the bytes at the HBM peak and the FLOPs at the bf16 peak."""
+    t_mem = nbytes / (hbm * 1e9)
+    t_ten = flops / (tflops * 1e12)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    if t_mem >= t_ten:
+        e = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+             "frac": round(gbs / hbm, 4)}
+    else:
+        e = {"bound": "tensor", "achieved": round(tfs, 1), "peak": tflops, "unit": "TFLOP/s",
+             "frac": round(tfs / tflops, 4)}
+    e["roofline_ms"] = round(max(t_mem, t_ten) * 1e3, 5)
+    e["gbs"] = round(gbs, 1)
+    e["tflops"] = round(tfs, 1)
+    return e
+
+
+def measure_workload(args, w, K, warmup, world, rank, local, dist, headline, min_steps=1):
+    """Time one workload's whole step (append + absorb + attention + combine)
+    from CUDA graphs over rotating input sets. Returns a dict; the headline
+    workload also gets the clock record, the end-to-end figures and the
+    host enqueue cost."""
     import torch
     from mla_latent_kv_73_b300 import _lib, synth
     from mla_latent_kv_73_b300.device_inputs import DeviceWeights, config_for, to_device
 
-    torch.cuda.set_device(local)
-    dist = init_dist(world, "nccl")
-    _lib.load()
-    w = synth.WORKLOADS[args.workload]
     lens = synth.seq_lens(w)
     B, n_q = w.batch, w.n_q
     Tq = B * n_q
@@ -227,31 +282,36 @@ def run_ours(args, world, rank, local):
     pt_np, num_blocks = synth.page_table(w, lens)
     max_blocks = pt_np.shape[1]
     cache_bytes, attn_flops = algorithmic(w, lens)
+    step_bytes, step_flops = step_algorithmic(w, lens)
 
-    # input sets: one per simulated layer
+    # input sets: one per simulated layer, together more than 3x L2
     wts = synth.weights(w)
     set_bytes = cache_bytes + (w.R * w.d_model + 2 * w.n_h * w.d_c * w.d_nope) * w.elem_bytes
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     n_sets = max(2, math.ceil(3 * l2 / set_bytes))
     gen = torch.Generator(device="cuda")
-    gen.manual_seed(1000 + rank)
+    gen.manual_seed(1000 + 17 * rank + w.seed)
     sets = []
     for k in range(n_sets):
         s = {}
         s["w"] = DeviceWeights(w, wts, cfg)
-        s["cache"] = torch.randn((num_blocks, w.block_size, w.R), generator=gen, device="cuda").to(dt)
+        s["cache"] = torch.randn((num_blocks, w.block_size, w.R), generator=gen,
+                                 device="cuda").to(dt)
         s["pt"] = to_device(pt_np, "i32")
         s["x"] = torch.randn((Tq, w.d_model), generator=gen, device="cuda").to(dt)
-        s["q"] = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen, device="cuda").to(dt)
+        s["q"] = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen,
+                             device="cuda").to(dt)
         s["sl"] = to_device(lens, "i32")  # per-set copies for the pipelined end-to-end run
         s["out"] = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
         sets.append(s)
     seq_lens = to_device(lens, "i32")
     seq_idx = to_device(np.repeat(np.arange(B), n_q).astype(np.int32), "i32")
-    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32), "i32")
+    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32),
+                    "i32")
     out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
     ws = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q, int(lens.sum())),
                      dtype=torch.uint8, device="cuda")
+
     def step(s, st):
         _lib.mla_append_kv(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], st)
         _lib.mla_decode_absorb_q(cfg, s["w"].handle, s["q"], seq_lens, max_blocks, ws, st)
@@ -259,31 +319,15 @@ def run_ours(args, world, rank, local):
         _lib.mla_decode_combine(cfg, s["w"].handle, seq_lens, B, n_q, out, ws, st)
 
     stream = torch.cuda.current_stream()
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(sets[i % n_sets], stream)
     torch.cuda.synchronize()
     st, code = _lib.mla_get_last_device_error(stream)
     if code:
-        raise RuntimeError(f"device error word {code:#x} after warm-up")
+        raise RuntimeError(f"{w.name}: device error word {code:#x} after warm-up")
 
-    # pinned host buffers for the end-to-end measurement
-    pin_x = torch.empty((Tq, w.d_model), dtype=dt, pin_memory=True)
-    pin_q = torch.empty((B, n_q, w.n_h, w.d_nope + w.d_r), dtype=dt, pin_memory=True)
-    pin_lens = torch.from_numpy(lens.astype(np.int32)).pin_memory()
-    pin_out = torch.empty((B, n_q, w.n_h, w.d_v), pin_memory=True)
-    pin_x.copy_(sets[0]["x"].cpu())
-    pin_q.copy_(sets[0]["q"].cpu())
-
-    def e2e_step(s, st):
-        s["x"].copy_(pin_x, non_blocking=True)
-        s["q"].copy_(pin_q, non_blocking=True)
-        seq_lens.copy_(pin_lens, non_blocking=True)
-        step(s, st)
-        pin_out.copy_(out, non_blocking=True)
-
-    # One CUDA graph per input set: a whole step; the attention kernel alone
-    # (the roofline kernel); a whole step with its host<->device copies; and
-    # a whole step with timing events between its four stages.
+    # One CUDA graph per input set: a whole step; the attention kernel alone;
+    # and a whole step with timing events between its four stages.
     n_stage_ev = 8
     stage_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
                 for _ in range(n_sets * n_stage_ev)]
@@ -299,7 +343,7 @@ def run_ours(args, world, rank, local):
         _lib.mla_decode_combine(cfg, s["w"].handle, seq_lens, B, n_q, out, ws, st)
         ev[4].record(st)
 
-    g_step, g_att, g_e2e, g_prof = [], [], [], []
+    g_step, g_att, g_prof = [], [], []
     for k in range(n_sets * n_stage_ev):
         s = sets[k % n_sets]
         g = torch.cuda.CUDAGraph()
@@ -309,8 +353,7 @@ def run_ours(args, world, rank, local):
     for s in sets:
         for lst, fn in ((g_step, lambda st, s=s: step(s, st)),
                         (g_att, lambda st, s=s: _lib.mla_decode_attend(
-                            cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, st)),
-                        (g_e2e, lambda st, s=s: e2e_step(s, st))):
+                            cfg, s["cache"], s["pt"], seq_lens, B, n_q, ws, st))):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn(torch.cuda.current_stream())
@@ -320,10 +363,19 @@ def run_ours(args, world, rank, local):
         g_att[i % n_sets].replay()
     torch.cuda.synchronize()
 
-    K = args.steps
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    if K is None:
+        t0.record()
+        for i in range(4 * n_sets):
+            g_step[i % n_sets].replay()
+        t1.record()
+        torch.cuda.synchronize()
+        est = t0.elapsed_time(t1) / (4 * n_sets)
+        K = int(min(3000, max(min_steps, 300.0 / max(est, 1e-3))))
+        K = int(max_over_ranks(K, dist, "cuda"))
+    clk = ClockSampler(local) if headline else contextlib.nullcontext()
+    with clk:
         barrier(dist)
         torch.cuda.synchronize()
         wall0 = time.time()
@@ -336,16 +388,16 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier(dist)
         wall1 = time.time()
-    clocks = clk.summary(wall0, wall1)
+    clocks = clk.summary(wall0, wall1) if headline else None
     total_ms = t0.elapsed_time(t1)
     st, code = _lib.mla_get_last_device_error(stream)
     if code:
-        raise RuntimeError(f"device error word {code:#x} in the timed region")
+        raise RuntimeError(f"{w.name}: device error word {code:#x} in the timed region")
     value, total_ms_max = whole_job_rate(Tq * K, total_ms, dist, "cuda")
     ms_per_step = total_ms_max / K
 
     # the attention kernel, launch by launch (each launch on a cold input set)
-    Ka = min(K, 2000)
+    Ka = min(max(K, 50), 2000)
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(Ka)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(Ka)]
     torch.cuda.synchronize()
@@ -370,11 +422,75 @@ def run_ours(args, world, rank, local):
             for j, n in enumerate(names):
                 acc[n].append(ev[j].elapsed_time(ev[j + 1]))
     stages = {n: round(1e3 * statistics.mean(v), 2) for n, v in acc.items()}
-    stages["note"] = "us per stage inside whole-step graph replays, cold input sets"
     stages["attend_alone"] = round(1e3 * statistics.mean(attend_ms), 2)
 
+    hbm, tflops, tflops_sus, src = measured_peaks()
+    # the attention kernel's time inside whole-step graphs (events on the
+    # launching stream around its node)
+    att_ms = statistics.mean(acc["attend"])
+    att = roofline_entry(cache_bytes, attn_flops, att_ms, hbm, tflops)
+    att["kernel"] = "attend_tc_kernel" if impl == 2 else "attend_simt_kernel"
+    att["kernel_ms"] = round(att_ms, 5)
+    step_roof = roofline_entry(step_bytes, step_flops, ms_per_step, hbm, tflops)
+    step_roof["bytes"] = int(step_bytes)
+    step_roof["flops"] = float(step_flops)
+    step_roof["what"] = ("whole step (append + absorb + attention + combine): cache + "
+                         "W_dkv||W_kr + W_uk + W_uv + x + new rows + q + out")
+    res = {
+        "workload": w.name, "value": value, "ms_per_step": ms_per_step, "steps": K,
+        "tokens_per_s": round(value, 1),
+        "cache_gbs": round(cache_bytes * K / (total_ms_max / 1e3) / 1e9, 1),
+        "cache_bytes": int(cache_bytes), "attention_flops": float(attn_flops),
+        "attention_roofline": att, "step_roofline": step_roof, "stage_us": stages,
+        "impl": impl, "peak_source": src, "lens": lens, "n_sets": n_sets,
+        "set_bytes": set_bytes, "l2": l2, "clocks": clocks, "host_us": host_us,
+    }
 
-    # end to end: pinned host inputs in, host result out, every step
+    if headline:
+        res["e2e"] = e2e_figures(w, lens, sets, n_sets, K, step, seq_lens, seq_idx, pos, out,
+                                 max_blocks, cfg, ws, dist, stream)
+    for s in sets:
+        s["w"].free()
+    del sets, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e_figures(w, lens, sets, n_sets, K, step, seq_lens, seq_idx, pos, out, max_blocks, cfg,
+                ws, dist, stream):
+    """The same step through the C ABI with its inputs copied up from pinned
+    host memory and its result read back, every step, inside the timed
+    region: serial (one stream), pipelined (copies on two side streams while
+    the previous step computes) and issued call by call from Python."""
+    import torch
+    from mla_latent_kv_73_b300 import _lib
+    B, n_q = w.batch, w.n_q
+    Tq = B * n_q
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pin_x = torch.empty((Tq, w.d_model), dtype=dt, pin_memory=True)
+    pin_q = torch.empty((B, n_q, w.n_h, w.d_nope + w.d_r), dtype=dt, pin_memory=True)
+    pin_lens = torch.from_numpy(lens.astype(np.int32)).pin_memory()
+    pin_out = torch.empty((B, n_q, w.n_h, w.d_v), pin_memory=True)
+    pin_x.copy_(sets[0]["x"].cpu())
+    pin_q.copy_(sets[0]["q"].cpu())
+
+    def e2e_step(s, st):
+        s["x"].copy_(pin_x, non_blocking=True)
+        s["q"].copy_(pin_q, non_blocking=True)
+        seq_lens.copy_(pin_lens, non_blocking=True)
+        step(s, st)
+        pin_out.copy_(out, non_blocking=True)
+
+    g_e2e = []
+    for s in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_step(s, torch.cuda.current_stream())
+        g_e2e.append(g)
+    for i in range(2 * n_sets):
+        g_e2e[i % n_sets].replay()
+    torch.cuda.synchronize()
     Ke = max(n_sets, K // 2)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -390,13 +506,13 @@ def run_ours(args, world, rank, local):
     h2d = pin_x.numel() * pin_x.element_size() + pin_q.numel() * pin_q.element_size() + \
         pin_lens.numel() * 4
     d2h = pin_out.numel() * 4
-    # the same steps pipelined: step i+1's inputs go up on one copy stream and
-    # step i's result comes down on another while step i computes. Each step
-    # still uploads its own inputs and reads back its own result; a graph of
-    # 8 * n_sets steps (long, so that the pipeline's fill and drain at the
-    # graph's ends are amortised) holds the copies, the steps and the
-    # cross-stream dependencies (a set's inputs are overwritten only after
-    # the step that read them, its output only after its read-back).
+
+    # Pipelined: step i+1's inputs go up on one copy stream and step i's
+    # result comes down on another while step i computes. Each step still
+    # uploads its own inputs and reads back its own result; a graph of
+    # 8 * n_sets steps holds the copies, the steps and the cross-stream
+    # dependencies (a set's inputs are overwritten only after the step that
+    # read them, its output only after its read-back).
     def step_io(s, st):
         _lib.mla_append_kv(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"], st)
         _lib.mla_decode_absorb_q(cfg, s["w"].handle, s["q"], s["sl"], max_blocks, ws, st)
@@ -458,70 +574,91 @@ def run_ours(args, world, rank, local):
     e1.record()
     torch.cuda.synchronize()
     e2e_direct = Tq * Kd / (e0.elapsed_time(e1) / 1e3)
+    return {"value": round(pipe_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": P * Rp, "graph": True,
+            "pipelined": "inputs of step i+1 up and result of step i down on two copy "
+                         "streams while step i computes",
+            "serial_value": round(e2e_value, 1), "serial_steps": Ke,
+            "no_graph_value": round(e2e_direct, 1)}
 
-    # roofline of the dominant kernel (attention), per launch
-    hbm, tflops, tflops_sus, src = measured_peaks()
-    # the attention kernel's time inside whole-step graphs (events on the
-    # launching stream around its node); the standalone single-kernel replay
-    # above also pays a graph launch and is reported beside it
-    att_ms = statistics.mean(acc["attend"])
-    achieved_gbs = cache_bytes / (att_ms / 1e3) / 1e9
-    tensor_tflops = attn_flops / (att_ms / 1e3) / 1e12
-    t_mem = cache_bytes / (hbm * 1e9)
-    t_ten = attn_flops / (tflops * 1e12)
-    bound = "hbm" if t_mem >= t_ten else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(tensor_tflops, 1), "peak": tflops,
-                "unit": "TFLOP/s", "frac": round(tensor_tflops / tflops, 4)}
-    roof["traffic"] = profiled_traffic(args.workload)
-    roof["peak_source"] = src
-    roof["kernel"] = "attend_tc_kernel" if impl == 2 else "attend_simt_kernel"
-    roof["kernel_ms"] = round(att_ms, 5)
-    roof["roofline_ms"] = round(max(t_mem, t_ten) * 1e3, 5)
-    roof["frac_of_roofline_time"] = round(max(t_mem, t_ten) * 1e3 / att_ms, 4)
-    roof["tensor_tflops"] = round(tensor_tflops, 1)
 
+def per_config_row(r):
+    a, s = r["attention_roofline"], r["step_roofline"]
+    return {"tokens_per_s": r["tokens_per_s"], "ms_per_step": round(r["ms_per_step"], 5),
+            "steps": r["steps"], "cache_gbs": r["cache_gbs"],
+            "attention": {k: a[k] for k in ("bound", "achieved", "unit", "frac", "kernel_ms",
+                                            "roofline_ms", "gbs", "tflops")},
+            "step": {k: s[k] for k in ("bound", "achieved", "unit", "frac", "roofline_ms",
+                                       "gbs", "tflops")},
+            "stage_us": r["stage_us"]}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from mla_latent_kv_73_b300 import _lib, synth
+
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    _lib.load()
+    head = synth.WORKLOADS[args.workload]
+    others = [] if args.only else [n for n in PER_CONFIG if n != head.name]
+    K = args.steps
+    r = measure_workload(args, head, K, args.warmup, world, rank, local, dist, headline=True)
+    rows = {head.name: per_config_row(r)} if head.dtype == "bf16" else {}
+    for name in others:
+        # K steps, or about 0.3 s of them if that is more (K=None: chosen
+        # from a short probe after the warm-up)
+        rc = measure_workload(args, synth.WORKLOADS[name], None, args.warmup, world, rank,
+                              local, dist, headline=False, min_steps=K)
+        rows[name] = per_config_row(rc)
+
+    w = head
+    lens = r["lens"]
+    att = dict(r["attention_roofline"])
+    roof = {k: att[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roof["traffic"] = profiled_traffic(w.name)
+    roof["peak_source"] = r["peak_source"]
+    roof["kernel"] = att["kernel"]
+    roof["kernel_ms"] = att["kernel_ms"]
+    roof["roofline_ms"] = att["roofline_ms"]
+    roof["what"] = "attention kernel only (a3): the latent cache against HBM, its FLOPs " \
+                   "against the bf16 tensor peak"
+    roof["tensor_tflops"] = att["tflops"]
     line = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": round(r["value"], 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5),
+        "ms_per_step": round(r["ms_per_step"], 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) cache rows, hidden states and queries; "
                 "N(0,1/fan_in) weights)",
-        "config": {"workload": w.name, "batch": B, "seq_len": int(lens[0]) if w.len_lo == w.len_hi
-                   else [w.len_lo, w.len_hi], "n_q": n_q, "n_h": w.n_h, "d_model": w.d_model,
-                   "d_c": w.d_c, "d_r": w.d_r, "block_size": w.block_size,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"{n_sets} rotating layer-sized input sets, "
-                         f"{n_sets * set_bytes / 2**20:.0f} MiB > 3x L2 ({l2 / 2**20:.0f} MiB)",
-                   "decode_kernel": "tensor_core" if impl == 2 else "cuda_core"},
-        "cache_gbs": round(cache_bytes * K / (total_ms_max / 1e3) / 1e9, 1),
+        "config": {"workload": w.name, "batch": w.batch,
+                   "seq_len": int(lens[0]) if w.len_lo == w.len_hi else [w.len_lo, w.len_hi],
+                   "total_cached_tokens": int(np.sum(lens)), "n_q": w.n_q, "n_h": w.n_h,
+                   "d_model": w.d_model, "d_c": w.d_c, "d_r": w.d_r,
+                   "block_size": w.block_size, "parallelism": f"replicas x{world}",
+                   "l2": f"{r['n_sets']} rotating layer-sized input sets, "
+                         f"{r['n_sets'] * r['set_bytes'] / 2**20:.0f} MiB > 3x L2 "
+                         f"({r['l2'] / 2**20:.0f} MiB)",
+                   "decode_kernel": "tensor_core" if r["impl"] == 2 else "cuda_core"},
+        "cache_gbs": r["cache_gbs"],
         "roofline": roof,
-        "e2e": {"value": round(pipe_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": P * Rp, "graph": True,
-                "pipelined": "inputs of step i+1 up and result of step i down on two copy "
-                             "streams while step i computes",
-                "serial_value": round(e2e_value, 1), "serial_steps": Ke,
-                "no_graph_value": round(e2e_direct, 1)},
+        "step_roofline": r["step_roofline"],
+        "per_config": rows,
+        "e2e": r["e2e"],
         "gpu_launches": 4 * K,
-        "stage_us": stages,
-        "host_enqueue_us_per_step": round(host_us, 2),
-        "clocks": clocks,
+        "stage_us": r["stage_us"],
+        "host_enqueue_us_per_step": round(r["host_us"], 2),
+        "clocks": r["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, lens, args.cpu_sample_heads)
-    for s in sets:
-        s["w"].free()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -871,8 +1008,23 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def self_launch(n, argv):
+    """Run this script on n local ranks through torch.distributed.run (one
+    process per GPU, rendezvous on 127.0.0.1). Returns its exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
 def main():
     args = parse()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(self_launch(args.gpus, sys.argv[1:]))
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)

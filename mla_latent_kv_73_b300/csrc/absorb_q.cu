@@ -10,6 +10,10 @@
 // block is rotated, per query position ("Multi-head Latent Attention: the
 // KV cache, compressed", section "RoPE, and why the explanations stop here").
 //
+// The queries are stored in the cache dtype for the tensor-core attention
+// (its MMA operands) and in fp32 for the CUDA-core attention, which then
+// keeps every score in fp32 from the query on.
+//
 // One CTA per (head, tile of 16 query tokens). It streams that head's
 // [d_c x d_nope] slice of W_uk once with 16-byte loads. Each thread owns two
 // latent rows and all 16 tokens, so every weight element is read once.
@@ -25,12 +29,12 @@ namespace {
 
 constexpr int AQ_TOK = 16, AQ_THREADS = 256;
 
-template <typename T>
+template <typename T, typename QT>
 __global__ void __launch_bounds__(AQ_THREADS)
 absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
                 const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
                 int n_q, int max_blocks, int TS, int G, int C, int K, float out_scale,
-                T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
+                QT* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
                 int32_t* first_b, uint32_t* err) {
   extern __shared__ __align__(16) float qn[];  // [d_nope][AQ_TOK], token fastest
   const int h = blockIdx.x;
@@ -95,9 +99,9 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
       }
     }
     for (int t = 0; t < ntok; ++t) {
-      T* o = qabs + (static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc0;
-      o[0] = from_f32<T>(acc0[t] * out_scale);
-      if (two) o[1] = from_f32<T>(acc1[t] * out_scale);
+      QT* o = qabs + (static_cast<size_t>(tok0 + t) * s.n_h + h) * R + dc0;
+      o[0] = from_f32<QT>(acc0[t] * out_scale);
+      if (two) o[1] = from_f32<QT>(acc1[t] * out_scale);
     }
   }
 
@@ -111,13 +115,13 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
     const float x1 = to_f32<T>(qr[k]), x2 = to_f32<T>(qr[k + half]);
     float c, sn;
     rope_cos_sin(pos, inv_freq[k], &c, &sn);
-    T* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
-    o[k] = from_f32<T>((x1 * c - x2 * sn) * out_scale);
-    o[k + half] = from_f32<T>((x1 * sn + x2 * c) * out_scale);
+    QT* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
+    o[k] = from_f32<QT>((x1 * c - x2 * sn) * out_scale);
+    o[k + half] = from_f32<QT>((x1 * sn + x2 * c) * out_scale);
   }
 }
 
-template <typename T>
+template <typename T, typename QT>
 cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const int32_t* seq_lens,
                        int max_blocks, int B, int n_q, const Partition& p, const WsView& ws,
                        float out_scale, uint32_t* err, cudaStream_t st) {
@@ -125,14 +129,14 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
   dim3 grid(s.n_h, (Tq + AQ_TOK - 1) / AQ_TOK);
   const size_t smem = sizeof(float) * AQ_TOK * s.d_nope;  // up to 64 KB (d_nope <= 1024)
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(absorb_q_kernel<T>,
+    cudaError_t e = cudaFuncSetAttribute(absorb_q_kernel<T, QT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  absorb_q_kernel<T><<<grid, AQ_THREADS, smem, st>>>(
+  absorb_q_kernel<T, QT><<<grid, AQ_THREADS, smem, st>>>(
       s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
-      max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<T*>(ws.qabs), ws.tiles, ws.prefix,
+      max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<QT*>(ws.qabs), ws.tiles, ws.prefix,
       ws.bounds, ws.first_b, err);
   return cudaGetLastError();
 }
@@ -141,12 +145,16 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
 
 cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
                             const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                            const Partition& p, const WsView& ws, float out_scale, uint32_t* err,
-                            cudaStream_t st) {
+                            const Partition& p, const WsView& ws, float out_scale, bool q_f32,
+                            uint32_t* err, cudaStream_t st) {
   if (dt == MLA_F32)
-    return absorb_q_t<float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err, st);
-  return absorb_q_t<__nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err,
-                                   st);
+    return absorb_q_t<float, float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err,
+                                    st);
+  if (q_f32)
+    return absorb_q_t<__nv_bfloat16, float>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws,
+                                            out_scale, err, st);
+  return absorb_q_t<__nv_bfloat16, __nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws,
+                                                  out_scale, err, st);
 }
 
 }  // namespace mla

@@ -125,7 +125,8 @@ mla_status make_plan(const mla_config* cfg, int B, int n_q, const DeviceInfo* di
   out->s = shape_of(cfg);
   out->impl = impl;
   out->part = partition_for(impl, out->s, B, n_q, di->sms, di->tc_pairs);
-  out->lay = ws_layout(out->s, dtype_bytes(cfg->dtype), B, n_q, out->part);
+  out->lay = ws_layout(out->s, impl == MLA_IMPL_CUDA_CORE ? 4 : dtype_bytes(cfg->dtype), B, n_q,
+                       out->part);
   return MLA_OK;
 }
 
@@ -160,11 +161,11 @@ Partition partition_for(int impl, const Shape& s, int B, int n_q, int num_sms, i
   return p;
 }
 
-WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p) {
+WsLayout ws_layout(const Shape& s, int q_bytes, int B, int n_q, const Partition& p) {
   WsLayout l;
   size_t off = 0;
   l.qabs = off;
-  off = align256(off + static_cast<size_t>(B) * n_q * s.n_h * s.R() * dtype_bytes);
+  off = align256(off + static_cast<size_t>(B) * n_q * s.n_h * s.R() * q_bytes);
   l.tiles = off;
   off = align256(off + sizeof(int32_t) * B);
   l.prefix = off;
@@ -423,7 +424,8 @@ mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void*
     return from_cuda(launch_absorb_q_tc(p.s, &w->w, q, seq_lens, max_blocks, B, n_q, p.part, v,
                                         out_scale, di->err, stream));
   return from_cuda(launch_absorb_q(p.s, cfg->dtype, &w->w, q, seq_lens, max_blocks, B, n_q,
-                                   p.part, v, out_scale, di->err, stream));
+                                   p.part, v, out_scale, p.impl == MLA_IMPL_CUDA_CORE, di->err,
+                                   stream));
 }
 
 mla_status mla_decode_attend(const mla_config* cfg, const void* cache, int32_t num_blocks,
@@ -594,7 +596,7 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
       p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (e == cudaSuccess)
     e = launch_q_finish(p.s, cfg->dtype, fw->w.inv_freq, proj, seq_lens, max_blocks, B, n_q,
-                        p.part, v, out_scale, di->err, stream);
+                        p.part, v, out_scale, p.impl == MLA_IMPL_CUDA_CORE, di->err, stream);
   // 2. split-KV latent attention, the same kernels as mla_decode
   if (e == cudaSuccess) {
     if (p.impl == MLA_IMPL_TENSOR_CORE)

@@ -10,7 +10,10 @@
 // "DeepSeek V3 Multi-Head Latent Attention (MLA): How It Slashes KV Cache
 // Memory", section "Low-Rank Key-Value Joint Compression".
 //
-// Three kernels share one epilogue:
+// bf16 appends run on the tensor cores (append_tc_kernel below, a split-K
+// tcgen05 GEMM of up to 256 tokens per launch; longer bulk fills are
+// consecutive launches). The CUDA-core kernels take fp32 and the shapes the
+// tensor-core kernel does not; three of them share one epilogue:
 //  * append_staged_kernel for decode-sized T (up to 256 tokens). The weight
 //    read (d_model x R) dominates. Each CTA owns 4 packed columns. One thread
 //    bulk-copies their d_model weights and the first 16 tokens' hidden states
@@ -339,6 +342,7 @@ append_gemm_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
 // rotary pairs (adjacent rows of the packed weight) and writes the cache
 // entries.
 constexpr int AT_THREADS = 128;
+constexpr int AT_MAX_TOK = 256;  // tokens per launch (the MMA N of one CTA)
 constexpr uint32_t AT_WBOX = 128 * 128;  // 128 rows x 64 bf16
 constexpr long long AT_WAIT = 2000000000LL;
 
@@ -511,7 +515,7 @@ bool append_tc_clusters_ok(int kcn, size_t smem) {
 // does not apply (for diagnostics).
 int append_tc_cluster_size(const Shape& s, int T, int* nkb_out, size_t* smem_out) {
   const int N = ((T + 15) / 16) * 16;
-  if (T < 1 || N > 256 || s.d_c % 2 != 0) return 0;
+  if (T < 1 || N > AT_MAX_TOK || s.d_c % 2 != 0) return 0;
   for (int kcn : {16, 8}) {
     if (s.d_model % (kcn * 64) != 0) continue;
     const int nkb = s.d_model / (kcn * 64);
@@ -583,11 +587,34 @@ template <typename T>
 cudaError_t append_t(const Shape& s, const Weights* w, const void* x, AppendArgs a, void* cache,
                      cudaStream_t st) {
   const int R = s.R();
+  const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0;
   if constexpr (sizeof(T) == 2) {
     cudaError_t e = cudaSuccess;
-    if (launch_append_tc(s, w, x, a, cache, st, &e)) return e;
+    if (a.T <= AT_MAX_TOK) {
+      if (launch_append_tc(s, w, x, a, cache, st, &e)) return e;
+    } else {
+      // Bulk fill on the tensor cores: consecutive launches of at most
+      // AT_MAX_TOK tokens each (every launch waits for the one before it,
+      // so the calls write in token order). The weight slice of each launch
+      // is read from L2 after the first.
+      int nkb = 0;
+      size_t smem = 0;
+      const int tail = a.T % AT_MAX_TOK;
+      if (aligned && append_tc_cluster_size(s, AT_MAX_TOK, &nkb, &smem) != 0 &&
+          (tail == 0 || append_tc_cluster_size(s, tail, &nkb, &smem) != 0)) {
+        for (int off = 0; off < a.T; off += AT_MAX_TOK) {
+          AppendArgs c = a;
+          c.seq_idx += off;
+          c.pos += off;
+          c.T = min(AT_MAX_TOK, a.T - off);
+          const T* xc = static_cast<const T*>(x) + static_cast<size_t>(off) * s.d_model;
+          if (!launch_append_tc(s, w, xc, c, cache, st, &e)) return cudaErrorInvalidValue;
+          if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+      }
+    }
   }
-  const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0;
   const size_t staged_smem = sizeof(T) * static_cast<size_t>(ST_COLS + ST_TOK) * s.d_model;
   if (a.T <= 256 && aligned && s.d_model % Vec<T>::N == 0 && staged_smem <= 200 * 1024) {
     static int attr_bytes[64] = {};

@@ -29,7 +29,7 @@ template <typename T>
 __global__ void __launch_bounds__(SG_THREADS)
 attend_simt_kernel(Shape s, const T* __restrict__ cache, int num_blocks,
                    const int32_t* __restrict__ page_table, int max_blocks, int B, int n_q,
-                   Partition p, const T* __restrict__ qabs, const int32_t* __restrict__ tiles,
+                   Partition p, const float* __restrict__ qabs, const int32_t* __restrict__ tiles,
                    const int32_t* __restrict__ prefix, const long long* __restrict__ bounds,
                    const int32_t* __restrict__ seq_lens, float* __restrict__ part_o,
                    float* __restrict__ part_lse, uint32_t* err) {
@@ -70,7 +70,7 @@ attend_simt_kernel(Shape s, const T* __restrict__ cache, int num_blocks,
     for (int i = tid; i < SG_ROWS * R; i += SG_THREADS) {
       const int rr = i / R, k = i % R, rg = g * SG_ROWS + rr;
       qs[rr * RP + k] = rg < rows_total
-                            ? to_f32<T>(qabs[(static_cast<size_t>(b) * rows_total + rg) * R + k])
+                            ? qabs[(static_cast<size_t>(b) * rows_total + rg) * R + k]
                             : 0.f;
     }
     const int rg = g * SG_ROWS + r;
@@ -164,7 +164,7 @@ cudaError_t attend_simt_t(const Shape& s, const void* cache, int num_blocks,
     if (e != cudaSuccess) return e;
   }
   kern<<<p.C, SG_THREADS, smem, st>>>(s, static_cast<const T*>(cache), num_blocks, page_table,
-                                      max_blocks, B, n_q, p, static_cast<const T*>(ws.qabs),
+                                      max_blocks, B, n_q, p, static_cast<const float*>(ws.qabs),
                                       ws.tiles, ws.prefix, ws.bounds, seq_lens, ws.part_o, ws.part_lse, err);
   return cudaGetLastError();
 }

@@ -313,7 +313,8 @@ sum_splits_kernel(const float* __restrict__ part, int S, size_t n, float* __rest
   }
 }
 
-// qabs[t, h] = out_scale * [q_lat | RoPE(q_rope, pos_t)] in T, from the fp32
+// qabs[t, h] = out_scale * [q_lat | RoPE(q_rope, pos_t)] in T (fp32 for the
+// CUDA-core attention, the cache dtype for the tensor-core one), from the fp32
 // projection qpre[t][h*R + n]. One block per (token, QF_HEADS heads), so
 // that each thread has only a few elements and the grid covers the SMs.
 // Block 0 also writes the split-KV plan.
@@ -543,8 +544,8 @@ cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, cons
 cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,
-                            uint32_t* err, cudaStream_t st) {
-  if (dt == MLA_F32)
+                            bool q_f32, uint32_t* err, cudaStream_t st) {
+  if (dt == MLA_F32 || q_f32)
     return q_finish_t<float>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws, out_scale,
                              err, st);
   return q_finish_t<__nv_bfloat16>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws,

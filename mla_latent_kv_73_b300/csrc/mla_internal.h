@@ -51,7 +51,9 @@ struct WsLayout {
   size_t qabs, tiles, prefix, bounds, first_b, part_o, part_lse, total;
 };
 
-WsLayout ws_layout(const Shape& s, int dtype_bytes, int B, int n_q, const Partition& p);
+// q_bytes: bytes per stored query element (4 for the CUDA-core attention,
+// the cache dtype's size for the tensor-core one).
+WsLayout ws_layout(const Shape& s, int q_bytes, int B, int n_q, const Partition& p);
 WsView ws_view(void* base, const WsLayout& l);
 
 // Library-owned packed weights.
@@ -92,12 +94,13 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st);
 
-// out_scale multiplies q_lat and q_pe before they are rounded to the cache
-// dtype (the tensor-core attention folds scale * log2(e) in here).
+// out_scale multiplies q_lat and q_pe before they are stored (the
+// tensor-core attention folds scale * log2(e) in here). q_f32: store them in
+// fp32 (the CUDA-core attention's queries), else in the cache dtype.
 cudaError_t launch_absorb_q(const Shape& s, mla_dtype dt, const Weights* w, const void* q,
                             const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                            const Partition& p, const WsView& ws, float out_scale, uint32_t* err,
-                            cudaStream_t st);
+                            const Partition& p, const WsView& ws, float out_scale, bool q_f32,
+                            uint32_t* err, cudaStream_t st);
 
 cudaError_t launch_attend_simt(const Shape& s, mla_dtype dt, const void* cache, int num_blocks,
                                const int32_t* page_table, int max_blocks, int B, int n_q,
@@ -151,7 +154,7 @@ cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, mla_dtype w_d
 cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,
-                            uint32_t* err, cudaStream_t st);
+                            bool q_f32, uint32_t* err, cudaStream_t st);
 cudaError_t launch_combine_latent(const Shape& s, int B, int n_q, const Partition& p,
                                   const WsView& ws, float* olat, cudaStream_t st);
 

@@ -49,3 +49,27 @@ def test_ragged_workloads_by_brute_force():
                 vis += int(L) - w.n_q + i + 1
         assert cache_bytes == rows * w.R * 2
         assert flops == 2.0 * w.n_h * (w.R + w.d_c) * vis
+
+
+def test_whole_step_bytes_and_flops():
+    """The whole step's roofline counts every input and output once: the
+    cache, the append's W_dkv||W_kr, W_uk and W_uv (bf16), the new tokens'
+    hidden states and rows, the queries, and the fp32 output."""
+    w = synth.WORKLOADS["dsv2_b16_l4096"]
+    lens = synth.seq_lens(w)
+    nbytes, flops = bench.step_algorithmic(w, lens)
+    tensors = {
+        "cache": 16 * 4096 * 576 * 2,
+        "W_dkv||W_kr": 5120 * 576 * 2,
+        "W_uk": 512 * 128 * 128 * 2,
+        "W_uv": 512 * 128 * 128 * 2,
+        "x": 16 * 5120 * 2,
+        "new rows": 16 * 576 * 2,
+        "q": 16 * 128 * 192 * 2,
+        "out": 16 * 128 * 128 * 4,
+    }
+    assert nbytes == sum(tensors.values()) == 116_967_424
+    _, attn = bench.algorithmic(w, lens)
+    assert flops == attn + 2 * 16 * (5120 * 576 + 128 * 512 * 128 * 2)
+    r = bench.roofline_entry(nbytes, flops, 0.0666, 6514.2, 1786.4)
+    assert r["bound"] == "hbm" and abs(r["frac"] - nbytes / 66.6e-6 / 6514.2e9) < 1e-4

@@ -78,3 +78,23 @@ def test_reference_arm_runs_on_rank_zero_only():
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(args, 2, 1) is None
     assert out.getvalue() == ""
+
+
+@pytest.mark.timeout(240)
+def test_gpus_flag_starts_one_process_per_rank():
+    """``bench.py --gpus 2`` outside torchrun starts two local ranks itself
+    (torch.distributed.run on 127.0.0.1); the reference arm, which needs no
+    GPU, then prints exactly one line, from rank 0, for the whole job."""
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, bench.__file__, "--gpus", "2", "--impl", "reference",
+                        "--workload", "tiny_fp32", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=220, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2

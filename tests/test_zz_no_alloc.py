@@ -60,7 +60,10 @@ def test_no_alloc_matches_decode_on_consecutive_calls():
                 _problem((200, 64), 2, seed=22),
                 _problem((2, 65, 130), 2, n_h=4, dtype="f32", seed=23, d_c=32, d_r=8, d_nope=16,
                          d_v=16)]
-    for p in problems:
+    first = None
+    # the first problem runs again last, after larger plans (more splits,
+    # more queries) have left their partials in the shared array
+    for k, p in enumerate(problems + problems[:1]):
         w = p["w"]
         shape = (w.batch, w.n_q, w.n_h, w.d_v)
         ref = torch.full(shape, float("nan"), device="cuda")
@@ -72,8 +75,53 @@ def test_no_alloc_matches_decode_on_consecutive_calls():
                                  got)
         torch.cuda.synchronize()
         _close(got.cpu().numpy(), ref.cpu().numpy(), w.dtype)
+        if k == 0:
+            first = got.cpu().numpy()
+        elif k == len(problems):
+            # the same problem gives the same bits, whatever came in between
+            assert np.array_equal(got.cpu().numpy(), first)
     for p in problems:
         p["dw"].free()
+
+
+def test_no_alloc_full_size_batch16():
+    """The DeepSeek-V2-shape batch of 16 x 4096 cached tokens fits the array;
+    two calls in a row match mla_decode."""
+    w = synth.WORKLOADS["dsv2_b16_l4096"]
+    cfg = config_for(w)
+    need = _lib.mla_decode_workspace_size(cfg, w.batch, w.n_q)
+    assert need <= _lib.MLA_NO_ALLOC_WORKSPACE_BYTES
+    lens = synth.seq_lens(w)
+    dw = DeviceWeights(w, synth.weights(w), cfg)
+    pt, nb = synth.page_table(w, lens)
+    store, _ = synth.fill_paged_cache(w, lens, pt, nb)
+    _, qs = synth.queries(w)
+    cache, ptd = to_device(store, w.dtype), to_device(pt, "i32")
+    sl, q = to_device(lens, "i32"), to_device(qs, w.dtype)
+    shape = (w.batch, w.n_q, w.n_h, w.d_v)
+    ref = torch.full(shape, float("nan"), device="cuda")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    _lib.mla_decode(cfg, dw.handle, q, cache, ptd, sl, ref, ws)
+    for _ in range(2):
+        got = torch.full(shape, float("nan"), device="cuda")
+        _lib.mla_decode_no_alloc(cfg, dw.handle, q, cache, ptd, sl, got)
+        torch.cuda.synchronize()
+        _close(got.cpu().numpy(), ref.cpu().numpy(), w.dtype)
+    dw.free()
+
+
+def test_no_alloc_fits_by_workload():
+    """Which of the benchmark workloads fit the fixed array: the fp32 tiny
+    one, DeepSeek-V2 batch 16 and batch 4 x 131072 (2 queries) do; batch 64
+    ragged and the 16-head batch of 256 need more scratch than the array
+    holds and get MLA_ERR_WORKSPACE from mla_decode_no_alloc."""
+    fits = {}
+    for name in synth.WORKLOAD_ORDER:
+        w = synth.WORKLOADS[name]
+        need = _lib.mla_decode_workspace_size(config_for(w), w.batch, w.n_q)
+        fits[name] = need <= _lib.MLA_NO_ALLOC_WORKSPACE_BYTES
+        print(f"{name}: decode workspace {need} B ({need / 2**20:.2f} MiB), fits: {fits[name]}")
+    assert fits["tiny_fp32"] and fits["dsv2_b16_l4096"]
 
 
 def test_no_alloc_rejects_requests_larger_than_its_array():
