@@ -223,7 +223,13 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
  *  - All calls on a device share the array. It keeps the previous call's
  *    contents, and nothing in it needs to start at zero. Calls whose GPU work
  *    overlaps (other streams, other host threads) race on it, so order them,
- *    for example by issuing them on one stream. */
+ *    for example by issuing them on one stream.
+ *  - The array's address is remembered per device for the life of the
+ *    process. Resetting a device (cudaDeviceReset) after the first call is
+ *    not supported: later calls on that device would use a stale address.
+ *  - On a B300 the DeepSeek-V2 shape (128 heads) fits with batch 16 (24.8
+ *    MiB) or batch 4 with 2 query tokens (21.7 MiB); batch 64 needs 43.6 MiB
+ *    and is rejected. The workspace does not depend on the cached lengths. */
 mla_status mla_decode_no_alloc(const mla_config* cfg, mla_weights w, const void* q,
                                const void* cache, int32_t num_blocks, const int32_t* page_table,
                                int32_t max_blocks, const int32_t* seq_lens, int32_t B,

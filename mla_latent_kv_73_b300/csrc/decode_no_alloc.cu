@@ -32,7 +32,9 @@ void* g_ws_ptr[kMaxDevices] = {};
 std::mutex g_ws_mu;
 
 // Device address of the array on the current device. The first call on a
-// device looks it up; later calls reuse it.
+// device looks it up; later calls reuse it for the life of the process (a
+// cudaDeviceReset in between is not supported: the remembered address
+// would belong to the destroyed context).
 mla_status workspace_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
