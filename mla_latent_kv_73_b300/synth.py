@@ -84,6 +84,13 @@ WORKLOADS = {
                                  len_lo=1024, len_hi=8192, dtype="bf16", seed=4),
 }
 
+# A prefill step (not one of the decode workloads): 512 new tokens per
+# sequence appended and attended in one call, at the end of 4096-token
+# sequences (the count includes the new tokens), DeepSeek-V2 shape.
+WORKLOADS["dsv2_prefill_b4_c512_l4096"] = Workload(
+    "dsv2_prefill_b4_c512_l4096", n_h=128, d_model=5120, d_c=512, d_r=64, d_nope=128, d_v=128,
+    batch=4, n_q=512, len_lo=4096, len_hi=4096, dtype="bf16", seed=5)
+
 WORKLOAD_ORDER = ["tiny_fp32", "dsv2_b16_l4096", "dsv2_b64_ragged",
                   "dsv2_b4_l131072_nq2", "nh16_b256_ragged"]
 

@@ -438,3 +438,65 @@ def test_full_size_peaked_softmax(wname, impl):
             assert np.all(np.isfinite(g_)) and rel <= bound and mab <= 4 * bound, \
                 f"{what} sample {k}: rel-L2 {rel:.3e} max-abs {mab:.3e} (bound {bound:.3e})"
     r.dw.free()
+
+
+# ---------------------------------------------------------------------------
+# Prefill chunks: many new tokens per sequence in one call
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("impl", list(IMPLS))
+@pytest.mark.parametrize("n_q", [64, 512])
+def test_prefill_chunk_end_to_end(n_q, impl):
+    """A prefill step: a chunk of n_q new tokens per sequence is appended
+    with one mla_append_kv call (their rows computed from hidden states) and
+    all of them are decoded in one mla_decode call, each new token seeing the
+    cached context and the chunk's tokens up to itself (causal inside the
+    chunk). Sequence 0 has 1000 tokens of earlier context; sequence 1 starts
+    from nothing, so its first new token sees only itself. Sampled outputs
+    against the oracle, which computes the chunk's rows itself (rounded once
+    to the cache dtype, as the cache stores them)."""
+    w = synth.Workload(f"prefill_{n_q}", n_h=128, d_model=1024, d_c=512, d_r=64, d_nope=128,
+                       d_v=128, batch=2, n_q=n_q, len_lo=0, len_hi=0, dtype="bf16", seed=40)
+    lens = np.array([1000 + n_q, n_q], dtype=np.int32)
+    cfg = config_for(w, IMPLS[impl])
+    wts = synth.weights(w)
+    dw = DeviceWeights(w, wts, cfg)
+    pt, nb = synth.page_table(w, lens, spare_blocks=1)
+    # earlier context of sequence 0: drawn rows; the chunk's rows come from append
+    ctx = synth.sequence_rows(w, 0, 1000)
+    store = np.full((nb * w.block_size, w.R), synth.round_bf16(np.float32([np.nan]))[1][0],
+                    dtype=np.uint16)
+    for j in range(1000):
+        store[O.paged_row_index(pt, 0, j, w.block_size)] = ctx[1][j]
+    cache = to_device(store.reshape(nb, w.block_size, w.R), "bf16")
+    T = int(2 * n_q)
+    xv, xs = synth.hidden_states(w, T, stream=7)
+    seq_idx = np.repeat(np.arange(2), n_q).astype(np.int32)
+    pos = np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32)
+    ptd = to_device(pt, "i32")
+    _lib.mla_append_kv(cfg, dw.handle, to_device(xs, "bf16"), to_device(seq_idx, "i32"),
+                       to_device(pos, "i32"), ptd, cache)
+    qv, qs = synth.queries(w)
+    out = torch.full((2, n_q, w.n_h, w.d_v), float("nan"), device="cuda")
+    ws = torch.empty(_lib.mla_decode_workspace_size(cfg, 2, n_q), dtype=torch.uint8,
+                     device="cuda")
+    _lib.mla_decode(cfg, dw.handle, to_device(qs, "bf16"), cache, ptd, to_device(lens, "i32"),
+                    out, ws)
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    new_rows = O.latent_rows(xv, wts.W_dkv, wts.W_kr, pos, w.rope_base)
+    new_rows = synth.round_bf16(new_rows.astype(np.float32))[0]
+    seq_rows = [np.concatenate([ctx[0], new_rows[:n_q]]), new_rows[n_q:]]
+    g = np.random.default_rng(n_q)
+    samples = [(b, i, h) for b in (0, 1) for i in sorted({0, 1, n_q // 2, n_q - 1,
+                                                          int(g.integers(0, n_q))})
+               for h in (0, int(g.integers(0, w.n_h)))]
+    ref = O.decode_materialised(qv, seq_rows, lens, wts.W_uk, wts.W_uv, w.d_c, w.d_nope, w.d_v,
+                                w.scale, w.rope_base, samples=samples)
+    check_bf16_each([got[s] for s in samples], [ref[s] for s in samples],
+                    f"prefill n_q={n_q} {impl}")
+    dw.free()
