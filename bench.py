@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true",
+                    help="skip the fp8-cache rows (per_config_fp8)")
     ap.add_argument("--only", action="store_true",
                     help="time the --workload alone (no per_config rows for the others)")
     ap.add_argument("--cpu-sample-heads", type=int, default=0,
@@ -582,6 +584,158 @@ def e2e_figures(w, lens, sets, n_sets, K, step, seq_lens, seq_idx, pos, out, max
             "no_graph_value": round(e2e_direct, 1)}
 
 
+def fp8_algorithmic(w, lens):
+    """Bytes of an fp8 cache (one e4m3 code per element and one fp32 scale
+    per row) and of the fp8 step: the cache, W_dkv||W_kr (bf16), W_uk,
+    W_uv, x, the new rows' codes and scales, q and the fp32 output. FLOPs
+    as for the bf16 step."""
+    rows = int(np.sum(lens))
+    cache_bytes = rows * (w.R + 4)
+    Tq = w.batch * w.n_q
+    eb = w.elem_bytes
+    step_bytes = (cache_bytes + (w.R * w.d_model + w.n_h * w.d_c * (w.d_nope + w.d_v)) * eb
+                  + Tq * (w.d_model + w.n_h * (w.d_nope + w.d_r)) * eb + Tq * (w.R + 4)
+                  + Tq * w.n_h * w.d_v * 4)
+    _, step_flops = step_algorithmic(w, lens)
+    return cache_bytes, step_bytes, step_flops
+
+
+def measure_workload_fp8(w, warmup, world, rank, local, dist, min_steps):
+    """The same step over an fp8 (e4m3) cache: mla_append_kv_fp8 of the new
+    tokens, then mla_decode_fp8 (absorb into fp16, attention over the codes,
+    combine). Timed from CUDA graphs over rotating input sets larger than
+    3x L2, about 0.3 s of steps (at least min_steps)."""
+    import torch
+    from mla_latent_kv_73_b300 import _lib, synth
+    from mla_latent_kv_73_b300.device_inputs import DeviceWeights, config_for, to_device
+
+    lens = synth.seq_lens(w)
+    B, n_q = w.batch, w.n_q
+    Tq = B * n_q
+    cfg = config_for(w)
+    pt_np, num_blocks = synth.page_table(w, lens)
+    cache_bytes, step_bytes, step_flops = fp8_algorithmic(w, lens)
+    wts = synth.weights(w)
+    set_bytes = cache_bytes + (w.R * w.d_model + 2 * w.n_h * w.d_c * w.d_nope) * w.elem_bytes
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    n_sets = max(2, math.ceil(3 * l2 / set_bytes))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5000 + 17 * rank + w.seed)
+    sets = []
+    for _ in range(n_sets):
+        s = {"w": DeviceWeights(w, wts, cfg), "pt": to_device(pt_np, "i32")}
+        # random e4m3 bytes 0..126 with a random sign: never a NaN pattern
+        c = torch.randint(0, 127, (num_blocks, w.block_size, w.R), generator=gen, device="cuda",
+                          dtype=torch.uint8)
+        c |= torch.randint(0, 2, c.shape, generator=gen, device="cuda", dtype=torch.uint8) << 7
+        s["cache"] = c
+        s["scale"] = torch.rand((num_blocks, w.block_size), generator=gen, device="cuda") * 0.01
+        s["x"] = torch.randn((Tq, w.d_model), generator=gen, device="cuda").to(torch.bfloat16)
+        s["q"] = torch.randn((B, n_q, w.n_h, w.d_nope + w.d_r), generator=gen,
+                             device="cuda").to(torch.bfloat16)
+        sets.append(s)
+    seq_lens = to_device(lens, "i32")
+    seq_idx = to_device(np.repeat(np.arange(B), n_q).astype(np.int32), "i32")
+    pos = to_device(np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32),
+                    "i32")
+    out = torch.empty((B, n_q, w.n_h, w.d_v), device="cuda")
+    ws = torch.empty(_lib.mla_decode_workspace_size(cfg, B, n_q), dtype=torch.uint8,
+                     device="cuda")
+    ws_a = torch.empty(_lib.mla_append_kv_fp8_workspace_size(cfg, Tq), dtype=torch.uint8,
+                       device="cuda")
+
+    def step(s, st, ev=None):
+        if ev is not None:
+            ev[0].record(st)
+        _lib.mla_append_kv_fp8(cfg, s["w"].handle, s["x"], seq_idx, pos, s["pt"], s["cache"],
+                               s["scale"], ws_a, st)
+        if ev is not None:
+            ev[1].record(st)
+        _lib.mla_decode_fp8(cfg, s["w"].handle, s["q"], s["cache"], s["scale"], s["pt"],
+                            seq_lens, out, ws, st)
+        if ev is not None:
+            ev[2].record(st)
+
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(sets[i % n_sets], stream)
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"{w.name} fp8: device error word {code:#x} after warm-up")
+    stage_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+                for _ in range(4 * n_sets)]
+    g_step, g_prof = [], []
+    for k, s in enumerate(sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(s, torch.cuda.current_stream())
+        g_step.append(g)
+    for k in range(4 * n_sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(sets[k % n_sets], torch.cuda.current_stream(), stage_ev[k])
+        g_prof.append(g)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(4 * n_sets):
+        g_step[i % n_sets].replay()
+    t1.record()
+    torch.cuda.synchronize()
+    est = t0.elapsed_time(t1) / (4 * n_sets)
+    K = int(max_over_ranks(int(min(3000, max(min_steps, 300.0 / max(est, 1e-3)))), dist, "cuda"))
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(K):
+        g_step[i % n_sets].replay()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"{w.name} fp8: device error word {code:#x} in the timed region")
+    value, total_ms_max = whole_job_rate(Tq * K, t0.elapsed_time(t1), dist, "cuda")
+    ms = total_ms_max / K
+    acc = {"append": [], "decode": []}
+    for rep in range(3):
+        for g in g_prof:
+            g.replay()
+        torch.cuda.synchronize()
+        if rep == 0:
+            continue
+        for ev in stage_ev:
+            acc["append"].append(ev[0].elapsed_time(ev[1]))
+            acc["decode"].append(ev[1].elapsed_time(ev[2]))
+    hbm, tflops, _, _ = measured_peaks()
+    dec_ms = statistics.mean(acc["decode"])
+    rows = int(np.sum(lens))
+    dec_bytes = cache_bytes + w.n_h * w.d_c * (w.d_nope + w.d_v) * w.elem_bytes + \
+        Tq * w.n_h * ((w.d_nope + w.d_r) * w.elem_bytes + w.d_v * 4)
+    _, attn_flops = algorithmic(w, lens)
+    dec_flops = attn_flops + 2.0 * Tq * w.n_h * w.d_c * (w.d_nope + w.d_v)
+    dec = roofline_entry(dec_bytes, dec_flops, dec_ms, hbm, tflops)
+    dec["kernel_ms"] = round(dec_ms, 5)
+    step_roof = roofline_entry(step_bytes, step_flops, ms, hbm, tflops)
+    for s in sets:
+        s["w"].free()
+    del sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": round(value, 1), "ms_per_step": round(ms, 5), "steps": K,
+            "cache_bytes": int(cache_bytes),
+            "cache_bytes_per_token": w.R + 4,
+            "cache_gbs": round(cache_bytes / (ms / 1e3) / 1e9, 1),
+            "decode_call": {k: dec[k] for k in ("bound", "achieved", "unit", "frac", "kernel_ms",
+                                                "roofline_ms", "gbs", "tflops")},
+            "step": {k: step_roof[k] for k in ("bound", "achieved", "unit", "frac",
+                                               "roofline_ms", "gbs", "tflops")},
+            "stage_us": {k: round(1e3 * statistics.mean(v), 2) for k, v in acc.items()},
+            "what": "mla_append_kv_fp8 + mla_decode_fp8 over an e4m3 cache with one fp32 scale "
+                    "per row; decode_call = absorb + attention + combine in one call"}
+
+
 def per_config_row(r):
     a, s = r["attention_roofline"], r["step_roofline"]
     return {"tokens_per_s": r["tokens_per_s"], "ms_per_step": round(r["ms_per_step"], 5),
@@ -612,6 +766,11 @@ def run_ours(args, world, rank, local):
                               local, dist, headline=False, min_steps=K)
         rows[name] = per_config_row(rc)
 
+    rows_fp8 = {}
+    if not args.only and not args.no_fp8:
+        for name in PER_CONFIG:
+            rows_fp8[name] = measure_workload_fp8(synth.WORKLOADS[name], args.warmup, world, rank,
+                                                  local, dist, min_steps=K)
     w = head
     lens = r["lens"]
     att = dict(r["attention_roofline"])
@@ -651,6 +810,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "step_roofline": r["step_roofline"],
         "per_config": rows,
+        "per_config_fp8": rows_fp8,
         "e2e": r["e2e"],
         "gpu_launches": 4 * K,
         "stage_us": r["stage_us"],

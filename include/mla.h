@@ -202,6 +202,66 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
                               int32_t B, int32_t n_q, float* out, void* workspace,
                               size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * fp8 latent cache: e4m3 codes with one fp32 scale per cache row.
+ *
+ * Source: "Multi-head Latent Attention and KV Cache Compression", section
+ * "Moving a trained MHA model over": quantisation can be stacked on the
+ * latent cache, and its error passes through the up-projections into every
+ * head. The page fixes neither the format nor the scale granularity. This
+ * library takes e4m3 in the "fn" variant (bias 7, 3 mantissa bits, largest
+ * finite value 448, no infinities) and one scale per row:
+ *     scale = max_k |row[k]| / 448   (1 for a row of zeros)
+ *     code[k] = e4m3(row[k] / scale), round to nearest, ties to even,
+ *               saturating at +-448
+ * with the scale and the division in fp32. A row dequantises to
+ * code[k] * scale. The cache layouts:
+ *   cache      [num_blocks, block_size, d_c + d_r] uint8 (e4m3 codes)
+ *   row_scale  [num_blocks, block_size] fp32
+ * Half the bytes of a bf16 cache per token, plus 4 bytes of scale.
+ * These calls need a bf16 config with d_c = 512, d_r = 64, d_nope = d_v =
+ * 128 and 64-token blocks (the tensor-core kernels), else they return
+ * MLA_ERR_UNSUPPORTED. Pointers to cache, row_scale, q and x must be 16-byte
+ * aligned (MLA_ERR_INVALID_ARG otherwise).
+ * ------------------------------------------------------------------------ */
+
+/* Quantise T fp32 rows and place them in the fp8 cache.
+ *   rows       [T, d_c + d_r] fp32 (device), row t belongs to token t
+ *   seq_idx, pos, page_table, B, max_blocks: as for mla_append_kv
+ * Writes each row's codes and scale to the cache row that the paged layout
+ * gives. Bad indices are skipped and set MLA_DEVERR_APPEND_INDEX or
+ * MLA_DEVERR_PAGE_RANGE. T = 0 is a no-op. */
+mla_status mla_quantize_rows_fp8(const mla_config* cfg, const float* rows, const int32_t* seq_idx,
+                                 const int32_t* pos, const int32_t* page_table, int32_t B,
+                                 int32_t max_blocks, void* cache, float* row_scale,
+                                 int32_t num_blocks, int32_t T, cudaStream_t stream);
+
+/* Bytes of device workspace that mla_append_kv_fp8 needs for T tokens: the
+ * fp32 rows of up to 256 tokens at a time. Writes the size to *bytes. */
+mla_status mla_append_kv_fp8_workspace_size(const mla_config* cfg, int32_t T, size_t* bytes);
+
+/* mla_append_kv into an fp8 cache: the rows [x W_dkv | RoPE(x W_kr, pos)]
+ * are computed in fp32 (256 tokens at a time, into the workspace), then
+ * quantised and placed as by mla_quantize_rows_fp8. Arguments as for
+ * mla_append_kv; workspace: at least mla_append_kv_fp8_workspace_size()
+ * bytes, 256-byte aligned, contents on entry irrelevant. */
+mla_status mla_append_kv_fp8(const mla_config* cfg, mla_weights w, const void* x,
+                             const int32_t* seq_idx, const int32_t* pos,
+                             const int32_t* page_table, int32_t B, int32_t max_blocks,
+                             void* cache, float* row_scale, int32_t num_blocks, int32_t T,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* mla_decode over an fp8 cache: the same absorbed-query attention on the
+ * dequantised rows (code * scale), with the same workspace
+ * (mla_decode_workspace_size). The queries are absorbed into fp16, the
+ * cache codes are widened to fp16 (exact) inside the attention kernel, the
+ * MMAs accumulate in fp32, and each row's scale multiplies its score and
+ * its value weight. Bad lengths and page ids behave as for mla_decode. */
+mla_status mla_decode_fp8(const mla_config* cfg, mla_weights w, const void* q, const void* cache,
+                          const float* row_scale, int32_t num_blocks, const int32_t* page_table,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                          float* out, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Size of the fixed device array that mla_decode_no_alloc uses in place of a
  * workspace: 32 MiB. */
 #define MLA_NO_ALLOC_WORKSPACE_BYTES ((size_t)32 << 20)

@@ -26,7 +26,9 @@ EXPORTS = ["mla_absorb_weights", "mla_weights_free", "mla_append_kv",
            "mla_decode_attend", "mla_decode_combine", "mla_decode_impl",
            "mla_get_last_device_error", "mla_status_string", "mla_decode_no_alloc",
            "mla_fold_full", "mla_full_weights_free", "mla_decode_full_workspace_size",
-           "mla_decode_full", "mla_decode_layer_workspace_size", "mla_decode_layer"]
+           "mla_decode_full", "mla_decode_layer_workspace_size", "mla_decode_layer",
+           "mla_quantize_rows_fp8", "mla_append_kv_fp8_workspace_size", "mla_append_kv_fp8",
+           "mla_decode_fp8"]
 MLA_NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -70,6 +72,12 @@ def _declare(lib):
         "mla_decode_layer_workspace_size": [cfgp, _I, _I, ctypes.POINTER(ctypes.c_size_t)],
         "mla_decode_layer": [cfgp, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P,
                              ctypes.c_size_t, _P],
+        "mla_quantize_rows_fp8": [cfgp, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P],
+        "mla_append_kv_fp8_workspace_size": [cfgp, _I, ctypes.POINTER(ctypes.c_size_t)],
+        "mla_append_kv_fp8": [cfgp, _P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _P,
+                              ctypes.c_size_t, _P],
+        "mla_decode_fp8": [cfgp, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_size_t,
+                           _P],
         "mla_get_last_device_error": [_P, ctypes.POINTER(ctypes.c_uint32)],
         "mla_status_string": [_I],
     }
@@ -159,6 +167,39 @@ def mla_decode(cfg, w, q, cache, page_table, seq_lens, out, workspace, stream=No
     check("mla_decode", load().mla_decode(
         ctypes.byref(cfg), w, ptr(q), ptr(cache), cache.shape[0], ptr(page_table),
         page_table.shape[1], ptr(seq_lens), B, n_q, ptr(out), ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream)))
+
+
+def mla_quantize_rows_fp8(cfg, rows, seq_idx, pos, page_table, cache, row_scale, stream=None):
+    """fp32 rows [T, R] -> e4m3 codes and row scales in the paged fp8 cache."""
+    B, max_blocks = page_table.shape
+    check("mla_quantize_rows_fp8", load().mla_quantize_rows_fp8(
+        ctypes.byref(cfg), ptr(rows), ptr(seq_idx), ptr(pos), ptr(page_table), B, max_blocks,
+        ptr(cache), ptr(row_scale), cache.shape[0], rows.shape[0], stream_handle(stream)))
+
+
+def mla_append_kv_fp8_workspace_size(cfg, T):
+    n = ctypes.c_size_t()
+    check("mla_append_kv_fp8_workspace_size", load().mla_append_kv_fp8_workspace_size(
+        ctypes.byref(cfg), T, ctypes.byref(n)))
+    return n.value
+
+
+def mla_append_kv_fp8(cfg, w, x, seq_idx, pos, page_table, cache, row_scale, workspace,
+                      stream=None):
+    B, max_blocks = page_table.shape
+    check("mla_append_kv_fp8", load().mla_append_kv_fp8(
+        ctypes.byref(cfg), w, ptr(x), ptr(seq_idx), ptr(pos), ptr(page_table), B, max_blocks,
+        ptr(cache), ptr(row_scale), cache.shape[0], x.shape[0], ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream)))
+
+
+def mla_decode_fp8(cfg, w, q, cache, row_scale, page_table, seq_lens, out, workspace,
+                   stream=None):
+    B, n_q = q.shape[0], q.shape[1]
+    check("mla_decode_fp8", load().mla_decode_fp8(
+        ctypes.byref(cfg), w, ptr(q), ptr(cache), ptr(row_scale), cache.shape[0],
+        ptr(page_table), page_table.shape[1], ptr(seq_lens), B, n_q, ptr(out), ptr(workspace),
         workspace.numel() * workspace.element_size(), stream_handle(stream)))
 
 

@@ -18,8 +18,9 @@
 // block of W_uk[h], each starting as soon as its two boxes have landed) issue
 // 8 MMAs each with M = 128 latent rows, N = tokens, K = 128, accumulating
 // q_lat^T in TMEM (4 blocks of up to 128 columns). Four warps read it back,
-// one latent row per lane, and store bf16. The other four warps rotate
-// q_rope meanwhile.
+// one latent row per lane, and store them in bf16 (fp16 for the attention
+// over an fp8 cache, whose MMAs take fp16 operands). The other four warps
+// rotate q_rope meanwhile.
 //
 // Block (0, 0) also writes the split-KV plan (tiles per sequence, their
 // prefix sum and the range boundaries), which the attention and combine
@@ -50,13 +51,14 @@ __device__ __forceinline__ uint64_t kdesc(const void* base, uint32_t byte_off) {
   return smem_desc(smem_u32(base) + byte_off, 16, 1024, kSwizzle128B);
 }
 
+template <typename OT>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_q, Shape s,
                    const __nv_bfloat16* __restrict__ q, const double* __restrict__ inv_freq,
                    const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
                    int G, int C, int K, int n_tok_box, float out_scale,
-                   __nv_bfloat16* __restrict__ qabs, int32_t* tiles, int32_t* prefix,
+                   OT* __restrict__ qabs, int32_t* tiles, int32_t* prefix,
                    long long* bounds, int32_t* first_b, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   AbsSmem& sm = *reinterpret_cast<AbsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -138,9 +140,9 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
       const float x1 = __bfloat162float(qr[k]), x2 = __bfloat162float(qr[k + 32]);
       float c, sn;
       rope_cos_sin(pos, inv_freq[k], &c, &sn);
-      __nv_bfloat16* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + 512;
-      o[k] = __float2bfloat16_rn((x1 * c - x2 * sn) * out_scale);
-      o[k + 32] = __float2bfloat16_rn((x1 * sn + x2 * c) * out_scale);
+      OT* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + 512;
+      o[k] = from_f32<OT>((x1 * c - x2 * sn) * out_scale);
+      o[k + 32] = from_f32<OT>((x1 * sn + x2 * c) * out_scale);
     }
   } else {
     // q_lat^T from TMEM: lane = latent row inside M-block j, column = token
@@ -161,7 +163,7 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
             const int tt = c0 + i;
             if (tt < ntok)
               qabs[(static_cast<size_t>(t0 + tt) * s.n_h + h) * R + dc] =
-                  __float2bfloat16_rn(v[i] * out_scale);
+                  from_f32<OT>(v[i] * out_scale);
           }
         }
       }
@@ -175,16 +177,12 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   }
 }
 
-}  // namespace
 
-bool absorb_tc_supported(const Shape& s, mla_dtype dt) {
-  return dt == MLA_BF16 && s.d_c == 512 && s.d_nope == 128 && s.d_r == 64;
-}
-
-cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
-                               const int32_t* seq_lens, int max_blocks, int B, int n_q,
-                               const Partition& p, const WsView& ws, float out_scale,
-                               uint32_t* err, cudaStream_t st) {
+template <typename OT>
+cudaError_t absorb_q_tc_t(const Shape& s, const Weights* w, const void* q,
+                          const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                          const Partition& p, const WsView& ws, float out_scale, uint32_t* err,
+                          cudaStream_t st) {
   const int Tq = B * n_q;
   const int n_tok_box = min(AT_TOK, ((Tq + 15) / 16) * 16);
   TmapSpec ws_spec{};
@@ -217,7 +215,7 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel<OT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -234,10 +232,27 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, absorb_q_tc_kernel,
+  return cudaLaunchKernelEx(&cfg, absorb_q_tc_kernel<OT>,
       tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
-      p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<__nv_bfloat16*>(ws.qabs), ws.tiles,
+      p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<OT*>(ws.qabs), ws.tiles,
       ws.prefix, ws.bounds, ws.first_b, err);
+}
+
+}  // namespace
+
+bool absorb_tc_supported(const Shape& s, mla_dtype dt) {
+  return dt == MLA_BF16 && s.d_c == 512 && s.d_nope == 128 && s.d_r == 64;
+}
+
+cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
+                               const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                               const Partition& p, const WsView& ws, float out_scale,
+                               bool q_half, uint32_t* err, cudaStream_t st) {
+  if (q_half)
+    return absorb_q_tc_t<__half>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err,
+                                 st);
+  return absorb_q_tc_t<__nv_bfloat16>(s, w, q, seq_lens, max_blocks, B, n_q, p, ws, out_scale,
+                                      err, st);
 }
 
 }  // namespace mla

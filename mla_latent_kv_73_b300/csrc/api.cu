@@ -240,6 +240,18 @@ mla_status prepare_decode(const mla_config* cfg, int B, int n_q, const void* cac
   return MLA_OK;
 }
 
+// The fp8 cache runs on the tensor-core kernels only: bf16 weights and
+// queries at the DeepSeek-V2 latent widths, 64-token blocks, a B300.
+bool fp8_supported(const mla_config* cfg, const DeviceInfo* di) {
+  const Shape s = shape_of(cfg);
+  return cfg->dtype == MLA_BF16 && cfg->impl != MLA_IMPL_CUDA_CORE && s.d_nope == 128 &&
+         s.d_v == 128 && attend_tc_supported(s, cfg->dtype) &&
+         absorb_tc_supported(s, cfg->dtype) && combine_tc_supported(s, cfg->dtype) &&
+         tc_device(di);
+}
+
+constexpr int kFp8AppendChunk = 256;  // tokens whose fp32 rows the workspace holds
+
 // Device scratch of mla_decode_full beyond the per-head decode's workspace:
 // the fp32 query projection [B*n_q][n_h*R] (reused for o_lat, which is no
 // wider), then the split partials of the two x W products.
@@ -422,7 +434,7 @@ mla_status mla_decode_absorb_q(const mla_config* cfg, mla_weights w, const void*
       p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (p.impl == MLA_IMPL_TENSOR_CORE && absorb_tc_supported(p.s, cfg->dtype) && aligned16(q))
     return from_cuda(launch_absorb_q_tc(p.s, &w->w, q, seq_lens, max_blocks, B, n_q, p.part, v,
-                                        out_scale, di->err, stream));
+                                        out_scale, false, di->err, stream));
   return from_cuda(launch_absorb_q(p.s, cfg->dtype, &w->w, q, seq_lens, max_blocks, B, n_q,
                                    p.part, v, out_scale, p.impl == MLA_IMPL_CUDA_CORE, di->err,
                                    stream));
@@ -490,6 +502,104 @@ mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const
                          workspace, ws_bytes, stream);
   if (st != MLA_OK) return st;
   return mla_decode_combine(&c2, w, seq_lens, B, n_q, out, workspace, ws_bytes, stream);
+}
+
+mla_status mla_quantize_rows_fp8(const mla_config* cfg, const float* rows, const int32_t* seq_idx,
+                                 const int32_t* pos, const int32_t* page_table, int32_t B,
+                                 int32_t max_blocks, void* cache, float* row_scale,
+                                 int32_t num_blocks, int32_t T, cudaStream_t stream) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (T < 0 || B < 1 || max_blocks < 1 || num_blocks < 1) return MLA_ERR_SHAPE;
+  if (T == 0) return MLA_OK;
+  if (!rows || !seq_idx || !pos || !page_table || !cache || !row_scale) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  if (!fp8_supported(cfg, di)) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(cache) || !aligned16(row_scale)) return MLA_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_rows_fp8(shape_of(cfg), rows, seq_idx, pos, page_table, B,
+                                            max_blocks, static_cast<uint8_t*>(cache), row_scale,
+                                            num_blocks, T, di->err, stream));
+}
+
+mla_status mla_append_kv_fp8_workspace_size(const mla_config* cfg, int32_t T, size_t* bytes) {
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = 0;
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (T < 0) return MLA_ERR_SHAPE;
+  const int chunk = T < kFp8AppendChunk ? T : kFp8AppendChunk;
+  *bytes = align256(sizeof(float) * static_cast<size_t>(chunk) * shape_of(cfg).R());
+  return MLA_OK;
+}
+
+mla_status mla_append_kv_fp8(const mla_config* cfg, mla_weights w, const void* x,
+                             const int32_t* seq_idx, const int32_t* pos,
+                             const int32_t* page_table, int32_t B, int32_t max_blocks,
+                             void* cache, float* row_scale, int32_t num_blocks, int32_t T,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (!w) return MLA_ERR_INVALID_ARG;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (T < 0 || B < 1 || max_blocks < 1 || num_blocks < 1) return MLA_ERR_SHAPE;
+  if (T == 0) return MLA_OK;
+  if (!x || !seq_idx || !pos || !page_table || !cache || !row_scale) return MLA_ERR_INVALID_ARG;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  if (!fp8_supported(cfg, di)) return MLA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(cache) || !aligned16(row_scale)) return MLA_ERR_INVALID_ARG;
+  size_t need = 0;
+  mla_append_kv_fp8_workspace_size(cfg, T, &need);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || ws_bytes < need)
+    return MLA_ERR_WORKSPACE;
+  const Shape s = shape_of(cfg);
+  float* rows = static_cast<float*>(workspace);
+  const char* xb = static_cast<const char*>(x);
+  const size_t x_row = static_cast<size_t>(s.d_model) * dtype_bytes(cfg->dtype);
+  cudaError_t e = cudaSuccess;
+  for (int off = 0; off < T && e == cudaSuccess; off += kFp8AppendChunk) {
+    const int n = T - off < kFp8AppendChunk ? T - off : kFp8AppendChunk;
+    e = launch_append_rows_f32(s, cfg->dtype, &w->w, xb + off * x_row, seq_idx + off, pos + off,
+                               n, rows, di->err, stream);
+    if (e == cudaSuccess)
+      e = launch_quantize_rows_fp8(s, rows, seq_idx + off, pos + off, page_table, B, max_blocks,
+                                   static_cast<uint8_t*>(cache), row_scale, num_blocks, n,
+                                   di->err, stream);
+  }
+  return from_cuda(e);
+}
+
+mla_status mla_decode_fp8(const mla_config* cfg, mla_weights w, const void* q, const void* cache,
+                          const float* row_scale, int32_t num_blocks, const int32_t* page_table,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t B, int32_t n_q,
+                          float* out, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!w || !q || !cache || !row_scale || !page_table || !seq_lens || !out)
+    return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  mla_status st = check_decode_args(cfg, B, n_q);
+  if (st != MLA_OK) return st;
+  const DeviceInfo* di = device_info();
+  if (!di) return MLA_ERR_CUDA;
+  if (!fp8_supported(cfg, di)) return MLA_ERR_UNSUPPORTED;
+  if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
+  if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(cache) || !aligned16(row_scale)) return MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * cfg->block_size > (1LL << 31) - 1) return MLA_ERR_SHAPE;
+  Plan p;
+  make_plan(cfg, B, n_q, di, MLA_IMPL_TENSOR_CORE, &p);
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MLA_ERR_WORKSPACE;
+  if (ws_bytes < p.lay.total) return MLA_ERR_WORKSPACE;
+  const WsView v = ws_view(workspace, p.lay);
+  // fp16 queries, pre-multiplied by scale * log2(e) as for the bf16 kernel
+  cudaError_t e = launch_absorb_q_tc(p.s, &w->w, q, seq_lens, max_blocks, B, n_q, p.part, v,
+                                     p.s.scale * 1.4426950408889634f, true, di->err, stream);
+  if (e == cudaSuccess)
+    e = launch_attend_tc_fp8(p.s, cache, row_scale, num_blocks, page_table, max_blocks, B, n_q,
+                             p.part, v, seq_lens, di->err, stream);
+  if (e == cudaSuccess) e = launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream);
+  return from_cuda(e);
 }
 
 mla_status mla_fold_full(const mla_config* cfg, const void* W_q, const void* W_uk,

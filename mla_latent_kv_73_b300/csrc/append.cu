@@ -38,10 +38,16 @@ struct AppendArgs {
   const int32_t* page_table;
   int B, max_blocks, num_blocks, T;
   uint32_t* err;
+  // When set, the rows go here instead, in fp32 and dense ([T][R], row t
+  // for token t, no paging): the input of the fp8 row quantiser.
+  float* rows_out;
 };
 
 // Physical row of token t, or -1 (and an error bit) if its indices are bad.
+// In the dense fp32 mode every token has a row (the quantiser checks the
+// indices when it places the rows).
 __device__ __forceinline__ long long append_row(const AppendArgs& a, const Shape& s, int t) {
+  if (a.rows_out) return t;
   const int b = a.seq_idx[t], p = a.pos[t];
   if (b < 0 || b >= a.B || p < 0 || p / s.bs >= a.max_blocks) {
     set_error(a.err, MLA_DEVERR_APPEND_INDEX);
@@ -53,6 +59,17 @@ __device__ __forceinline__ long long append_row(const AppendArgs& a, const Shape
     return -1;
   }
   return static_cast<long long>(page) * s.bs + p % s.bs;
+}
+
+// Stores the finished value of cache column `dst` of the row returned by
+// append_row: into the paged cache in T, or in fp32 into the dense rows.
+template <typename T>
+__device__ __forceinline__ void put_value(const AppendArgs& a, T* cache, long long row, int R,
+                                          int dst, float v) {
+  if (a.rows_out)
+    a.rows_out[row * R + dst] = v;
+  else
+    cache[row * R + dst] = from_f32<T>(v);
 }
 
 // Value of packed column pc after RoPE, given the pre-rotation values of the
@@ -141,7 +158,7 @@ append_gemv_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
           const int dst = finish_column(s, a.inv_freq, pc, res[c * GEMV_TOK + t],
                                         res[ce * GEMV_TOK + t], res[(ce + 1) * GEMV_TOK + t],
                                         a.pos[tok], &out);
-          cache[row * R + dst] = from_f32<T>(out);
+          put_value<T>(a, cache, row, R, dst, out);
         }
       }
     }
@@ -251,7 +268,7 @@ append_staged_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
           const int dst = finish_column(s, a.inv_freq, pc, res[c * ST_TOK + tt],
                                         res[ce * ST_TOK + tt], res[(ce + 1) * ST_TOK + tt],
                                         a.pos[tok], &out);
-          cache[row * R + dst] = from_f32<T>(out);
+          put_value<T>(a, cache, row, R, dst, out);
         }
       }
     }
@@ -323,7 +340,7 @@ append_gemm_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
       float out;
       const int dst =
           finish_column(s, a.inv_freq, pc, acc[i][j], acc[i][je], acc[i][je + 1], a.pos[tok], &out);
-      cache[row * R + dst] = from_f32<T>(out);
+      put_value<T>(a, cache, row, R, dst, out);
     }
   }
 }
@@ -458,10 +475,10 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     if (row < 0) continue;
     float out;
     int dst = finish_column(s, a.inv_freq, pc0, v0, v0, v1, a.pos[t], &out);
-    cache[row * R + dst] = __float2bfloat16_rn(out);
+    put_value<__nv_bfloat16>(a, cache, row, R, dst, out);
     if (pc0 + 1 < R) {
       dst = finish_column(s, a.inv_freq, pc0 + 1, v1, v0, v1, a.pos[t], &out);
-      cache[row * R + dst] = __float2bfloat16_rn(out);
+      put_value<__nv_bfloat16>(a, cache, row, R, dst, out);
     }
   }
   cluster_sync();  // no CTA leaves while a peer may still read its partial
@@ -606,6 +623,7 @@ cudaError_t append_t(const Shape& s, const Weights* w, const void* x, AppendArgs
           AppendArgs c = a;
           c.seq_idx += off;
           c.pos += off;
+          if (c.rows_out) c.rows_out += static_cast<size_t>(off) * R;
           c.T = min(AT_MAX_TOK, a.T - off);
           const T* xc = static_cast<const T*>(x) + static_cast<size_t>(off) * s.d_model;
           if (!launch_append_tc(s, w, xc, c, cache, st, &e)) return cudaErrorInvalidValue;
@@ -649,9 +667,18 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st) {
-  AppendArgs a{w->inv_freq, seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err};
+  AppendArgs a{w->inv_freq, seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err,
+               nullptr};
   if (dt == MLA_F32) return append_t<float>(s, w, x, a, cache, st);
   return append_t<__nv_bfloat16>(s, w, x, a, cache, st);
+}
+
+cudaError_t launch_append_rows_f32(const Shape& s, mla_dtype dt, const Weights* w, const void* x,
+                                   const int32_t* seq_idx, const int32_t* pos, int T,
+                                   float* rows, uint32_t* err, cudaStream_t st) {
+  AppendArgs a{w->inv_freq, seq_idx, pos, nullptr, 1, 1, 1, T, err, rows};
+  if (dt == MLA_F32) return append_t<float>(s, w, x, a, nullptr, st);
+  return append_t<__nv_bfloat16>(s, w, x, a, nullptr, st);
 }
 
 }  // namespace mla

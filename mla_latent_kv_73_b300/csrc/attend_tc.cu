@@ -86,6 +86,7 @@
 // meets its peer at the final cluster barrier, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cmath>
 #include <mutex>
@@ -121,18 +122,48 @@ constexpr uint32_t SEND_BAR = 5;              // named barrier of the four sende
 constexpr long long WAIT_LIMIT = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float RESCALE_THRESHOLD = 8.f;        // log2 units
 
-struct __align__(1024) PairSmem {
+// fp8 (e4m3) cache: per page and CTA, the latent codes of this CTA's 256
+// columns, its 32 rotary codes and the page's 64 row scales arrive by TMA in
+// a ring of F8_STAGES; the softmax warps convert them to fp16 (exact for
+// every e4m3 value) into F8_KV_STAGES compute stages laid out like the bf16
+// ones, two tiles ahead of the score MMAs.
+constexpr int F8_STAGES = 2;
+constexpr int F8_KV_STAGES = 3;
+constexpr uint32_t F8C_BYTES = TP_TOK * 256;
+constexpr uint32_t F8R_BYTES = TP_TOK * 32;
+constexpr uint32_t F8_TX_BYTES = F8C_BYTES + F8R_BYTES + TP_TOK * 4;
+
+struct __align__(128) F8Stage {
+  uint8_t c[F8C_BYTES];  // [token][256 codes], no swizzle
+  uint8_t r[F8R_BYTES];  // [token][32 codes]
+  float s[TP_TOK];       // row scales of the page
+};
+
+template <bool FP8>
+struct F8Part {
+  F8Stage st[F8_STAGES];
+  float kscale[F8_KV_STAGES][TP_TOK];   // row scales of a compute stage (0 past the end)
+  float klscale[F8_KV_STAGES][TP_TOK];  // their log2 (-inf past the end)
+  uint64_t full[F8_STAGES], empty[F8_STAGES];
+};
+template <>
+struct F8Part<false> {};
+
+template <bool FP8>
+struct __align__(1024) PairSmemT {
+  static constexpr int NS = FP8 ? F8_KV_STAGES : TP_STAGES;  // compute stages
   uint8_t qc[QC_BOX];  // Q latent columns 0..63 of this CTA's half
   uint8_t qr[QR_BOX];
   struct Stage {
     uint8_t c[4][KC_BOX];
     uint8_t r[KR_BOX];
-  } kv[TP_STAGES];
+  } kv[NS];
   // peer's partial scores, fp16 pairs: [buffer][row][64 tokens], 16-byte units swizzled
   uint32_t xbuf[2][TP_ROWS * TP_TOK / 2];
   // this CTA's partial scores of the tile being sent, same layout
   uint32_t sendbuf[TP_ROWS * TP_TOK / 2];
-  uint64_t kv_full[TP_STAGES], kv_empty[TP_STAGES];
+  F8Part<FP8> f8;
+  uint64_t kv_full[NS], kv_empty[NS];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];   // score slot by tile parity
   uint64_t own_ready[2];            // fp16 own partial written back to the slot
@@ -146,6 +177,9 @@ struct __align__(1024) PairSmem {
   float st_l[2][TP_ROWS];      // [column half]: row sums at the end of a piece
 };
 
+static_assert(sizeof(PairSmemT<false>) + 1024 <= 227 * 1024, "bf16 pair smem above 227 KB");
+static_assert(sizeof(PairSmemT<true>) + 1024 <= 227 * 1024, "fp8 pair smem above 227 KB");
+
 struct PairArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
@@ -155,7 +189,8 @@ struct PairArgs {
   const int32_t* first_b;   // [P] sequence of each range's first work item
   float* part_o;
   float* part_lse;
-  const __nv_bfloat16* qabs;  // [q_rows][576] absorbed queries (for the TMEM part of Q)
+  const uint16_t* qabs;       // [q_rows][576] absorbed queries, bf16 or fp16 bits (the TMEM part of Q)
+  const float* row_scale;     // fp8 cache: [num_blocks * 64] row scales
   uint32_t* err;
   long long q_rows;
   int num_blocks, max_blocks, B, n_q, n_h, G, P;
@@ -231,12 +266,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void note_timeout(PairSmem& sm, uint32_t* err) {
+template <class SM>
+__device__ __forceinline__ void note_timeout(SM& sm, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&sm.abort_flag) = 1;
   set_error(err, MLA_DEVERR_TIMEOUT);
 }
 
-__device__ __forceinline__ bool aborted(PairSmem& sm) {
+template <class SM>
+__device__ __forceinline__ bool aborted(SM& sm) {
   return *reinterpret_cast<volatile int*>(&sm.abort_flag) != 0;
 }
 
@@ -282,7 +319,8 @@ __device__ __forceinline__ uint32_t xoff(int row, int u) {
 // this tile is not processed), SEND_LATE in the leader if its wait for the
 // peer's buffer timed out here (then nothing was sent), else SEND_OK.
 enum SendResult { SEND_OK = 0, SEND_LATE = 1, SEND_STOP = 2 };
-__device__ __forceinline__ SendResult send_tile(PairSmem& sm, uint32_t slot, int row, int lane,
+template <class SM>
+__device__ __forceinline__ SendResult send_tile(SM& sm, uint32_t slot, int row, int lane,
                                                 bool leader, uint32_t kv, uint32_t peer,
                                                 bool bad) {
   const int b = kv & 1;
@@ -344,7 +382,8 @@ __device__ __forceinline__ SendResult send_tile(PairSmem& sm, uint32_t slot, int
 // read them as their A operand, once the previous piece's score MMAs are
 // done with them. Rows past the end of the queries are zero. Returns true on
 // timeout.
-__device__ __forceinline__ bool load_q_tmem(PairSmem& sm, const PairArgs& a, uint32_t tmem,
+template <class SM>
+__device__ __forceinline__ bool load_q_tmem(SM& sm, const PairArgs& a, uint32_t tmem,
                                             uint32_t lane_base, int row, int lane, uint32_t rank,
                                             const TileCursor& cur) {
   bool bad = false;
@@ -374,14 +413,95 @@ __device__ __forceinline__ bool load_q_tmem(PairSmem& sm, const PairArgs& a, uin
   return bad;
 }
 
+// 16 e4m3 codes (one 16-byte unit, lowest address first) -> 16 fp16 values
+// in eight f16x2 words, same order. Every e4m3 value is exact in fp16.
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& v, uint32_t (&w)[8]) {
+  const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(in[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(in[i] >> 16), __NV_E4M3);
+    w[2 * i] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+    w[2 * i + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+  }
+}
+
+// fp8 cache: the softmax warps (thread gtid of 256) convert tile cv.kv from
+// its e4m3 ring stage into its fp16 compute stage, in the layout the TMA
+// gives the bf16 stages (four 128-byte-swizzled latent boxes, one
+// 64-byte-swizzled rotary box), and copy the page's row scales (and their
+// log2) beside it. Rows past the sequence's end become zeros with scale 0,
+// whatever the cache holds there. Each warp then arrives on the compute
+// stage's full barrier and the ring stage's empty barrier. Returns false on
+// a timeout (nothing converted, nothing arrived).
+template <class SM>
+__device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const TileCursor& cv,
+                                             int gtid, int lane) {
+  const uint32_t j = cv.kv;
+  const int s8 = j % F8_STAGES, sc = j % F8_KV_STAGES;
+  bool ok = true;
+  // the compute stage is free once the value MMAs of tile j - 3 are done
+  if (j >= F8_KV_STAGES)
+    ok = mbar_wait(&sm.kv_empty[sc], ((j / F8_KV_STAGES) - 1) & 1, WAIT_LIMIT);
+  ok = ok && mbar_wait(&sm.f8.full[s8], (j / F8_STAGES) & 1, WAIT_LIMIT);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  const int L = a.seq_lens[cv.pc.b];
+  const int valid = min(TP_TOK, max(0, L - cv.tile() * TP_TOK));
+  const F8Stage& f = sm.f8.st[s8];
+  auto& dst = sm.kv[sc];
+  constexpr int kUnits = 18;  // 16-byte input units per row: 16 latent, 2 rotary
+  for (int k = gtid; k < TP_TOK * kUnits; k += TP_SM_WARPS * 32) {
+    const int r = k / kUnits, u = k - r * kUnits;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < valid)
+      v = u < 16 ? *reinterpret_cast<const uint4*>(f.c + r * 256 + u * 16)
+                 : *reinterpret_cast<const uint4*>(f.r + r * 32 + (u - 16) * 16);
+    uint32_t w[8];
+    e4m3x16_to_f16(v, w);
+    uint8_t* row;
+    int ua, ub;
+    if (u < 16) {  // latent box u / 4, 16-byte units 2 (u % 4) and 2 (u % 4) + 1 of 8
+      row = dst.c[u >> 2] + r * 128;
+      const int u0 = 2 * (u & 3);
+      ua = u0 ^ (r & 7);
+      ub = (u0 + 1) ^ (r & 7);
+    } else {  // rotary box, units 2 (u - 16) and 2 (u - 16) + 1 of 4
+      row = dst.r + r * 64;
+      const int u0 = 2 * (u - 16), x = (r >> 1) & 3;
+      ua = u0 ^ x;
+      ub = (u0 + 1) ^ x;
+    }
+    *reinterpret_cast<uint4*>(row + ua * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + ub * 16) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  if (gtid < TP_TOK) {
+    const bool in = gtid < valid;
+    const float sv = in ? f.s[gtid] : 0.f;
+    sm.f8.kscale[sc][gtid] = sv;
+    sm.f8.klscale[sc][gtid] = in ? __log2f(sv) : -INFINITY;
+  }
+  fence_proxy_async_smem();  // the converted tile is read by the MMAs
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(&sm.kv_full[sc]);
+    mbar_arrive(&sm.f8.empty[s8]);
+  }
+  return true;
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(TP_THREADS, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
                  const __grid_constant__ CUtensorMap tmap_qr,
                  const __grid_constant__ CUtensorMap tmap_kc,
                  const __grid_constant__ CUtensorMap tmap_kr, PairArgs a) {
+  using Smem = PairSmemT<FP8>;
+  constexpr int NS = Smem::NS;
   extern __shared__ uint8_t smem_raw[];
-  PairSmem& sm = *reinterpret_cast<PairSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = static_cast<int>(cluster_id_x());
@@ -389,9 +509,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   // Setup first: with programmatic dependent launch it overlaps the end of
   // the query-absorption kernel, whose outputs are read only after the wait.
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TP_STAGES; ++s) {
-      mbar_init(&sm.kv_full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      // bf16: the TMA's bytes; fp8: the eight converting softmax warps
+      mbar_init(&sm.kv_full[s], FP8 ? TP_SM_WARPS : 1);
       mbar_init(&sm.kv_empty[s], 1);
+    }
+    if constexpr (FP8) {
+      for (int s = 0; s < F8_STAGES; ++s) {
+        mbar_init(&sm.f8.full[s], 1);
+        mbar_init(&sm.f8.empty[s], TP_SM_WARPS);
+      }
     }
     mbar_init(&sm.q_full, 1 + 4);  // TMA bytes + the four sender warps' TMEM part
     mbar_init(&sm.q_empty, 2);     // one commit from each score-MMA issuer
@@ -441,7 +568,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       const int xr = 512 + 32 * static_cast<int>(rank);
       uint32_t kv_it = 0;
       int piece_idx = 0;
-      uint32_t issued[TP_STAGES] = {};
+      constexpr int RING = FP8 ? F8_STAGES : TP_STAGES;  // stages the TMA fills
+      uint32_t issued[RING] = {};
       bool stop = false;
       int prev_g = static_cast<int>(it_begin / T_all), next_b = a.first_b[pair];
       for (long long it = it_begin; it < it_end && !stop && !aborted(sm);) {
@@ -461,9 +589,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         for (int t = pc.t_first; t < pc.t_first + pc.n_tiles; ++t) {
           int page = page_next;
           if (t + 1 < pc.t_first + pc.n_tiles) page_next = pt[t + 1];
-          const int s = kv_it % TP_STAGES;
-          const uint32_t n = kv_it / TP_STAGES;
-          if (kv_it >= TP_STAGES && !mbar_wait(&sm.kv_empty[s], (n - 1) & 1, WAIT_LIMIT)) {
+          const int s = kv_it % RING;
+          const uint32_t n = kv_it / RING;
+          uint64_t* empty_bar;
+          if constexpr (FP8) empty_bar = &sm.f8.empty[s];
+          else empty_bar = &sm.kv_empty[s];
+          if (kv_it >= RING && !mbar_wait(empty_bar, (n - 1) & 1, WAIT_LIMIT)) {
             note_timeout(sm, a.err);
             stop = true;
             break;
@@ -472,16 +603,27 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
             set_error(a.err, MLA_DEVERR_PAGE_RANGE);
             page = 0;
           }
-          mbar_arrive_expect_tx(&sm.kv_full[s], STAGE_BYTES);
-          if (a.chunked) {
-            tma_load_3d_hint(sm.kv[s].c[0], &tmap_kc, 0, page * TP_TOK,
-                             4 * static_cast<int>(rank), &sm.kv_full[s], pol);
+          if constexpr (FP8) {
+            // this CTA's 256 latent codes and 32 rotary codes of the page's
+            // 64 rows, and the page's 64 row scales
+            mbar_arrive_expect_tx(&sm.f8.full[s], F8_TX_BYTES);
+            tma_load_2d_hint(sm.f8.st[s].c, &tmap_kc, 256 * static_cast<int>(rank),
+                             page * TP_TOK, &sm.f8.full[s], pol);
+            tma_load_2d_hint(sm.f8.st[s].r, &tmap_kr, xr, page * TP_TOK, &sm.f8.full[s], pol);
+            bulk_load(sm.f8.st[s].s, a.row_scale + static_cast<size_t>(page) * TP_TOK,
+                      TP_TOK * 4, &sm.f8.full[s]);
           } else {
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d_hint(sm.kv[s].c[j], &tmap_kc, 256 * static_cast<int>(rank) + 64 * j,
-                               page * TP_TOK, &sm.kv_full[s], pol);
+            mbar_arrive_expect_tx(&sm.kv_full[s], STAGE_BYTES);
+            if (a.chunked) {
+              tma_load_3d_hint(sm.kv[s].c[0], &tmap_kc, 0, page * TP_TOK,
+                               4 * static_cast<int>(rank), &sm.kv_full[s], pol);
+            } else {
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d_hint(sm.kv[s].c[j], &tmap_kc, 256 * static_cast<int>(rank) + 64 * j,
+                                 page * TP_TOK, &sm.kv_full[s], pol);
+            }
+            tma_load_2d_hint(sm.kv[s].r, &tmap_kr, xr, page * TP_TOK, &sm.kv_full[s], pol);
           }
-          tma_load_2d_hint(sm.kv[s].r, &tmap_kr, xr, page * TP_TOK, &sm.kv_full[s], pol);
           ++issued[s];
           ++kv_it;
         }
@@ -489,8 +631,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         it += pc.n_tiles;
       }
       // Never leave a TMA write in flight past the end of the CTA.
-      for (int s = 0; s < TP_STAGES; ++s)
-        if (issued[s] > 0) mbar_wait(&sm.kv_full[s], (issued[s] - 1) & 1, WAIT_LIMIT);
+      for (int s = 0; s < RING; ++s) {
+        if (issued[s] == 0) continue;
+        if constexpr (FP8) mbar_wait(&sm.f8.full[s], (issued[s] - 1) & 1, WAIT_LIMIT);
+        else mbar_wait(&sm.kv_full[s], (issued[s] - 1) & 1, WAIT_LIMIT);
+      }
       if (piece_idx > 0) mbar_wait(&sm.q_full, (piece_idx - 1) & 1, WAIT_LIMIT);
     }
   } else if (warp == 1) {
@@ -498,12 +643,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     // O (this CTA's 256 latent columns) += P C, with P read from TMEM.
     // pv_done[t & 1] tells the softmax when the P buffer and O are free.
     if (lane == 0) {
-      const uint32_t idPV = idesc_bf16_f32(128, 256, false, true);
+      const uint32_t idPV = FP8 ? idesc_f16_f32(128, 256, false, true)
+                                : idesc_bf16_f32(128, 256, false, true);
       // C as the MN-major B operand: latent columns are contiguous (64 per
       // 128-byte row, the next 64 one box further), tokens step 128 B,
       // 8-token groups are 1024 B apart.
       const uint64_t dC0 = smem_desc(smem_u32(sm.kv[0].c[0]), KC_BOX, 1024, kSwizzle128B);
-      constexpr uint32_t kStageDesc = sizeof(PairSmem::Stage) >> 4;  // stage stride, 16-B units
+      constexpr uint32_t kStageDesc = sizeof(typename Smem::Stage) >> 4;  // stage stride, 16-B units
       bool ok = true;
       TileCursor cur;
       cur.init(it_begin, it_end, a, pair);
@@ -516,7 +662,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
           break;
         }
         tc_fence_after();
-        const int s = t % TP_STAGES;
+        const int s = t % NS;
         const uint32_t pcol = tmem + TM_P;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -539,12 +685,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     // steps. Two issuers keep the tensor pipe fed while either waits.
     if (lane == 0) {
       const uint32_t half = static_cast<uint32_t>(warp - 2);  // tile parity
-      const uint32_t idS = idesc_bf16_f32(128, TP_TOK, false, false);
+      const uint32_t idS = FP8 ? idesc_f16_f32(128, TP_TOK, false, false)
+                               : idesc_bf16_f32(128, TP_TOK, false, false);
       const uint64_t dQc = smem_desc(smem_u32(sm.qc), 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(smem_u32(sm.qr), 16, 512, kSwizzle64B);
       const uint64_t dKc0 = smem_desc(smem_u32(sm.kv[0].c[0]), 16, 1024, kSwizzle128B);
       const uint64_t dKr0 = smem_desc(smem_u32(sm.kv[0].r), 16, 512, kSwizzle64B);
-      constexpr uint32_t kStageDesc = sizeof(PairSmem::Stage) >> 4;  // stage stride, 16-B units
+      constexpr uint32_t kStageDesc = sizeof(typename Smem::Stage) >> 4;  // stage stride, 16-B units
       const uint32_t dS = tmem + TM_S + 64 * half;
       bool ok = true;
       TileCursor cur;
@@ -561,8 +708,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
             ok = false;
             break;
           }
-          const int s = t % TP_STAGES;
-          if (!mbar_wait(&sm.kv_full[s], (t / TP_STAGES) & 1, WAIT_LIMIT)) { ok = false; break; }
+          const int s = t % NS;
+          if (!mbar_wait(&sm.kv_full[s], (t / NS) & 1, WAIT_LIMIT)) { ok = false; break; }
           tc_fence_after();
           const uint64_t dK = dKc0 + s * kStageDesc;
 #pragma unroll
@@ -626,6 +773,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     float l = 0.f, m = -INFINITY;
     int L = 0, rows_valid = 0, pos_q = 0;
     bool row_ok = false, bad = false;
+    // fp8 cache: cv walks the tiles two ahead of cur, converting each into
+    // its compute stage (the first two before the loop).
+    TileCursor cv;
+    if constexpr (FP8) {
+      cv.init(it_begin, it_end, a, pair);
+      for (int k = 0; k < 2 && cv.valid() && !bad; ++k, cv.next(a))
+        bad = !convert_tile(sm, a, cv, gtid, lane);
+    }
     // The two warps of a lane quarter leave the loop together, right after a
     // pair barrier has merged their timeout flags, so neither can be left
     // waiting at a named barrier.
@@ -642,7 +797,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
         pos_q = L - a.n_q + (row_ok ? (cur.pc.g * TP_ROWS + row) / a.n_h : 0);
       }
       const int t = cur.tile();
-      const int s2 = kv % TP_STAGES;
+      const int s2 = kv % NS;
 
       // 1. full scaled scores = own fp16-rounded partial (written back into
       // the score slot by the sender warps) + the peer's (exchange buffer)
@@ -673,6 +828,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
           }
         }
       }
+      if constexpr (FP8) {
+        // x_j = q . code_j; the score is scale_j x_j. (The scales were
+        // written by these warps, released on the stage's full barrier.)
+        bad |= !mbar_wait(&sm.kv_full[s2], (kv / NS) & 1, WAIT_LIMIT);
+        const float* ks = sm.f8.kscale[s2] + 32 * hh;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sc[c] *= ks[c];
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -688,12 +851,23 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
 #pragma unroll
         for (int c = 0; c < 32; ++c) sc[c] = (row_ok && j0 + c <= pos_q) ? sc[c] : -INFINITY;
       }
-      float pm[4];
+      if constexpr (FP8) {
+        // The running max tracks s_j + log2(scale_j), so that the value
+        // weights p_j scale_j stay below 2^8 (fp16 range); l keeps the sum
+        // of p_j itself. Any common reference cancels in O / l.
+        const float* kl = sm.f8.klscale[s2] + 32 * hh;
+        float pm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        pm[u] = fmaxf(fmaxf(fmaxf(sc[8 * u], sc[8 * u + 1]), fmaxf(sc[8 * u + 2], sc[8 * u + 3])),
-                      fmaxf(fmaxf(sc[8 * u + 4], sc[8 * u + 5]), fmaxf(sc[8 * u + 6], sc[8 * u + 7])));
-      sm.xmax[b][hh][row] = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+        for (int c = 0; c < 32; ++c) pm = fmaxf(pm, sc[c] + kl[c]);
+        sm.xmax[b][hh][row] = pm;
+      } else {
+        float pm[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pm[u] = fmaxf(fmaxf(fmaxf(sc[8 * u], sc[8 * u + 1]), fmaxf(sc[8 * u + 2], sc[8 * u + 3])),
+                        fmaxf(fmaxf(sc[8 * u + 4], sc[8 * u + 5]), fmaxf(sc[8 * u + 6], sc[8 * u + 7])));
+        sm.xmax[b][hh][row] = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+      }
       if (named_bar_or(bar_id, 64, bad)) {
         bad = true;
         break;
@@ -707,22 +881,30 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       // instead maps its -inf scores to 2^-inf = 0 rather than NaN.
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
 
-      // 3. P (bf16 pairs) into the TMEM buffer, once the previous tile's
-      // value MMA has read it
-      if (kv >= 1) bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
-      bad = __any_sync(0xffffffffu, bad);
-      tc_fence_after();
+      // 3. P (bf16 pairs; fp8 cache: p_j scale_j in fp16 pairs) into the
+      // TMEM buffer, once the previous tile's value MMA has read it
       {
         float psum = 0.f;
         uint32_t w[16];
+        const float* ks = nullptr;
+        if constexpr (FP8) ks = sm.f8.kscale[s2] + 32 * hh;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const float p0 = fast_exp2(sc[2 * k] - m_sub);
           const float p1 = fast_exp2(sc[2 * k + 1] - m_sub);
           psum += p0 + p1;
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+          if constexpr (FP8) {
+            const __half2 ph = __floats2half2_rn(p0 * ks[2 * k], p1 * ks[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&ph);
+          } else {
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            w[k] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
         }
+        if (kv >= 1)
+          bad |= !mbar_wait(&sm.pv_done[(kv - 1) & 1], ((kv - 1) >> 1) & 1, WAIT_LIMIT);
+        bad = __any_sync(0xffffffffu, bad);
+        tc_fence_after();
         if (!bad) tmem_st16u(tmem + lane_base + TM_P + 16 * hh, w);
         tmem_wait_st();
         if (row_ok) l = (m_old == -INFINITY) ? psum : l * fast_exp2(m_old - m_use) + psum;
@@ -748,8 +930,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
 
       // Rows past the end of the sequence may hold anything; zero their
       // latent columns so that 0 * garbage cannot reach the accumulator.
+      // (The fp8 conversion already wrote zeros there.)
       const int jt = t * TP_TOK;
-      if (jt + TP_TOK > L) {
+      if (!FP8 && jt + TP_TOK > L) {
         const int r0 = max(L - jt, 0);            // first invalid row in this tile
         const int n16 = (TP_TOK - r0) * 4 * 8;    // rows x boxes x 16-byte units
         for (int i2 = gtid; i2 < n16; i2 += TP_SM_WARPS * 32) {
@@ -761,6 +944,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[b]);
+      if constexpr (FP8) {
+        // tile kv + 2 goes into the compute stage of tile kv - 1, whose
+        // value MMAs are done (waited for above)
+        if (cv.valid() && !bad) {
+          bad = !convert_tile(sm, a, cv, gtid, lane);
+          cv.next(a);
+        }
+      }
 
       if (cur.last()) {
         // ---- epilogue of the piece: O / l -> workspace slot
@@ -830,29 +1021,34 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   }
 }
 
-size_t smem_bytes() { return sizeof(PairSmem) + 1024; }
+template <bool FP8>
+size_t smem_bytes() { return sizeof(PairSmemT<FP8>) + 1024; }
 
+template <bool FP8>
 bool set_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && done[dev]) return true;
-  if (cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_bytes())) != cudaSuccess)
+  if (cudaFuncSetAttribute(attend_tc_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes<FP8>())) != cudaSuccess)
     return false;
   if (dev >= 0 && dev < 64) done[dev] = true;
   return true;
 }
 
+// A [rows][576] matrix of 16-bit (bf16 or fp16) or 8-bit elements, boxes of
+// box_cols x box_rows.
 bool rows_map(TmapSpec* sp, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
-              CUtensorMapSwizzle sw) {
+              CUtensorMapSwizzle sw,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   *sp = TmapSpec{};
-  sp->dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  sp->dtype = dt;
   sp->rank = 2;
   sp->base = base;
   sp->dims[0] = 576;
   sp->dims[1] = rows;
-  sp->strides[0] = 576 * 2;
+  sp->strides[0] = 576 * (dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2);
   sp->box[0] = box_cols;
   sp->box[1] = box_rows;
   sp->swizzle = sw;
@@ -890,14 +1086,14 @@ bool attend_tc_supported(const Shape& s, mla_dtype dt) {
 // Number of CTA pairs that can be resident at once (the attention grid is
 // that many clusters of two), or 0 if the kernel cannot be configured.
 int attend_tc_max_pairs() {
-  if (!set_smem_attr()) {
+  if (!set_smem_attr<false>() || !set_smem_attr<true>()) {
     cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(TP_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.dynamicSmemBytes = smem_bytes<false>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -906,37 +1102,56 @@ int attend_tc_max_pairs() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
-                             const int32_t* page_table, int max_blocks, int B, int n_q,
-                             const Partition& p, const WsView& ws, const int32_t* seq_lens,
-                             uint32_t* err, cudaStream_t st) {
+namespace {
+
+// Shared by the bf16 and fp8 launches: the kernel, its tensor maps, the
+// pair grid of 2-CTA clusters and programmatic dependent launch.
+template <bool FP8>
+cudaError_t launch_pairs(const Shape& s, const void* cache, const float* row_scale,
+                         int num_blocks, const int32_t* page_table, int max_blocks, int B,
+                         int n_q, const Partition& p, const WsView& ws, const int32_t* seq_lens,
+                         uint32_t* err, cudaStream_t st) {
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * s.n_h;
   const uint64_t kv_rows = static_cast<uint64_t>(num_blocks) * TP_TOK;
+  const CUtensorMapDataType qdt =
+      FP8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   TmapSpec sp;
   CUtensorMap tqc, tqr, tkc, tkr;
-  rows_map(&sp, ws.qabs, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  rows_map(&sp, ws.qabs, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, qdt);
   if (!get_tmap(sp, &tqc)) return cudaErrorInvalidValue;
-  rows_map(&sp, ws.qabs, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+  rows_map(&sp, ws.qabs, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B, qdt);
   if (!get_tmap(sp, &tqr)) return cudaErrorInvalidValue;
-  // A stage's four latent boxes as one 3-D box; if the driver does not take
-  // that view, four 2-D boxes.
-  bool chunked = true;
-  chunks_map(&sp, cache, kv_rows, 64, 4);
-  if (!get_tmap(sp, &tkc)) chunked = false;
-  if (!chunked) {
-    rows_map(&sp, cache, kv_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  bool chunked = false;
+  if constexpr (FP8) {
+    // e4m3 codes, unswizzled: a stage's 256 latent codes x 64 rows, and its
+    // 32 rotary codes x 64 rows
+    rows_map(&sp, cache, kv_rows, 256, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_DATA_TYPE_UINT8);
     if (!get_tmap(sp, &tkc)) return cudaErrorInvalidValue;
+    rows_map(&sp, cache, kv_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (!get_tmap(sp, &tkr)) return cudaErrorInvalidValue;
+  } else {
+    // A stage's four latent boxes as one 3-D box; if the driver does not take
+    // that view, four 2-D boxes.
+    chunked = true;
+    chunks_map(&sp, cache, kv_rows, 64, 4);
+    if (!get_tmap(sp, &tkc)) chunked = false;
+    if (!chunked) {
+      rows_map(&sp, cache, kv_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (!get_tmap(sp, &tkc)) return cudaErrorInvalidValue;
+    }
+    rows_map(&sp, cache, kv_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!get_tmap(sp, &tkr)) return cudaErrorInvalidValue;
   }
-  rows_map(&sp, cache, kv_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!get_tmap(sp, &tkr)) return cudaErrorInvalidValue;
-  if (!set_smem_attr()) return cudaErrorInvalidValue;
+  if (!set_smem_attr<FP8>()) return cudaErrorInvalidValue;
   PairArgs a;
   a.page_table = page_table;
   a.seq_lens = seq_lens;
@@ -946,7 +1161,8 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   a.first_b = ws.first_b;
   a.part_o = ws.part_o;
   a.part_lse = ws.part_lse;
-  a.qabs = static_cast<const __nv_bfloat16*>(ws.qabs);
+  a.qabs = static_cast<const uint16_t*>(ws.qabs);
+  a.row_scale = row_scale;
   a.q_rows = static_cast<long long>(q_rows);
   a.chunked = chunked ? 1 : 0;
   a.err = err;
@@ -960,7 +1176,7 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.C, 1, 1);
   cfg.blockDim = dim3(TP_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.dynamicSmemBytes = smem_bytes<FP8>();
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -973,7 +1189,25 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attend_tc_kernel, tqc, tqr, tkc, tkr, a);
+  return cudaLaunchKernelEx(&cfg, attend_tc_kernel<FP8>, tqc, tqr, tkc, tkr, a);
+}
+
+}  // namespace
+
+cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
+                             const int32_t* page_table, int max_blocks, int B, int n_q,
+                             const Partition& p, const WsView& ws, const int32_t* seq_lens,
+                             uint32_t* err, cudaStream_t st) {
+  return launch_pairs<false>(s, cache, nullptr, num_blocks, page_table, max_blocks, B, n_q, p, ws,
+                             seq_lens, err, st);
+}
+
+cudaError_t launch_attend_tc_fp8(const Shape& s, const void* codes, const float* row_scale,
+                                 int num_blocks, const int32_t* page_table, int max_blocks, int B,
+                                 int n_q, const Partition& p, const WsView& ws,
+                                 const int32_t* seq_lens, uint32_t* err, cudaStream_t st) {
+  return launch_pairs<true>(s, codes, row_scale, num_blocks, page_table, max_blocks, B, n_q, p,
+                            ws, seq_lens, err, st);
 }
 
 }  // namespace mla

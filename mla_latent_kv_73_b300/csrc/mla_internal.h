@@ -93,6 +93,18 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st);
+// The append's rows [x W_dkv | RoPE(x W_kr, pos)] in fp32, dense ([T][R], row
+// t for token t), for the fp8 quantiser; nothing is written to a cache.
+cudaError_t launch_append_rows_f32(const Shape& s, mla_dtype dt, const Weights* w, const void* x,
+                                   const int32_t* seq_idx, const int32_t* pos, int T,
+                                   float* rows, uint32_t* err, cudaStream_t st);
+
+// fp8 (e4m3) latent cache: dense fp32 rows -> one scale per row and e4m3
+// codes, placed through the page table (fp8.cu).
+cudaError_t launch_quantize_rows_fp8(const Shape& s, const float* rows, const int32_t* seq_idx,
+                                     const int32_t* pos, const int32_t* page_table, int B,
+                                     int max_blocks, uint8_t* codes, float* row_scale,
+                                     int num_blocks, int T, uint32_t* err, cudaStream_t st);
 
 // out_scale multiplies q_lat and q_pe before they are stored (the
 // tensor-core attention folds scale * log2(e) in here). q_f32: store them in
@@ -116,14 +128,22 @@ cudaError_t launch_attend_tc(const Shape& s, const void* cache, int num_blocks,
                              const int32_t* page_table, int max_blocks, int B, int n_q,
                              const Partition& p, const WsView& ws, const int32_t* seq_lens,
                              uint32_t* err, cudaStream_t st);
+// The same over an fp8 (e4m3) cache with one fp32 scale per row
+// (row_scale[num_blocks * 64]); the queries in the workspace are fp16.
+cudaError_t launch_attend_tc_fp8(const Shape& s, const void* codes, const float* row_scale,
+                                 int num_blocks, const int32_t* page_table, int max_blocks, int B,
+                                 int n_q, const Partition& p, const WsView& ws,
+                                 const int32_t* seq_lens, uint32_t* err, cudaStream_t st);
 
 // Tensor-core absorption and combine (bf16, d_c = 512, d_nope = 128, d_r = 64,
 // d_v = 128). The query pointer must be 16-byte aligned for the TMA.
+// q_half: store the absorbed queries in fp16 (for the attention over an fp8
+// cache) instead of bf16.
 bool absorb_tc_supported(const Shape& s, mla_dtype dt);
 cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
                                const int32_t* seq_lens, int max_blocks, int B, int n_q,
                                const Partition& p, const WsView& ws, float out_scale,
-                               uint32_t* err, cudaStream_t st);
+                               bool q_half, uint32_t* err, cudaStream_t st);
 bool combine_tc_supported(const Shape& s, mla_dtype dt);
 cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
                               const Partition& p, const WsView& ws, float* out, uint32_t* err,

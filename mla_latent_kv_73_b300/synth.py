@@ -26,7 +26,7 @@ import math
 import numpy as np
 
 # Sub-stream ids
-_S_WEIGHTS, _S_LENS, _S_PAGES, _S_CACHE, _S_Q, _S_X = 1, 2, 3, 4, 5, 6
+_S_WEIGHTS, _S_LENS, _S_PAGES, _S_CACHE, _S_Q, _S_X, _S_FP8 = 1, 2, 3, 4, 5, 6, 7
 
 
 @dataclasses.dataclass(frozen=True)
@@ -222,3 +222,47 @@ def hidden_states(w: Workload, T, stream=0):
     """Hidden states x [T, d_model] ~ N(0, 1): (values float32, storage)."""
     a = normal(rng(w.seed, _S_X, stream), (int(T), w.d_model))
     return to_dtype(a, w.dtype)
+
+
+def fp8_sequence_codes(w: Workload, b, L):
+    """Cache rows of sequence b for an fp8 (e4m3) cache, drawn directly as
+    codes: (codes uint8 [L, R], row scales float32 [L]).
+
+    Each code byte is assembled from a sign bit, a 4-bit exponent field drawn
+    around 12 (magnitudes near 2^5) and a uniform 3-bit mantissa; the NaN
+    pattern (exponent 15 with mantissa 7) is never drawn. Row scales are
+    uniform in [1/320, 1/96], so the rows' values have a standard deviation
+    near one, like the bf16 workloads' rows. No
+    rounding or quantisation happens here: both sides decode these bytes.
+    """
+    g = rng(w.seed, _S_FP8, b)
+    L = int(L)
+    e = np.clip(np.rint(g.normal(12.0, 2.0, size=(L, w.R))), 0, 15).astype(np.uint8)
+    m = g.integers(0, 8, size=(L, w.R), dtype=np.uint8)
+    m = np.where((e == 15) & (m == 7), np.uint8(6), m)
+    sign = g.integers(0, 2, size=(L, w.R), dtype=np.uint8)
+    codes = (sign << 7) | (e << 3) | m
+    scales = g.uniform(1 / 320, 1 / 96, size=L).astype(np.float32)
+    return codes.astype(np.uint8), scales
+
+
+def fill_paged_cache_fp8(w: Workload, lens, pt, num_blocks, keep=None):
+    """Paged fp8 cache holding every sequence: (codes [num_blocks, bs, R]
+    uint8, scales [num_blocks, bs] float32, per-sequence (codes, scales)).
+    Rows no sequence owns hold code 0 and scale 0. ``keep`` as for
+    fill_paged_cache."""
+    bs = w.block_size
+    codes = np.zeros((num_blocks * bs, w.R), dtype=np.uint8)
+    scales = np.zeros(num_blocks * bs, dtype=np.float32)
+    per_seq = [None] * len(lens)
+    for b, L in enumerate(lens):
+        c, sc = fp8_sequence_codes(w, b, L)
+        if keep is None or b in keep:
+            per_seq[b] = (c, sc)
+        nb = (int(L) + bs - 1) // bs
+        for k in range(nb):
+            lo, hi = k * bs, min((k + 1) * bs, int(L))
+            p = int(pt[b, k])
+            codes[p * bs:p * bs + (hi - lo)] = c[lo:hi]
+            scales[p * bs:p * bs + (hi - lo)] = sc[lo:hi]
+    return codes.reshape(num_blocks, bs, w.R), scales.reshape(num_blocks, bs), per_seq
