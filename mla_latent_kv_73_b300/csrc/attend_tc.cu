@@ -104,6 +104,10 @@ constexpr int TP_ROWS = 128;                  // query rows per group (MMA M)
 constexpr int TP_TOK = 64;                    // tokens per tile = page size
 constexpr int TP_STAGES = 4;
 constexpr int TP_THREADS = 512;
+constexpr int F8_CONV_WARP0 = 16;             // fp8 cache: first converter warp
+constexpr int F8_CONV_WARPS = 4;
+template <bool FP8>
+constexpr int kThreads = FP8 ? TP_THREADS + 32 * F8_CONV_WARPS : TP_THREADS;
 constexpr int TP_SEND_WARP0 = 4;              // first sender warp
 constexpr int TP_SM_WARP0 = 8;                // first softmax warp
 constexpr int TP_SM_WARPS = 8;
@@ -428,17 +432,17 @@ __device__ __forceinline__ void e4m3x16_to_f16(const uint4& v, uint32_t (&w)[8])
   }
 }
 
-// fp8 cache: the softmax warps (thread gtid of 256) convert tile cv.kv from
-// its e4m3 ring stage into its fp16 compute stage, in the layout the TMA
+// fp8 cache: the converter warps (thread ctid of NTHR) convert tile cv.kv
+// from its e4m3 ring stage into its fp16 compute stage, in the layout the TMA
 // gives the bf16 stages (four 128-byte-swizzled latent boxes, one
 // 64-byte-swizzled rotary box), and copy the page's row scales (and their
 // log2) beside it. Rows past the sequence's end become zeros with scale 0,
 // whatever the cache holds there. Each warp then arrives on the compute
 // stage's full barrier and the ring stage's empty barrier. Returns false on
 // a timeout (nothing converted, nothing arrived).
-template <class SM>
+template <int NTHR, class SM>
 __device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const TileCursor& cv,
-                                             int gtid, int lane) {
+                                             int ctid, int lane) {
   const uint32_t j = cv.kv;
   const int s8 = j % F8_STAGES, sc = j % F8_KV_STAGES;
   bool ok = true;
@@ -452,7 +456,7 @@ __device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const Ti
   const F8Stage& f = sm.f8.st[s8];
   auto& dst = sm.kv[sc];
   constexpr int kUnits = 18;  // 16-byte input units per row: 16 latent, 2 rotary
-  for (int k = gtid; k < TP_TOK * kUnits; k += TP_SM_WARPS * 32) {
+  for (int k = ctid; k < TP_TOK * kUnits; k += NTHR) {
     const int r = k / kUnits, u = k - r * kUnits;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < valid)
@@ -476,11 +480,11 @@ __device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const Ti
     *reinterpret_cast<uint4*>(row + ua * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(row + ub * 16) = make_uint4(w[4], w[5], w[6], w[7]);
   }
-  if (gtid < TP_TOK) {
-    const bool in = gtid < valid;
-    const float sv = in ? f.s[gtid] : 0.f;
-    sm.f8.kscale[sc][gtid] = sv;
-    sm.f8.klscale[sc][gtid] = in ? __log2f(sv) : -INFINITY;
+  for (int k = ctid; k < TP_TOK; k += NTHR) {
+    const bool in = k < valid;
+    const float sv = in ? f.s[k] : 0.f;
+    sm.f8.kscale[sc][k] = sv;
+    sm.f8.klscale[sc][k] = in ? __log2f(sv) : -INFINITY;
   }
   fence_proxy_async_smem();  // the converted tile is read by the MMAs
   __syncwarp();
@@ -492,7 +496,7 @@ __device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const Ti
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(TP_THREADS, 1)
+__global__ void __launch_bounds__(kThreads<FP8>, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
                  const __grid_constant__ CUtensorMap tmap_qr,
                  const __grid_constant__ CUtensorMap tmap_kc,
@@ -510,14 +514,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
   // the query-absorption kernel, whose outputs are read only after the wait.
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      // bf16: the TMA's bytes; fp8: the eight converting softmax warps
-      mbar_init(&sm.kv_full[s], FP8 ? TP_SM_WARPS : 1);
+      // bf16: the TMA's bytes; fp8: the converter warps
+      mbar_init(&sm.kv_full[s], FP8 ? F8_CONV_WARPS : 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
     if constexpr (FP8) {
       for (int s = 0; s < F8_STAGES; ++s) {
         mbar_init(&sm.f8.full[s], 1);
-        mbar_init(&sm.f8.empty[s], TP_SM_WARPS);
+        mbar_init(&sm.f8.empty[s], F8_CONV_WARPS);
       }
     }
     mbar_init(&sm.q_full, 1 + 4);  // TMA bytes + the four sender warps' TMEM part
@@ -754,6 +758,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     }
     if (leader) bulk_wait_all();  // the last copies land before the peer may leave
     if (bad && lane == 0) note_timeout(sm, a.err);
+  } else if (warp >= F8_CONV_WARP0) {
+    // ------------------------------------------------------------ fp8 converter warps 16..19
+    // Each tile as soon as its codes have landed and its compute stage is
+    // free, independently of the other roles (no named barriers here).
+    if constexpr (FP8) {
+      const int ctid = (warp - F8_CONV_WARP0) * 32 + lane;
+      TileCursor cv;
+      cv.init(it_begin, it_end, a, pair);
+      bool bad = false;
+      for (; cv.valid() && !bad && !aborted(sm); cv.next(a))
+        bad = !convert_tile<32 * F8_CONV_WARPS>(sm, a, cv, ctid, lane);
+      if (bad && lane == 0) note_timeout(sm, a.err);
+    }
   } else {
     // ------------------------------------------------------------ softmax warps 8..15
     // Warp w reads TMEM lane quarter w % 4 (query rows 32 (w % 4) .. +31, one
@@ -773,14 +790,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
     float l = 0.f, m = -INFINITY;
     int L = 0, rows_valid = 0, pos_q = 0;
     bool row_ok = false, bad = false;
-    // fp8 cache: cv walks the tiles two ahead of cur, converting each into
-    // its compute stage (the first two before the loop).
-    TileCursor cv;
-    if constexpr (FP8) {
-      cv.init(it_begin, it_end, a, pair);
-      for (int k = 0; k < 2 && cv.valid() && !bad; ++k, cv.next(a))
-        bad = !convert_tile(sm, a, cv, gtid, lane);
-    }
     // The two warps of a lane quarter leave the loop together, right after a
     // pair barrier has merged their timeout flags, so neither can be left
     // waiting at a named barrier.
@@ -944,14 +953,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.p_full[b]);
-      if constexpr (FP8) {
-        // tile kv + 2 goes into the compute stage of tile kv - 1, whose
-        // value MMAs are done (waited for above)
-        if (cv.valid() && !bad) {
-          bad = !convert_tile(sm, a, cv, gtid, lane);
-          cv.next(a);
-        }
-      }
 
       if (cur.last()) {
         // ---- epilogue of the piece: O / l -> workspace slot
@@ -1175,7 +1176,7 @@ cudaError_t launch_pairs(const Shape& s, const void* cache, const float* row_sca
   a.P = p.C;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.C, 1, 1);
-  cfg.blockDim = dim3(TP_THREADS, 1, 1);
+  cfg.blockDim = dim3(kThreads<FP8>, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes<FP8>();
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

@@ -246,6 +246,18 @@ def fp8_sequence_codes(w: Workload, b, L):
     return codes.astype(np.uint8), scales
 
 
+def fp8_uniform_codes(w: Workload, b, L):
+    """Like fp8_sequence_codes, but every finite e4m3 code (all 254 bytes
+    except the two NaN patterns, subnormals and +-448 included) is equally
+    likely; row scales uniform in [1/4096, 1/1024]."""
+    g = rng(w.seed, _S_FP8, 1000 + b)
+    L = int(L)
+    c = g.integers(0, 254, size=(L, w.R), dtype=np.int64)
+    c = c + (c >= 0x7F) + (c >= 0xFE)   # skip 0x7f and 0xff
+    scales = g.uniform(1 / 4096, 1 / 1024, size=L).astype(np.float32)
+    return c.astype(np.uint8), scales
+
+
 def fill_paged_cache_fp8(w: Workload, lens, pt, num_blocks, keep=None):
     """Paged fp8 cache holding every sequence: (codes [num_blocks, bs, R]
     uint8, scales [num_blocks, bs] float32, per-sequence (codes, scales)).

@@ -160,7 +160,7 @@ class Fp8Run:
     rows are random bytes drawn on the device (their outputs are not
     checked)."""
 
-    def __init__(self, w, lens, keep=None, spare_blocks=2):
+    def __init__(self, w, lens, keep=None, spare_blocks=2, uniform=False):
         self.w, self.lens = w, lens
         self.cfg = config_for(w)
         self.wts = synth.weights(w)
@@ -181,7 +181,8 @@ class Fp8Run:
         flat_c = self.cache.view(-1, w.R)
         flat_s = self.scales.view(-1)
         for b in want:
-            c, sc = synth.fp8_sequence_codes(w, b, lens[b])
+            gen_codes = synth.fp8_uniform_codes if uniform else synth.fp8_sequence_codes
+            c, sc = gen_codes(w, b, lens[b])
             idx = np.array([O.paged_row_index(pt, b, j, bs) for j in range(int(lens[b]))])
             ti = torch.from_numpy(idx.astype(np.int64)).cuda()
             flat_c.index_copy_(0, ti, torch.from_numpy(c).cuda())
@@ -214,13 +215,16 @@ SMALL = {
     "causal_nq2": dict(lens=(2, 65, 129, 640), n_q=2),
     "nh16": dict(n_h=16, lens=(1, 17, 64, 100, 129, 250, 333, 400, 3)),
     "one_long_seq": dict(lens=(64 * 37 + 5,)),
+    "all_codes": dict(lens=(3, 130, 700), uniform=True),
 }
 
 
 @pytest.mark.parametrize("case", list(SMALL))
 def test_decode_fp8_small(case):
-    w, lens = small(**SMALL[case])
-    r = Fp8Run(w, lens)
+    kw = dict(SMALL[case])
+    uniform = kw.pop("uniform", False)
+    w, lens = small(**kw)
+    r = Fp8Run(w, lens, uniform=uniform)
     got = r.decode()
     st, code = _lib.mla_get_last_device_error()
     assert code == 0
