@@ -118,9 +118,11 @@ typedef struct mla_weights_s* mla_weights; /* opaque, library-owned */
  * W_uv to the output side).
  *   W_dkv [d_model, d_c], W_kr [d_model, d_r]       row-major, cfg->dtype
  *   W_uk  [d_c, n_h*d_nope], W_uv [d_c, n_h*d_v]   row-major, cfg->dtype
- * Allocates library-owned device buffers, queues the repacking kernels on
- * `stream`, and returns the handle in *out. The caller's weight buffers may
- * be freed once `stream` has passed this call. Release the handle with
+ * Allocates library-owned device buffers, runs the repacking kernels on
+ * `stream` and waits for them, then returns the handle in *out. The packed
+ * weights are complete and never written again while the handle lives, so
+ * the decode kernels may load them before the previous kernel on their
+ * stream has finished. The caller's weight buffers may be freed on return. Release the handle with
  * mla_weights_free. The handle is bound to the config it was built with and
  * to the current device. */
 mla_status mla_absorb_weights(const mla_config* cfg, const void* W_dkv, const void* W_kr,

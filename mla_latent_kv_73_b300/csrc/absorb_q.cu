@@ -32,7 +32,7 @@ constexpr int AQ_TOK = 16, AQ_THREADS = 256;
 template <typename T, typename QT>
 __global__ void __launch_bounds__(AQ_THREADS)
 absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
-                const double* __restrict__ inv_freq, const int32_t* __restrict__ seq_lens, int B,
+                const uint64_t* __restrict__ rope_turns, const int32_t* __restrict__ seq_lens, int B,
                 int n_q, int max_blocks, int TS, int G, int C, int K, float out_scale,
                 QT* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
                 int32_t* first_b, uint32_t* err) {
@@ -114,7 +114,7 @@ absorb_q_kernel(Shape s, const T* __restrict__ q, const T* __restrict__ w_uk,
     const T* qr = q + (static_cast<size_t>(tok) * s.n_h + h) * dq + s.d_nope;
     const float x1 = to_f32<T>(qr[k]), x2 = to_f32<T>(qr[k + half]);
     float c, sn;
-    rope_cos_sin(pos, inv_freq[k], &c, &sn);
+    rope_cos_sin(pos, rope_turns[k], &c, &sn);
     QT* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + s.d_c;
     o[k] = from_f32<QT>((x1 * c - x2 * sn) * out_scale);
     o[k + half] = from_f32<QT>((x1 * sn + x2 * c) * out_scale);
@@ -135,7 +135,7 @@ cudaError_t absorb_q_t(const Shape& s, const Weights* w, const void* q, const in
     if (e != cudaSuccess) return e;
   }
   absorb_q_kernel<T, QT><<<grid, AQ_THREADS, smem, st>>>(
-      s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->inv_freq, seq_lens, B, n_q,
+      s, static_cast<const T*>(q), static_cast<const T*>(w->w_uk), w->rope_turns, seq_lens, B, n_q,
       max_blocks, p.TS, p.G, p.C, p.K, out_scale, static_cast<QT*>(ws.qabs), ws.tiles, ws.prefix,
       ws.bounds, ws.first_b, err);
   return cudaGetLastError();

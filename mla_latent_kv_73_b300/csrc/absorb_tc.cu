@@ -12,8 +12,8 @@
 //
 // Per head this is a dense [512 x 128] x [128 x tokens] product, so it runs on
 // tcgen05: one CTA per (head, up to 128 query tokens). TMA stages the head's
-// whole W_uk slice (128 KB, eight 128 x 64 boxes) and the tokens' q_nope
-// (a 3-D box over [token][head][dim]) into shared memory in one go, so the
+// whole W_uk slice (128 KB, eight 128 x 64 boxes) and the tokens' q (three
+// 3-D boxes over [token][head][dim]) into shared memory in one go, so the
 // weight stream has 128 KB in flight per SM. Four threads (one per 128-row
 // block of W_uk[h], each starting as soon as its two boxes have landed) issue
 // 8 MMAs each with M = 128 latent rows, N = tokens, K = 128, accumulating
@@ -42,7 +42,7 @@ constexpr long long AT_WAIT = 2000000000LL;    // ~1 s
 
 struct __align__(1024) AbsSmem {
   uint8_t w[8][AT_WBOX];          // box (M-block j, K-chunk kc) at index 2*j + kc
-  uint8_t q[2][AT_TOK * 128];     // K-chunk kc: token rows of 128 B
+  uint8_t q[3][AT_TOK * 128];     // K-chunks 0, 1 of q_nope, then q_rope: token rows of 128 B
   uint64_t full_q, full_w[4], done;
   uint32_t tmem_base;
 };
@@ -55,7 +55,7 @@ template <typename OT>
 __global__ void __launch_bounds__(AT_THREADS, 1)
 absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_q, Shape s,
-                   const __nv_bfloat16* __restrict__ q, const double* __restrict__ inv_freq,
+                   const __nv_bfloat16* __restrict__ q, const uint64_t* __restrict__ rope_turns,
                    const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
                    int G, int C, int K, int n_tok_box, float out_scale,
                    OT* __restrict__ qabs, int32_t* tiles, int32_t* prefix,
@@ -87,24 +87,23 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   bool ok = true;
 
   // With programmatic dependent launch this CTA may start while the previous
-  // kernel (the append) still runs: pull W_uk[h] into L2 (coherent, so safe
-  // at any time), then wait for that kernel before loading anything into the
-  // SM or reading the queries.
+  // kernel (the append) still runs. The packed W_uk is complete and never
+  // written once its handle exists (mla_absorb_weights returns after the
+  // packing kernels), so its loads start at once; the queries are read only
+  // after the wait for the previous kernel.
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_q);
-    for (int j = 0; j < 4; ++j)
-      for (int kc = 0; kc < 2; ++kc) tma_prefetch_2d(&tmap_w, 64 * kc, h * 512 + 128 * j);
-  }
-  griddep_wait();
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&sm.full_q, 2 * n_tok_box * 128);
-    for (int kc = 0; kc < 2; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full_q);
     for (int j = 0; j < 4; ++j) {
       mbar_arrive_expect_tx(&sm.full_w[j], 2 * AT_WBOX);
       for (int kc = 0; kc < 2; ++kc)
         tma_load_2d(sm.w[2 * j + kc], &tmap_w, 64 * kc, h * 512 + 128 * j, &sm.full_w[j]);
     }
+  }
+  griddep_wait();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&sm.full_q, 3 * n_tok_box * 128);
+    for (int kc = 0; kc < 3; ++kc) tma_load_3d(sm.q[kc], &tmap_q, 64 * kc, h, t0, &sm.full_q);
   }
   // The attention kernel may be scheduled now; it waits for this grid to
   // complete before it reads the queries or the plan.
@@ -131,41 +130,74 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
   }
 
   if (warp >= 4) {
-    // rotary block of each query, rotated at the query's own position
-    for (int i = threadIdx.x - 128; i < ntok * 32; i += 128) {
-      const int tt = i / 32, k = i % 32;
-      const int tok = t0 + tt, b = tok / n_q, qi = tok % n_q;
-      const int pos = seq_lens[b] - n_q + qi;
-      const __nv_bfloat16* qr = q + (static_cast<size_t>(tok) * s.n_h + h) * DQ + 128;
-      const float x1 = __bfloat162float(qr[k]), x2 = __bfloat162float(qr[k + 32]);
-      float c, sn;
-      rope_cos_sin(pos, inv_freq[k], &c, &sn);
-      OT* o = qabs + (static_cast<size_t>(tok) * s.n_h + h) * R + 512;
-      o[k] = from_f32<OT>((x1 * c - x2 * sn) * out_scale);
-      o[k + 32] = from_f32<OT>((x1 * sn + x2 * c) * out_scale);
+    // rotary block of each query, rotated at the query's own position, from
+    // the q_rope box the TMA put in shared memory (128-byte swizzle: dims
+    // [8u, 8u + 8) of token row t sit in 16-byte unit u ^ (t & 7)). Lane k
+    // owns rotary pair (k, k + 32); warp w4 takes tokens w4, w4 + 4, ...
+    const int k = lane, w4 = warp - 4;
+    const uint64_t turns = rope_turns[k];
+    const bool qok = mbar_wait(&sm.full_q, 0, AT_WAIT);
+    if (!qok && k == 0) set_error(err, MLA_DEVERR_TIMEOUT);
+    const uint8_t* qr = sm.q[2];
+    // four tokens at a time: their loads and angle computations are
+    // independent, so their latencies overlap
+    constexpr int U = 4;
+    for (int tb = w4; qok && tb < ntok; tb += 4 * U) {
+      int pos[U];
+      float x1[U], x2[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int tt = min(tb + 4 * u, ntok - 1), tok = t0 + tt;
+        pos[u] = seq_lens[tok / n_q] - n_q + tok % n_q;
+        const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(qr + tt * 128);
+        x1[u] = __bfloat162float(row[(((k >> 3) ^ (tt & 7)) << 3) + (k & 7)]);
+        x2[u] = __bfloat162float(row[((((k + 32) >> 3) ^ (tt & 7)) << 3) + (k & 7)]);
+      }
+      float c[U], sn[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) rope_cos_sin(pos[u], turns, &c[u], &sn[u]);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int tt = tb + 4 * u;
+        if (tt >= ntok) break;
+        OT* o = qabs + (static_cast<size_t>(t0 + tt) * s.n_h + h) * R + 512;
+        o[k] = from_f32<OT>((x1[u] * c[u] - x2[u] * sn[u]) * out_scale);
+        o[k + 32] = from_f32<OT>((x1[u] * sn[u] + x2[u] * c[u]) * out_scale);
+      }
     }
   } else {
-    // q_lat^T from TMEM: lane = latent row inside M-block j, column = token
+    // q_lat^T from TMEM (lane = latent row inside M-block j, column =
+    // token), transposed through shared memory: the MMAs are done with
+    // W_uk[h], so its buffer holds q_lat as [token][512]; then every token's
+    // 1 KB row goes out in 16-byte stores.
     const bool done = mbar_wait(&sm.done, 0, 2 * AT_WAIT);
     tc_fence_after();
     if (!done) {
       if (lane == 0 && warp == 0) set_error(err, MLA_DEVERR_TIMEOUT);
     } else {
+      OT* stg = reinterpret_cast<OT*>(sm.w[0]);  // [n_tok_box][512]
       const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
-      for (int j = 0; j < 4; ++j) {
-        const int dc = 128 * j + 32 * warp + lane;
-        for (int c0 = 0; c0 < n_tok_box; c0 += 16) {
-          float v[16];
-          tmem_ld16(tmem + lane_base + 128 * j + c0, v);
-          tmem_wait_ld();
+      // 16 tokens of all four blocks per TMEM round trip
+      for (int c0 = 0; c0 < n_tok_box; c0 += 16) {
+        float v[4][16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int tt = c0 + i;
-            if (tt < ntok)
-              qabs[(static_cast<size_t>(t0 + tt) * s.n_h + h) * R + dc] =
-                  from_f32<OT>(v[i] * out_scale);
-          }
+        for (int j = 0; j < 4; ++j) tmem_ld16(tmem + lane_base + 128 * j + c0, v[j]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int dc = 128 * j + 32 * warp + lane;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) stg[(c0 + i) * 512 + dc] = from_f32<OT>(v[j][i] * out_scale);
         }
+      }
+    }
+    named_bar_sync(1, 128);  // the four warps' rows are in place
+    if (done) {
+      const OT* stg = reinterpret_cast<const OT*>(sm.w[0]);
+      for (int i = threadIdx.x; i < ntok * 64; i += 128) {
+        const int tt = i / 64, u = i % 64;  // 16-byte unit u of token tt's 512 values
+        *reinterpret_cast<uint4*>(qabs + (static_cast<size_t>(t0 + tt) * s.n_h + h) * R + 8 * u) =
+            *reinterpret_cast<const uint4*>(stg + tt * 512 + 8 * u);
       }
     }
   }
@@ -233,7 +265,7 @@ cudaError_t absorb_q_tc_t(const Shape& s, const Weights* w, const void* q,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, absorb_q_tc_kernel<OT>,
-      tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->inv_freq, seq_lens, B, n_q, max_blocks,
+      tw, tq, s, static_cast<const __nv_bfloat16*>(q), w->rope_turns, seq_lens, B, n_q, max_blocks,
       p.TS, p.G, p.C, p.K, n_tok_box, out_scale, static_cast<OT*>(ws.qabs), ws.tiles,
       ws.prefix, ws.bounds, ws.first_b, err);
 }

@@ -211,6 +211,17 @@ using namespace mla;
 
 namespace {
 
+// RoPE frequencies theta_i = base^(-2i/d_r), stored for the device as
+// theta_i / (2 pi) in units of 2^-64 turns (round to nearest). Extended
+// precision on the host keeps the stored fraction within half a unit.
+void rope_turn_table(float base, int d_r, uint64_t* out) {
+  const long double two_pi = 8.0L * std::atan(1.0L);
+  for (int i = 0; i < d_r / 2; ++i) {
+    const long double theta = std::pow(static_cast<long double>(base), -2.0L * i / d_r);
+    out[i] = static_cast<uint64_t>(std::ldexp(theta / two_pi, 64) + 0.5L);
+  }
+}
+
 bool same_shape(const mla_config* a, const mla_config* b) {
   return a->n_h == b->n_h && a->d_model == b->d_model && a->d_c == b->d_c && a->d_r == b->d_r &&
          a->d_nope == b->d_nope && a->d_v == b->d_v && a->dtype == b->dtype;
@@ -318,25 +329,26 @@ mla_status mla_absorb_weights(const mla_config* cfg, const void* W_dkv, const vo
     cudaFree(h->w.w_dkvr);
     cudaFree(h->w.w_uk);
     cudaFree(h->w.w_uv);
-    cudaFree(h->w.inv_freq);
+    cudaFree(h->w.rope_turns);
     delete h;
   };
   if (cudaMalloc(&h->w.w_dkvr, n_dkvr) != cudaSuccess ||
       cudaMalloc(&h->w.w_uk, n_uk) != cudaSuccess || cudaMalloc(&h->w.w_uv, n_uv) != cudaSuccess ||
-      cudaMalloc(&h->w.inv_freq, sizeof(double) * half) != cudaSuccess) {
+      cudaMalloc(&h->w.rope_turns, sizeof(uint64_t) * half) != cudaSuccess) {
     cudaGetLastError();
     release();
     return MLA_ERR_CUDA;
   }
-  // RoPE inverse frequencies base^(-2i/d_r), in fp64 on the host.
-  double inv[512];
-  for (int i = 0; i < half; ++i)
-    inv[i] = std::pow(static_cast<double>(cfg->rope_base), -2.0 * i / s.d_r);
-  cudaError_t e = cudaMemcpyAsync(h->w.inv_freq, inv, sizeof(double) * half,
+  uint64_t turns[512];
+  rope_turn_table(cfg->rope_base, s.d_r, turns);
+  cudaError_t e = cudaMemcpyAsync(h->w.rope_turns, turns, sizeof(uint64_t) * half,
                                   cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e == cudaSuccess)
     e = launch_pack_weights(s, cfg->dtype, W_dkv, W_kr, W_uk, W_uv, &h->w, stream);
+  // The decode kernels load the packed weights before they wait for their
+  // predecessor on the stream, so the packing has to be complete here.
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     cudaStreamSynchronize(stream);
@@ -356,7 +368,7 @@ mla_status mla_weights_free(mla_weights w) {
   cudaFree(w->w.w_dkvr);
   cudaFree(w->w.w_uk);
   cudaFree(w->w.w_uv);
-  cudaFree(w->w.inv_freq);
+  cudaFree(w->w.rope_turns);
   if (prev >= 0) cudaSetDevice(prev);
   delete w;
   return MLA_OK;
@@ -473,7 +485,8 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
   const WsView v = ws_view(workspace, p.lay);
-  if (p.impl == MLA_IMPL_TENSOR_CORE && combine_tc_supported(p.s, cfg->dtype))
+  // (the tensor-core combine writes out in 16-byte vectors)
+  if (p.impl == MLA_IMPL_TENSOR_CORE && combine_tc_supported(p.s, cfg->dtype) && aligned16(out))
     return from_cuda(launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream));
   return from_cuda(launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out,
                                   stream));
@@ -598,7 +611,10 @@ mla_status mla_decode_fp8(const mla_config* cfg, mla_weights w, const void* q, c
   if (e == cudaSuccess)
     e = launch_attend_tc_fp8(p.s, cache, row_scale, num_blocks, page_table, max_blocks, B, n_q,
                              p.part, v, seq_lens, di->err, stream);
-  if (e == cudaSuccess) e = launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream);
+  if (e == cudaSuccess)
+    e = aligned16(out)
+            ? launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream)
+            : launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out, stream);
   return from_cuda(e);
 }
 
@@ -626,19 +642,18 @@ mla_status mla_fold_full(const mla_config* cfg, const void* W_q, const void* W_u
   auto release = [h]() {
     cudaFree(h->w.w_qf);
     cudaFree(h->w.w_vo);
-    cudaFree(h->w.inv_freq);
+    cudaFree(h->w.rope_turns);
     delete h;
   };
   if (cudaMalloc(&h->w.w_qf, n_qf) != cudaSuccess || cudaMalloc(&h->w.w_vo, n_vo) != cudaSuccess ||
-      cudaMalloc(&h->w.inv_freq, sizeof(double) * half) != cudaSuccess) {
+      cudaMalloc(&h->w.rope_turns, sizeof(uint64_t) * half) != cudaSuccess) {
     cudaGetLastError();
     release();
     return MLA_ERR_CUDA;
   }
-  double inv[512];
-  for (int i = 0; i < half; ++i)
-    inv[i] = std::pow(static_cast<double>(cfg->rope_base), -2.0 * i / s.d_r);
-  cudaError_t e = cudaMemcpyAsync(h->w.inv_freq, inv, sizeof(double) * half,
+  uint64_t turns[512];
+  rope_turn_table(cfg->rope_base, s.d_r, turns);
+  cudaError_t e = cudaMemcpyAsync(h->w.rope_turns, turns, sizeof(uint64_t) * half,
                                   cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e == cudaSuccess)
@@ -661,7 +676,7 @@ mla_status mla_full_weights_free(mla_full_weights w) {
   cudaDeviceSynchronize();
   cudaFree(w->w.w_qf);
   cudaFree(w->w.w_vo);
-  cudaFree(w->w.inv_freq);
+  cudaFree(w->w.rope_turns);
   if (prev >= 0) cudaSetDevice(prev);
   delete w;
   return MLA_OK;
@@ -705,7 +720,7 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   const float out_scale =
       p.impl == MLA_IMPL_TENSOR_CORE ? p.s.scale * 1.4426950408889634f : 1.f;
   if (e == cudaSuccess)
-    e = launch_q_finish(p.s, cfg->dtype, fw->w.inv_freq, proj, seq_lens, max_blocks, B, n_q,
+    e = launch_q_finish(p.s, cfg->dtype, fw->w.rope_turns, proj, seq_lens, max_blocks, B, n_q,
                         p.part, v, out_scale, p.impl == MLA_IMPL_CUDA_CORE, di->err, stream);
   // 2. split-KV latent attention, the same kernels as mla_decode
   if (e == cudaSuccess) {

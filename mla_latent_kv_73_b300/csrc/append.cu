@@ -32,7 +32,7 @@ namespace mla {
 namespace {
 
 struct AppendArgs {
-  const double* inv_freq;
+  const uint64_t* rope_turns;
   const int32_t* seq_idx;
   const int32_t* pos;
   const int32_t* page_table;
@@ -75,7 +75,7 @@ __device__ __forceinline__ void put_value(const AppendArgs& a, T* cache, long lo
 // Value of packed column pc after RoPE, given the pre-rotation values of the
 // pair it belongs to (v_even: rotary dim i, v_odd: rotary dim i + d_r/2).
 // Returns the cache column it lands in.
-__device__ __forceinline__ int finish_column(const Shape& s, const double* inv_freq, int pc,
+__device__ __forceinline__ int finish_column(const Shape& s, const uint64_t* rope_turns, int pc,
                                              float v_self, float v_even, float v_odd, int pos,
                                              float* out) {
   if (pc < s.d_c) {
@@ -84,7 +84,7 @@ __device__ __forceinline__ int finish_column(const Shape& s, const double* inv_f
   }
   const int j = pc - s.d_c, i = j >> 1, e = j & 1, half = s.d_r / 2;
   float c, sn;
-  rope_cos_sin(pos, inv_freq[i], &c, &sn);
+  rope_cos_sin(pos, rope_turns[i], &c, &sn);
   *out = e == 0 ? v_even * c - v_odd * sn : v_even * sn + v_odd * c;
   return s.d_c + i + e * half;
 }
@@ -155,7 +155,7 @@ append_gemv_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
         if (row >= 0) {
           const int ce = c & ~1;  // even member of the pair inside this CTA
           float out;
-          const int dst = finish_column(s, a.inv_freq, pc, res[c * GEMV_TOK + t],
+          const int dst = finish_column(s, a.rope_turns, pc, res[c * GEMV_TOK + t],
                                         res[ce * GEMV_TOK + t], res[(ce + 1) * GEMV_TOK + t],
                                         a.pos[tok], &out);
           put_value<T>(a, cache, row, R, dst, out);
@@ -265,7 +265,7 @@ append_staged_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
         if (row >= 0) {
           const int ce = c & ~1;  // even member of the rotary pair inside this CTA
           float out;
-          const int dst = finish_column(s, a.inv_freq, pc, res[c * ST_TOK + tt],
+          const int dst = finish_column(s, a.rope_turns, pc, res[c * ST_TOK + tt],
                                         res[ce * ST_TOK + tt], res[(ce + 1) * ST_TOK + tt],
                                         a.pos[tok], &out);
           put_value<T>(a, cache, row, R, dst, out);
@@ -339,7 +339,7 @@ append_gemm_kernel(Shape s, const T* __restrict__ x, const T* __restrict__ Wp,
       const int je = j & ~1;
       float out;
       const int dst =
-          finish_column(s, a.inv_freq, pc, acc[i][j], acc[i][je], acc[i][je + 1], a.pos[tok], &out);
+          finish_column(s, a.rope_turns, pc, acc[i][j], acc[i][je], acc[i][je + 1], a.pos[tok], &out);
       put_value<T>(a, cache, row, R, dst, out);
     }
   }
@@ -377,7 +377,10 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
   uint8_t* A = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
   uint8_t* X = A + nkb * AT_WBOX;                             // nkb boxes of N rows x 128 B
-  float* red = reinterpret_cast<float*>(X + nkb * N * 128);   // [128 rows][N] fp32 partial
+  // [128 rows][N + 1] fp32 partial: the padded row keeps the 32 rows a warp
+  // writes per column in 32 different banks
+  float* red = reinterpret_cast<float*>(X + nkb * N * 128);
+  const int NP = N + 1;
   __shared__ uint64_t full, done;
   __shared__ uint32_t tmem_base;
   const uint32_t kc = cluster_ctarank();
@@ -398,22 +401,20 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   // With programmatic dependent launch this CTA may start while the previous
-  // kernel still runs: pull the weight slice into L2 (coherent, so safe at
-  // any time), then wait for that kernel before loading anything into the SM
-  // or touching the hidden states and the cache.
+  // kernel still runs. The packed weights are complete and never written
+  // once their handle exists, so the weight slice is loaded at once; the
+  // hidden states and the cache are touched only after the wait for that
+  // kernel.
   const int k0 = static_cast<int>(kc) * nkb * 64;
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_x);
-    for (int j = 0; j < nkb; ++j) tma_prefetch_2d(&tmap_w, k0 + 64 * j, mb * 128);
+    mbar_arrive_expect_tx(&full, nkb * (AT_WBOX + N * 128));
+    for (int j = 0; j < nkb; ++j) tma_load_2d(A + j * AT_WBOX, &tmap_w, k0 + 64 * j, mb * 128, &full);
   }
   griddep_wait();
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&full, nkb * (AT_WBOX + N * 128));
-    for (int j = 0; j < nkb; ++j) {
-      tma_load_2d(A + j * AT_WBOX, &tmap_w, k0 + 64 * j, mb * 128, &full);
-      tma_load_2d(X + j * N * 128, &tmap_x, k0 + 64 * j, 0, &full);
-    }
+    for (int j = 0; j < nkb; ++j) tma_load_2d(X + j * N * 128, &tmap_x, k0 + 64 * j, 0, &full);
     if (mbar_wait(&full, 0, AT_WAIT)) {
       tc_fence_after();
       const uint32_t idesc = idesc_bf16_f32(128, N, false, false);
@@ -441,7 +442,7 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
       tmem_ld16(tmem + lane_base + c0, v);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 16; ++i) red[row * N + c0 + i] = ok ? v[i] : 0.f;
+      for (int i = 0; i < 16; ++i) red[row * NP + c0 + i] = ok ? v[i] : 0.f;
     }
   }
   if (!ok && threadIdx.x == 0) set_error(a.err, MLA_DEVERR_TIMEOUT);
@@ -459,8 +460,8 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     for (int src = 0; src < 16; ++src) {
       if (src < kcn) {
         const float* r = map_to_rank(red, static_cast<uint32_t>(src));
-        p0[src] = r[r0 * N + t];
-        p1[src] = r[(r0 + 1) * N + t];
+        p0[src] = r[r0 * NP + t];
+        p1[src] = r[(r0 + 1) * NP + t];
       } else {
         p0[src] = p1[src] = 0.f;
       }
@@ -474,10 +475,10 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     const long long row = append_row(a, s, t);
     if (row < 0) continue;
     float out;
-    int dst = finish_column(s, a.inv_freq, pc0, v0, v0, v1, a.pos[t], &out);
+    int dst = finish_column(s, a.rope_turns, pc0, v0, v0, v1, a.pos[t], &out);
     put_value<__nv_bfloat16>(a, cache, row, R, dst, out);
     if (pc0 + 1 < R) {
-      dst = finish_column(s, a.inv_freq, pc0 + 1, v1, v0, v1, a.pos[t], &out);
+      dst = finish_column(s, a.rope_turns, pc0 + 1, v1, v0, v1, a.pos[t], &out);
       put_value<__nv_bfloat16>(a, cache, row, R, dst, out);
     }
   }
@@ -490,7 +491,7 @@ append_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
 
 // Dynamic shared memory of append_tc_kernel for N tokens and nkb boxes.
 size_t append_tc_smem(int nkb, int N) {
-  return 1024 + static_cast<size_t>(nkb) * (AT_WBOX + N * 128) + static_cast<size_t>(128) * N * 4;
+  return 1024 + static_cast<size_t>(nkb) * (AT_WBOX + N * 128) + static_cast<size_t>(128) * (N + 1) * 4;
 }
 
 // Whether clusters of kcn CTAs of append_tc_kernel, each with `smem` bytes,
@@ -667,7 +668,7 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
                           const int32_t* seq_idx, const int32_t* pos, const int32_t* page_table,
                           int B, int max_blocks, void* cache, int num_blocks, int T,
                           uint32_t* err, cudaStream_t st) {
-  AppendArgs a{w->inv_freq, seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err,
+  AppendArgs a{w->rope_turns, seq_idx, pos, page_table, B, max_blocks, num_blocks, T, err,
                nullptr};
   if (dt == MLA_F32) return append_t<float>(s, w, x, a, cache, st);
   return append_t<__nv_bfloat16>(s, w, x, a, cache, st);
@@ -676,7 +677,7 @@ cudaError_t launch_append(const Shape& s, mla_dtype dt, const Weights* w, const 
 cudaError_t launch_append_rows_f32(const Shape& s, mla_dtype dt, const Weights* w, const void* x,
                                    const int32_t* seq_idx, const int32_t* pos, int T,
                                    float* rows, uint32_t* err, cudaStream_t st) {
-  AppendArgs a{w->inv_freq, seq_idx, pos, nullptr, 1, 1, 1, T, err, rows};
+  AppendArgs a{w->rope_turns, seq_idx, pos, nullptr, 1, 1, 1, T, err, rows};
   if (dt == MLA_F32) return append_t<float>(s, w, x, a, nullptr, st);
   return append_t<__nv_bfloat16>(s, w, x, a, nullptr, st);
 }

@@ -86,20 +86,18 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   // With programmatic dependent launch this CTA may start while the attention
-  // kernel still runs: pull W_uv[h] into L2 (coherent, so safe at any time),
-  // then wait for the attention kernel before loading anything into the SM.
+  // kernel still runs. The packed W_uv is complete and never written once its
+  // handle exists, so its loads start at once; everything the attention
+  // kernel writes is read only after the wait.
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmap_w);
-    for (int kc = 0; kc < 8; ++kc) tma_prefetch_2d(&tmap_w, 64 * kc, h * 128);
+    mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
+    for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
   }
   griddep_wait();
   // the next kernel (its weights are constant) may start its prologue now;
   // it waits for this one to finish before it reads anything this one writes
   griddep_launch_dependents();
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
-    for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
-  }
 
   // 1. per token: the CTAs holding its pieces and their merge weights
   //    exp(lse_s - lse). The plan loads of all tokens go out together (the
@@ -258,8 +256,13 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
     mma_commit(&sm.done);
   }
   if (warp < 4) {
+    // out^T from TMEM (lane = output dim, column = token), transposed
+    // through the o_lat staging (the MMAs are done with it) as
+    // [token][128] fp32, then each token's 512-byte row goes out in 16-byte
+    // stores.
     const bool done = mbar_wait(&sm.done, 0, 2 * CT_WAIT);
     tc_fence_after();
+    float* stg = reinterpret_cast<float*>(sm.o[0][0]);  // [n_box][128]
     if (done) {
       const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
       const int dv = 32 * warp + lane;
@@ -271,15 +274,18 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
         tmem_ld16(tmem + lane_base + 96 + c0, v3);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = (v[i] + v1[i]) + (v2[i] + v3[i]);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int tt = c0 + i;
-          if (tt < ntok) out[(static_cast<size_t>(t0 + tt) * n_h + h) * 128 + dv] = v[i];
-        }
+        for (int i = 0; i < 16; ++i) stg[(c0 + i) * 128 + dv] = (v[i] + v1[i]) + (v2[i] + v3[i]);
       }
     } else if (warp == 0 && lane == 0) {
       set_error(err, MLA_DEVERR_TIMEOUT);
+    }
+    named_bar_sync(1, 128);  // the four warps' columns are in place
+    if (done) {
+      for (int i = threadIdx.x; i < ntok * 32; i += 128) {
+        const int tt = i / 32, u = i % 32;  // 16-byte unit u of token tt's 128 outputs
+        *reinterpret_cast<float4*>(out + (static_cast<size_t>(t0 + tt) * n_h + h) * 128 + 4 * u) =
+            *reinterpret_cast<const float4*>(stg + tt * 128 + 4 * u);
+      }
     }
   }
   tc_fence_before();

@@ -31,19 +31,21 @@ __device__ __forceinline__ __half from_f32<__half>(float v) {
   return __float2half_rn(v);
 }
 
-// cos/sin of pos * inv_freq, where inv_freq = base^(-2i/d_r) comes from a
-// table built on the host in fp64. The angle is formed in fp64 and reduced
-// to [-pi, pi] with one fused multiply-add against 2*pi (Cody-Waite style,
-// one constant). The reduced angle is good to about 1e-11 rad at positions
-// up to 2^17, and to about 1e-6 rad at 2^31. CUDA's fp32 sincosf then
-// evaluates it. Each angle costs 4 fp64 operations, which matters because
-// B300's fp64 rate is low.
-__device__ __forceinline__ void rope_cos_sin(int pos, double inv_freq, float* c, float* s) {
-  const double two_pi = 6.283185307179586;
-  const double a = static_cast<double>(pos) * inv_freq;
-  const double k = rint(a * 0.15915494309189535);
-  const float r = static_cast<float>(fma(-k, two_pi, a));
-  sincosf(r, s, c);
+// cos/sin of the RoPE angle pos * theta_i, theta_i = base^(-2i/d_r).
+// rope_turns holds theta_i / (2 pi) as a 64-bit binary fraction of a turn
+// (built on the host in extended precision). The integer product
+// pos * rope_turns, taken modulo 2^64, is then exactly the fractional part of
+// the angle in turns, with no range reduction and no fp64 arithmetic (B300's
+// fp64 rate is low). Its top 32 bits, read as a signed number, are the angle
+// in [-1/2, 1/2) turns; sincospif evaluates sin/cos of pi times twice that.
+// The representation error of theta_i / (2 pi) is at most 2^-65 turns, so
+// the angle is good to about 2^-48 turns at positions up to 2^17; the fp32
+// argument of sincospif adds at most 2^-25 (relative to pi), as a directly
+// reduced fp32 angle would.
+__device__ __forceinline__ void rope_cos_sin(int pos, uint64_t rope_turns, float* c, float* s) {
+  const uint64_t f = static_cast<uint64_t>(static_cast<uint32_t>(pos)) * rope_turns;
+  const int32_t hi = static_cast<int32_t>(static_cast<uint32_t>(f >> 32));
+  sincospif(static_cast<float>(hi) * 0x1p-31f, s, c);
 }
 
 // 16-byte vector loads of T, widened to fp32.

@@ -322,7 +322,7 @@ constexpr int QF_HEADS = 2;
 
 template <typename T>
 __global__ void __launch_bounds__(QF_THREADS)
-q_finish_kernel(Shape s, const float* __restrict__ qpre, const double* __restrict__ inv_freq,
+q_finish_kernel(Shape s, const float* __restrict__ qpre, const uint64_t* __restrict__ rope_turns,
                 const int32_t* __restrict__ seq_lens, int B, int n_q, int max_blocks, int TS,
                 int G, int C, int K, float out_scale, T* __restrict__ qabs, int32_t* tiles,
                 int32_t* prefix, long long* bounds, int32_t* first_b, uint32_t* err) {
@@ -347,7 +347,7 @@ q_finish_kernel(Shape s, const float* __restrict__ qpre, const double* __restric
       const int k = n - s.d_c;
       const float x1 = sh[s.d_c + k], x2 = sh[s.d_c + k + half];
       float c, sn;
-      rope_cos_sin(pos, inv_freq[k], &c, &sn);
+      rope_cos_sin(pos, rope_turns[k], &c, &sn);
       dh[s.d_c + k] = from_f32<T>((x1 * c - x2 * sn) * out_scale);
       dh[s.d_c + k + half] = from_f32<T>((x1 * sn + x2 * c) * out_scale);
     }
@@ -424,14 +424,14 @@ cudaError_t fold_t(const Shape& s, const void* W_q, const void* W_uk, const void
 }
 
 template <typename T>
-cudaError_t q_finish_t(const Shape& s, const double* inv_freq, const float* qpre,
+cudaError_t q_finish_t(const Shape& s, const uint64_t* rope_turns, const float* qpre,
                        const int32_t* seq_lens, int max_blocks, int B, int n_q, const Partition& p,
                        const WsView& ws, float out_scale, uint32_t* err, cudaStream_t st) {
   const long long blocks =
       static_cast<long long>(B) * n_q * ((s.n_h + QF_HEADS - 1) / QF_HEADS);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   q_finish_kernel<T><<<static_cast<unsigned>(blocks), QF_THREADS, 0, st>>>(
-      s, qpre, inv_freq, seq_lens, B, n_q, max_blocks, p.TS, p.G, p.C, p.K, out_scale,
+      s, qpre, rope_turns, seq_lens, B, n_q, max_blocks, p.TS, p.G, p.C, p.K, out_scale,
       static_cast<T*>(ws.qabs), ws.tiles, ws.prefix, ws.bounds, ws.first_b, err);
   return cudaGetLastError();
 }
@@ -541,14 +541,14 @@ cudaError_t launch_fold_full(const Shape& s, mla_dtype dt, const void* W_q, cons
   return fold_t<__nv_bfloat16>(s, W_q, W_uk, W_uv, W_o, w, sms, st);
 }
 
-cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
+cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const uint64_t* rope_turns,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,
                             bool q_f32, uint32_t* err, cudaStream_t st) {
   if (dt == MLA_F32 || q_f32)
-    return q_finish_t<float>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws, out_scale,
+    return q_finish_t<float>(s, rope_turns, qpre, seq_lens, max_blocks, B, n_q, p, ws, out_scale,
                              err, st);
-  return q_finish_t<__nv_bfloat16>(s, inv_freq, qpre, seq_lens, max_blocks, B, n_q, p, ws,
+  return q_finish_t<__nv_bfloat16>(s, rope_turns, qpre, seq_lens, max_blocks, B, n_q, p, ws,
                                    out_scale, err, st);
 }
 

@@ -66,7 +66,7 @@ struct Weights {
                   // dims i and i + d_r/2 sit in adjacent packed columns.
   void* w_uk;     // [n_h][d_c][d_nope]
   void* w_uv;     // [n_h][d_v][d_c]: per head, one contiguous d_c row per output
-  double* inv_freq;  // [d_r/2] rope_base^(-2i/d_r), computed on the host in fp64
+  uint64_t* rope_turns;  // [d_r/2] rope_base^(-2i/d_r) / (2 pi) as a 64-bit fraction of a turn
 };
 
 // Library-owned weights of the full-fold variant (x_q in, y out).
@@ -76,7 +76,7 @@ struct FullWeights {
   int device;
   float* w_qf;       // [d_model][n_h*R]: per head [W_abs[h] | W_qr[h]] (fp32)
   float* w_vo;       // [n_h*d_c][d_model]: row h*d_c + c of W_uv[h] W_o[h] (fp32)
-  double* inv_freq;  // [d_r/2] rope_base^(-2i/d_r), computed on the host in fp64
+  uint64_t* rope_turns;  // [d_r/2] rope_base^(-2i/d_r) / (2 pi) as a 64-bit fraction of a turn
 };
 
 // Split of K across CTAs for one x W product: S splits of k_split each.
@@ -171,7 +171,7 @@ size_t xw_part_floats(int M, int N, const XwPlan& p);
 cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, mla_dtype w_dt,
                       const void* W, int N, float* out, float* part, const XwPlan& p,
                       uint32_t* err, bool pdl, cudaStream_t st);
-cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const double* inv_freq,
+cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const uint64_t* rope_turns,
                             const float* qpre, const int32_t* seq_lens, int max_blocks, int B,
                             int n_q, const Partition& p, const WsView& ws, float out_scale,
                             bool q_f32, uint32_t* err, cudaStream_t st);

@@ -329,6 +329,24 @@ def test_kernels_agree_and_steps_equal_fused():
     b.dw.free()
 
 
+def test_output_off_its_16_byte_alignment():
+    """out at a 4-byte offset: the tensor-core combine writes 16-byte
+    vectors, so the library takes the CUDA-core combine for it; the result
+    matches the aligned call's within the bf16 bound."""
+    w, lens = small_workload(lens=(5, 128, 129, 300), n_q=2, seed=4)
+    r = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
+    ref = r.decode()
+    n = w.batch * w.n_q * w.n_h * w.d_v
+    buf = torch.full((n + 1,), float("nan"), device="cuda")
+    out = buf[1:].view(w.batch, w.n_q, w.n_h, w.d_v)
+    assert out.data_ptr() % 16 == 4
+    _lib.mla_decode(r.cfg, r.dw.handle, r.q, r.cache, r.pt, r.sl, out, r.ws)
+    torch.cuda.synchronize()
+    check_bf16(out.cpu().numpy(), ref, "misaligned out")
+    check_bf16(out.cpu().numpy(), r.oracle(), "misaligned out vs oracle")
+    r.dw.free()
+
+
 def test_bad_lengths_and_pages_are_flagged():
     w, lens = small_workload(lens=(0, 70, 100))  # seq 0 shorter than n_q
     r = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
