@@ -3,6 +3,7 @@
 // them allocates device memory except mla_absorb_weights.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -487,7 +488,7 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
   const WsView v = ws_view(workspace, p.lay);
   // (the tensor-core combine writes out in 16-byte vectors)
   if (p.impl == MLA_IMPL_TENSOR_CORE && combine_tc_supported(p.s, cfg->dtype) && aligned16(out))
-    return from_cuda(launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream));
+    return from_cuda(launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, nullptr, di->err, stream));
   return from_cuda(launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out,
                                   stream));
 }
@@ -613,7 +614,7 @@ mla_status mla_decode_fp8(const mla_config* cfg, mla_weights w, const void* q, c
                              p.part, v, seq_lens, di->err, stream);
   if (e == cudaSuccess)
     e = aligned16(out)
-            ? launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, di->err, stream)
+            ? launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, nullptr, di->err, stream)
             : launch_combine(p.s, cfg->dtype, &w->w, seq_lens, B, n_q, p.part, v, out, stream);
   return from_cuda(e);
 }
@@ -740,6 +741,33 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
   return from_cuda(e);
 }
 
+namespace {
+
+// Workspace of mla_decode_layer past the decode's own: the bf16 hi/lo copy
+// of out that the tensor-core projection reads (decode-sized batches only),
+// then the projection's split partials, sized for either projection kernel.
+struct LayerExtra {
+  size_t hilo_bytes, part_bytes;
+  XwPlan po, pp;  // K splits of the CUDA-core and the tensor-core projection
+};
+LayerExtra layer_extra(const mla_config* cfg, int M, const DeviceInfo* di) {
+  const int K = cfg->n_h * cfg->d_v, N = cfg->d_model;
+  LayerExtra x;
+  x.po = xw_plan(M, K, N, di->sms);
+  size_t floats = xw_part_floats(M, N, x.po);
+  x.hilo_bytes = 0;
+  x.pp = x.po;
+  if (M <= PROJ_TC_MAX_TOKENS) {
+    x.hilo_bytes = align256(sizeof(uint16_t) * 2 * static_cast<size_t>(M) * K);
+    x.pp = proj_tc_plan(M, K, N, di->sms);
+    if (x.pp.S > 1) floats = std::max(floats, static_cast<size_t>(x.pp.S) * M * N);
+  }
+  x.part_bytes = align256(sizeof(float) * floats);
+  return x;
+}
+
+}  // namespace
+
 mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
                                            size_t* bytes) {
   if (!bytes) return MLA_ERR_INVALID_ARG;
@@ -749,8 +777,8 @@ mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int
   if (st != MLA_OK) return st;
   const DeviceInfo* di = device_info();
   if (!di) return MLA_ERR_CUDA;
-  const XwPlan po = xw_plan(B * n_q, cfg->n_h * cfg->d_v, cfg->d_model, di->sms);
-  *bytes = base + align256(sizeof(float) * xw_part_floats(B * n_q, cfg->d_model, po));
+  const LayerExtra x = layer_extra(cfg, B * n_q, di);
+  *bytes = base + x.hilo_bytes + x.part_bytes;
   return MLA_OK;
 }
 
@@ -770,21 +798,41 @@ mla_status mla_decode_layer(const mla_config* cfg, mla_weights w, const void* W_
   if (st != MLA_OK) return st;
   if (!same_shape(cfg, &w->cfg)) return MLA_ERR_SHAPE;
   if (current_device() != w->w.device) return MLA_ERR_INVALID_ARG;
-  const int M = B * n_q;
-  const XwPlan po = xw_plan(M, p.s.n_h * p.s.d_v, p.s.d_model, di->sms);
-  const size_t part_bytes = align256(sizeof(float) * xw_part_floats(M, p.s.d_model, po));
-  if (ws_bytes < p.lay.total + part_bytes) return MLA_ERR_WORKSPACE;
+  const int M = B * n_q, K = p.s.n_h * p.s.d_v, N = p.s.d_model;
+  const LayerExtra xl = layer_extra(cfg, M, di);
+  if (ws_bytes < p.lay.total + xl.hilo_bytes + xl.part_bytes) return MLA_ERR_WORKSPACE;
+  char* extra = static_cast<char*>(workspace) + p.lay.total;
+  uint16_t* hilo = reinterpret_cast<uint16_t*>(extra);
+  float* part = reinterpret_cast<float*>(extra + xl.hilo_bytes);
   // The new tokens go into the cache first, then the decode reads them.
   st = mla_append_kv(cfg, w, x, seq_idx, pos, page_table, B, max_blocks, cache, num_blocks, M,
                      stream);
   if (st != MLA_OK) return st;
-  st = mla_decode(cfg, w, q, cache, num_blocks, page_table, max_blocks, seq_lens, B, n_q, out,
-                  workspace, ws_bytes, stream);
+  // The tensor-core projection takes out from the tensor-core combine as a
+  // bf16 hi/lo pair; every other case projects out (fp32) on the CUDA cores.
+  const bool tc = p.impl == MLA_IMPL_TENSOR_CORE && combine_tc_supported(p.s, cfg->dtype) &&
+                  aligned16(out) && xl.hilo_bytes > 0 && proj_tc_applies(M, K, N, W_o);
+  if (!tc) {
+    st = mla_decode(cfg, w, q, cache, num_blocks, page_table, max_blocks, seq_lens, B, n_q, out,
+                    workspace, ws_bytes, stream);
+    if (st != MLA_OK) return st;
+    // y = concat_h(o_h) W_o, launched early: its W_o stream overlaps the combine
+    return from_cuda(launch_xw(MLA_F32, out, M, K, cfg->dtype, W_o, N, y, part, xl.po, di->err,
+                               true, stream));
+  }
+  mla_config c2 = *cfg;
+  c2.impl = p.impl;
+  st = mla_decode_absorb_q(&c2, w, q, seq_lens, max_blocks, B, n_q, workspace, ws_bytes, stream);
   if (st != MLA_OK) return st;
-  // y = concat_h(o_h) W_o, launched early: its W_o stream overlaps the combine
-  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + p.lay.total);
-  return from_cuda(launch_xw(MLA_F32, out, M, p.s.n_h * p.s.d_v, cfg->dtype, W_o, p.s.d_model, y,
-                             part, po, di->err, true, stream));
+  st = mla_decode_attend(&c2, cache, num_blocks, page_table, max_blocks, seq_lens, B, n_q,
+                         workspace, ws_bytes, stream);
+  if (st != MLA_OK) return st;
+  const WsView v = ws_view(workspace, p.lay);
+  cudaError_t e = launch_combine_tc(p.s, &w->w, B, n_q, p.part, v, out, hilo, di->err, stream);
+  // y = concat_h(o_h) W_o on the tensor cores, launched early: its W_o
+  // stream overlaps the combine
+  if (e == cudaSuccess) e = launch_proj_tc(hilo, M, K, W_o, N, y, part, xl.pp, di->err, stream);
+  return from_cuda(e);
 }
 
 mla_status mla_get_last_device_error(cudaStream_t stream, uint32_t* code) {

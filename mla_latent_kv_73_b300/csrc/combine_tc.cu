@@ -62,7 +62,8 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
                   const int32_t* __restrict__ tiles, const int32_t* __restrict__ prefix,
                   const long long* __restrict__ bounds, int B, int n_q, Partition p,
                   const float* __restrict__ part_o,
-                  const float* __restrict__ part_lse, float* __restrict__ out, uint32_t* err) {
+                  const float* __restrict__ part_lse, float* __restrict__ out,
+                  uint16_t* __restrict__ hilo, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   CombSmem& sm = *reinterpret_cast<CombSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -281,10 +282,21 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
     }
     named_bar_sync(1, 128);  // the four warps' columns are in place
     if (done) {
+      const size_t plane = static_cast<size_t>(Tq) * n_h * 128;  // elements of hi (and of lo)
       for (int i = threadIdx.x; i < ntok * 32; i += 128) {
         const int tt = i / 32, u = i % 32;  // 16-byte unit u of token tt's 128 outputs
-        *reinterpret_cast<float4*>(out + (static_cast<size_t>(t0 + tt) * n_h + h) * 128 + 4 * u) =
-            *reinterpret_cast<const float4*>(stg + tt * 128 + 4 * u);
+        const size_t e = (static_cast<size_t>(t0 + tt) * n_h + h) * 128 + 4 * u;
+        const float4 v = *reinterpret_cast<const float4*>(stg + tt * 128 + 4 * u);
+        *reinterpret_cast<float4*>(out + e) = v;
+        if (hilo) {
+          const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y);
+          const __nv_bfloat162 h1 = __floats2bfloat162_rn(v.z, v.w);
+          *reinterpret_cast<uint2*>(hilo + e) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+          *reinterpret_cast<uint2*>(hilo + plane + e) =
+              make_uint2(pack_bf16x2(v.x - __low2float(h0), v.y - __high2float(h0)),
+                         pack_bf16x2(v.z - __low2float(h1), v.w - __high2float(h1)));
+        }
       }
     }
   }
@@ -303,8 +315,8 @@ bool combine_tc_supported(const Shape& s, mla_dtype dt) {
 }
 
 cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
-                              const Partition& p, const WsView& ws, float* out, uint32_t* err,
-                              cudaStream_t st) {
+                              const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
+                              uint32_t* err, cudaStream_t st) {
   const int Tq = B * n_q;
   TmapSpec spec{};
   spec.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -347,7 +359,7 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
                             static_cast<const int32_t*>(ws.prefix),
                             static_cast<const long long*>(ws.bounds), B, n_q, p,
                             static_cast<const float*>(ws.part_o),
-                            static_cast<const float*>(ws.part_lse), out, err);
+                            static_cast<const float*>(ws.part_lse), out, hilo, err);
 }
 
 }  // namespace mla

@@ -527,9 +527,13 @@ cudaError_t launch_xw(mla_dtype a_dt, const void* A, int M, int K, mla_dtype w_d
   else
     e = xw_t<bf16, bf16>(A, M, K, W, N, p.k_split, dst, err, grid, pdl, st);
   if (e != cudaSuccess || p.S == 1) return e;
-  const size_t n = static_cast<size_t>(M) * N;
+  return launch_sum_splits(part, p.S, static_cast<size_t>(M) * N, out, st);
+}
+
+cudaError_t launch_sum_splits(const float* part, int S, size_t n, float* out, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
   const size_t blocks = (n + 255) / 256;
-  sum_splits_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(part, p.S, n,
+  sum_splits_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(part, S, n,
                                                                                        out);
   return cudaGetLastError();
 }

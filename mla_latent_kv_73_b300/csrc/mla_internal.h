@@ -144,10 +144,12 @@ cudaError_t launch_absorb_q_tc(const Shape& s, const Weights* w, const void* q,
                                const int32_t* seq_lens, int max_blocks, int B, int n_q,
                                const Partition& p, const WsView& ws, float out_scale,
                                bool q_half, uint32_t* err, cudaStream_t st);
+// hilo (optional, else null): out also as bf16 hi [B*n_q][n_h*d_v] followed
+// by bf16 lo = bf16(out - hi), the operand of launch_proj_tc.
 bool combine_tc_supported(const Shape& s, mla_dtype dt);
 cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
-                              const Partition& p, const WsView& ws, float* out, uint32_t* err,
-                              cudaStream_t st);
+                              const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
+                              uint32_t* err, cudaStream_t st);
 
 cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
@@ -177,6 +179,19 @@ cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const uint64_t* rope_t
                             bool q_f32, uint32_t* err, cudaStream_t st);
 cudaError_t launch_combine_latent(const Shape& s, int B, int n_q, const Partition& p,
                                   const WsView& ws, float* olat, cudaStream_t st);
+// out[i] = sum_z part[z][i] over the S splits, in increasing z.
+cudaError_t launch_sum_splits(const float* part, int S, size_t n, float* out, cudaStream_t st);
+
+// Tensor-core output projection y[M x N] = A W for up to PROJ_TC_MAX_TOKENS
+// rows of A, given as bf16 hi [M][K] followed by bf16 lo [M][K] (A = hi +
+// lo), and W [K][N] bf16 row-major. proj_tc_applies: the sizes and W's
+// alignment suit the kernel. proj_tc_plan: the K split (part needs S*M*N
+// floats when S > 1).
+constexpr int PROJ_TC_MAX_TOKENS = 64;
+bool proj_tc_applies(int M, int K, int N, const void* W);
+XwPlan proj_tc_plan(int M, int K, int N, int sms);
+cudaError_t launch_proj_tc(const uint16_t* hilo, int M, int K, const void* W, int N, float* y,
+                           float* part, const XwPlan& p, uint32_t* err, cudaStream_t st);
 
 // Partition parameters for each attention kernel.
 // tc_pairs: CTA pairs resident at once for the tensor-core attention kernel.

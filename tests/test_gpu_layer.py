@@ -44,7 +44,7 @@ def check(dtype, got, ref, what=""):
 
 
 def run_layer(n_h, d_model, d_c, d_r, d_nope, d_v, lens, n_q, dtype, seed,
-              impl=_lib.MLA_IMPL_AUTO, w_o_offset=0):
+              impl=_lib.MLA_IMPL_AUTO, w_o_offset=0, out_offset=0):
     w = synth.Workload(f"layer_{n_h}_{d_model}_{n_q}_{seed}", n_h=n_h, d_model=d_model, d_c=d_c,
                        d_r=d_r, d_nope=d_nope, d_v=d_v, batch=len(lens), n_q=n_q, len_lo=0,
                        len_hi=0, dtype=dtype, seed=seed)
@@ -66,7 +66,8 @@ def run_layer(n_h, d_model, d_c, d_r, d_nope, d_v, lens, n_q, dtype, seed,
     seq_idx = np.repeat(np.arange(B), n_q).astype(np.int32)
     pos = np.concatenate([np.arange(L - n_q, L) for L in lens]).astype(np.int32)
     qv, qs = synth.queries(w)
-    out = torch.full((B, n_q, n_h, d_v), float("nan"), device="cuda")
+    out = torch.full((B * n_q * n_h * d_v + out_offset,), float("nan"), device="cuda")
+    out = out[out_offset:].view(B, n_q, n_h, d_v)  # off 16-byte alignment when out_offset % 4
     y = torch.full((B, n_q, d_model), float("nan"), device="cuda")
     ws = torch.empty(_lib.mla_decode_layer_workspace_size(cfg, B, n_q), dtype=torch.uint8,
                      device="cuda")
@@ -123,3 +124,28 @@ def test_layer_dsv2_widths():
     out, y, o_ref, y_ref = run_layer(128, 5120, 512, 64, 128, 128, (70, 257), 1, "bf16", 34)
     check("bf16", out, o_ref, "out")
     check("bf16", y, y_ref, "y")
+
+
+@pytest.mark.parametrize("lens,n_q,d_model", [
+    ((3, 64, 65, 130, 200, 257) * 4, 2, 200),  # 48 tokens; outputs 128..199 fill a tile partly
+    ((5, 90) * 20, 2, 256),                     # 80 tokens: past the tensor-core projection's 64
+])
+def test_layer_token_counts_and_ragged_outputs(lens, n_q, d_model):
+    out, y, o_ref, y_ref = run_layer(16, d_model, 512, 64, 128, 128, lens, n_q, "bf16", 35)
+    check("bf16", out, o_ref, "out")
+    check("bf16", y, y_ref, "y")
+
+
+def test_layer_projection_paths_agree():
+    """out off its 16-byte alignment sends the step through the CUDA-core
+    combine and projection (fp32 out); the aligned call goes through the
+    tensor-core ones (out as a bf16 hi + lo pair). Both match the oracle, and
+    each other to well within the bf16 bound."""
+    args = (16, 512, 512, 64, 128, 128, (9, 64, 300), 2, "bf16", 36)
+    out_a, y_a, o_ref, y_ref = run_layer(*args)
+    out_b, y_b, _, _ = run_layer(*args, out_offset=1)
+    check("bf16", y_a, y_ref, "y tensor-core projection")
+    check("bf16", y_b, y_ref, "y CUDA-core projection")
+    for a, b, what in ((out_a, out_b, "combines"), (y_a, y_b, "projections")):
+        rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+        assert rel <= 1e-4, f"{what} differ: rel-L2 {rel:.3e}"
