@@ -27,6 +27,8 @@
 // the slice's partial (or straight into y when K is not split). The partials
 // are summed in a fixed order by a second kernel, so y does not depend on
 // timing.
+#include <algorithm>
+
 #include "device_common.cuh"
 #include "sm100_ptx.cuh"
 #include "tmap.h"
@@ -178,7 +180,10 @@ size_t proj_smem() {
   return sizeof(PjSmem<NT>) + 1024;
 }
 
-// CTAs of proj_tc_kernel<NT> one SM holds (0 if the kernel cannot be set up).
+// CTAs of proj_tc_kernel<NT> one SM holds (0 if the kernel cannot be set
+// up): its shared memory (with the per-block reservation) against the SM's,
+// its TMEM columns against 512. The kernel asks for the largest shared-memory
+// carveout, so the launch gets the SM's whole shared memory.
 template <int NT>
 int proj_resident() {
   static int cached[64] = {};
@@ -186,14 +191,21 @@ int proj_resident() {
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   const int smem = static_cast<int>(proj_smem<NT>());
-  int n = 0;
+  int smem_sm = 0, reserved = 0;
   if (cudaFuncSetAttribute(proj_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<NT>, PJ_THREADS, smem) !=
+      cudaFuncSetAttribute(proj_tc_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
           cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
+  constexpr int tcols = NT <= 32 ? 32 : 64;
+  int n = smem_sm / (smem + reserved);
+  n = std::min(n, std::min(512 / tcols, 2048 / PJ_THREADS));
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
