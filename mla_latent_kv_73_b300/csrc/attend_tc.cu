@@ -38,9 +38,9 @@
 // TMEM (512 columns): two 64-column score slots (tile parity), a 32-column
 // buffer for P (bf16 pairs, read by the value MMA straight from TMEM as its
 // A operand), 96 columns of Q (192 of this CTA's latent columns) and the
-// 256-column latent accumulator. After the sender warps have read a score
-// slot they write the fp16-rounded partial back into it (as fp32), where
-// the softmax warps pick up their own half of the sum.
+// 256-column latent accumulator. The sender warps and the softmax warps
+// both read a score slot; each rounds the CTA's partial to fp16 the same
+// way, the senders for the peer and the softmax for its own half of the sum.
 //
 // The partials travel by the bulk-copy engine (cp.async.bulk from a local
 // staging buffer into the peer's exchange buffer), not by st.async from
@@ -57,13 +57,13 @@
 //               tiles, each into its own score slot
 //   warps 4..7  senders: warp w reads the score slot's lane quarter w % 4
 //               (one query row per lane, all 64 tokens), rounds the partial
-//               to fp16, writes the rounded values back to TMEM and the fp16
-//               words into the staging buffer, from which one thread copies
-//               them to the peer. They also put the TMEM part of Q in place
-//               at each piece.
+//               to fp16 and writes the fp16 words into the staging buffer,
+//               from which one thread copies them to the peer. They also put
+//               the TMEM part of Q in place at each piece.
 //   warps 8..15 softmax: warp w reads lane quarter w % 4 and tokens
-//               [32h, 32h + 32), h = (w - 8) / 4, and adds the peer's fp16
-//               partial to its own with one mixed-precision add per score.
+//               [32h, 32h + 32), h = (w - 8) / 4, rounds its own partial to
+//               fp16 and adds the peer's with one mixed-precision add per
+//               score.
 //               The two warps of a lane quarter meet at a 64-thread named
 //               barrier to agree on the row maximum. One set of warps handles
 //               every tile, so the running max and row sums live in
@@ -170,7 +170,7 @@ struct __align__(1024) PairSmemT {
   uint64_t kv_full[NS], kv_empty[NS];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_empty[2];   // score slot by tile parity
-  uint64_t own_ready[2];            // fp16 own partial written back to the slot
+  uint64_t own_ready[2];            // the sender warps are done reading the slot
   uint64_t x_full[2], x_sendok[2];  // peer's partial arrived / peer's buffer free
   uint64_t p_full[2], pv_done[2];
   uint64_t o_full, o_empty;
@@ -314,9 +314,9 @@ __device__ __forceinline__ uint32_t xoff(int row, int u) {
 // Sender side of tile kv, for query row `row` (one per lane of the warp's
 // lane quarter): reads this CTA's partial scores of all 64 tokens from the
 // score slot (the queries carry scale * log2(e), so they are in log2
-// units), rounds them to fp16, writes the rounded values back into the slot
-// (as fp32) for this CTA's softmax and the fp16 words into the staging
-// buffer. The leader thread then copies the staged tile into the peer's
+// units), rounds them to fp16 and writes the fp16 words into the staging
+// buffer. (This CTA's softmax reads the slot itself and rounds the same
+// way.) The leader thread then copies the staged tile into the peer's
 // exchange buffer kv & 1 with one bulk copy that counts its bytes on the
 // peer's mbarrier. `bad` carries this thread's earlier timeouts. Returns
 // SEND_STOP in all 128 sender threads if any of them had timed out (then
@@ -345,14 +345,7 @@ __device__ __forceinline__ SendResult send_tile(SM& sm, uint32_t slot, int row, 
     for (int k = 0; k < 8; ++k) {
       h[k] = pack_half2(v0[2 * k], v0[2 * k + 1]);
       h[8 + k] = pack_half2(v1[2 * k], v1[2 * k + 1]);
-      const float2 r0 = unpack_half2(h[k]), r1 = unpack_half2(h[8 + k]);
-      v0[2 * k] = r0.x;
-      v0[2 * k + 1] = r0.y;
-      v1[2 * k] = r1.x;
-      v1[2 * k + 1] = r1.y;
     }
-    tmem_st16(slot + 32 * half, v0);
-    tmem_st16(slot + 32 * half + 16, v1);
   }
   const uint32_t stg = smem_u32(sm.sendbuf);
 #pragma unroll
@@ -362,7 +355,6 @@ __device__ __forceinline__ SendResult send_tile(SM& sm, uint32_t slot, int row, 
   for (int u = 0; u < 4; ++u)
     st_shared_v4(stg + xoff(row, 4 + u), h1[4 * u], h1[4 * u + 1], h1[4 * u + 2], h1[4 * u + 3]);
   fence_proxy_async_smem();  // the staged words are read by the bulk copy
-  tmem_wait_st();
   tc_fence_before();
   named_bar_sync(SEND_BAR, 128);
   if (lane == 0) mbar_arrive(&sm.own_ready[b]);
@@ -456,8 +448,22 @@ __device__ __forceinline__ bool convert_tile(SM& sm, const PairArgs& a, const Ti
   const F8Stage& f = sm.f8.st[s8];
   auto& dst = sm.kv[sc];
   constexpr int kUnits = 18;  // 16-byte input units per row: 16 latent, 2 rotary
+  static_assert(NTHR % 32 == 0, "warps take whole 32-item groups");
   for (int k = ctid; k < TP_TOK * kUnits; k += NTHR) {
-    const int r = k / kUnits, u = k - r * kUnits;
+    // Latent items go in 8-thread phases over rows 2 rp and 2 rp + 1: the
+    // first row's four units of box bsel, the second's of box bsel ^ 1. Their
+    // loads and both stores then fall in eight different 16-byte bank
+    // groups (the rows' swizzles differ in the low bit). Rotary items follow.
+    int r, u;
+    if (k < TP_TOK * 16) {
+      const int rp = k >> 5, bsel = (k >> 3) & 3, t = k & 7, rr = t >> 2;
+      r = 2 * rp + rr;
+      u = 4 * (bsel ^ rr) + (t & 3);
+    } else {
+      const int kk = k - TP_TOK * 16;
+      r = kk >> 1;
+      u = 16 + (kk & 1);
+    }
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < valid)
       v = u < 16 ? *reinterpret_cast<const uint4*>(f.c + r * 256 + u * 16)
@@ -808,8 +814,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       const int t = cur.tile();
       const int s2 = kv % NS;
 
-      // 1. full scaled scores = own fp16-rounded partial (written back into
-      // the score slot by the sender warps) + the peer's (exchange buffer)
+      // 1. full scaled scores = own partial (score slot) rounded to fp16 +
+      // the peer's fp16 partial (exchange buffer): both CTAs add the same two
+      // fp16 values, so they hold bit-identical scores
       bad |= !mbar_wait(&sm.own_ready[b], (kv >> 1) & 1, WAIT_LIMIT);
       bad |= !mbar_wait(&sm.x_full[b], (kv >> 1) & 1, WAIT_LIMIT);
       bad = __any_sync(0xffffffffu, bad);
@@ -831,7 +838,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const int c = 8 * u + 2 * w;
-            const float2 x = add_half2_f32(pw[w], ow[c >> 4][c & 15], ow[c >> 4][(c & 15) + 1]);
+            const float2 o = unpack_half2(pack_half2(ow[c >> 4][c & 15], ow[c >> 4][(c & 15) + 1]));
+            const float2 x = add_half2_f32(pw[w], o.x, o.y);
             sc[c] = x.x;
             sc[c + 1] = x.y;
           }
