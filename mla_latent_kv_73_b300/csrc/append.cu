@@ -601,38 +601,224 @@ bool launch_append_tc(const Shape& s, const Weights* w, const void* x, const App
   return true;
 }
 
+// ---- tensor-core GEMM path for many bf16 tokens ----
+//
+// D[R x T] = Wp x^T in tiles of 128 packed columns x 128 tokens (MMA M and
+// N), one CTA per tile, each over the whole of d_model: thread 0 streams the
+// weight rows and the tokens' hidden states through a 6-stage TMA ring of
+// 64-wide K chunks, thread 32 issues 4 MMAs per chunk into one TMEM
+// accumulator, and no partial sum leaves the CTA. The four warps then read
+// the accumulator (lane = packed column, so a rotary pair sits in two
+// adjacent lanes), apply RoPE with the partner's value from a shuffle, and
+// write each token's row. This is the path for bulk fills and prefill
+// chunks, where the split-K kernel's whole-slice staging does not fit in
+// shared memory.
+constexpr int MM_N = 128;                // tokens per CTA
+constexpr int MM_STAGES = 6;
+constexpr uint32_t MM_ABOX = 128 * 128;  // 128 packed rows x 64 bf16
+constexpr uint32_t MM_BBOX = MM_N * 128; // 128 tokens x 64 bf16
+
+struct __align__(1024) MmSmem {
+  uint8_t a[MM_STAGES][MM_ABOX];
+  uint8_t b[MM_STAGES][MM_BBOX];
+  uint64_t full[MM_STAGES], empty[MM_STAGES], done;
+  long long row[MM_N];                   // cache row of each token of the tile (-1: skip)
+  int pos[MM_N];
+  uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(128, 1)
+append_mm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+                 Shape s, int nk, __nv_bfloat16* __restrict__ cache, AppendArgs a) {
+  using namespace mla_ptx;
+  extern __shared__ uint8_t mm_raw[];
+  MmSmem& sm = *reinterpret_cast<MmSmem*>((reinterpret_cast<uintptr_t>(mm_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+  const int mb = blockIdx.x, t0 = blockIdx.y * MM_N;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int R = s.R();
+  constexpr uint32_t STAGE_TX = MM_ABOX + MM_BBOX;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < MM_STAGES; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    mbar_init(&sm.done, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sm.tmem_base, MM_N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (threadIdx.x == 0) {
+    // The packed weights are complete and never written once their handle
+    // exists: their first chunks are requested before the wait for the
+    // previous kernel; the hidden states only after it.
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_x);
+    const int pre = min(nk, MM_STAGES);
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&sm.full[i], STAGE_TX);
+      tma_load_2d(sm.a[i], &tmap_w, 64 * i, mb * 128, &sm.full[i]);
+    }
+    griddep_wait();
+    for (int i = 0; i < pre; ++i) tma_load_2d(sm.b[i], &tmap_x, 64 * i, t0, &sm.full[i]);
+    int issued = pre;
+    bool ok = true;
+    for (int i = MM_STAGES; i < nk; ++i) {
+      const int st = i % MM_STAGES;
+      if (!mbar_wait(&sm.empty[st], ((i / MM_STAGES) - 1) & 1, AT_WAIT)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&sm.full[st], STAGE_TX);
+      tma_load_2d(sm.a[st], &tmap_w, 64 * i, mb * 128, &sm.full[st]);
+      tma_load_2d(sm.b[st], &tmap_x, 64 * i, t0, &sm.full[st]);
+      issued = i + 1;
+    }
+    if (!ok) {
+      set_error(a.err, MLA_DEVERR_TIMEOUT);
+      // the loads already issued land before the CTA may exit
+      for (int i = max(0, issued - MM_STAGES); i < issued; ++i)
+        mbar_wait(&sm.full[i % MM_STAGES], (i / MM_STAGES) & 1, AT_WAIT);
+    }
+  } else if (threadIdx.x == 32) {
+    const uint32_t idesc = idesc_bf16_f32(128, MM_N, false, false);
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      const int st = i % MM_STAGES;
+      if (!mbar_wait(&sm.full[st], (i / MM_STAGES) & 1, AT_WAIT)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_bf16_ss(tmem, at_desc(sm.a[st], 32 * k), at_desc(sm.b[st], 32 * k), idesc,
+                    (i > 0 || k > 0) ? 1u : 0u);
+      mma_commit(&sm.empty[st]);
+    }
+    if (!ok) set_error(a.err, MLA_DEVERR_TIMEOUT);
+    mma_commit(&sm.done);  // arrives once every MMA issued above is done
+  }
+  griddep_wait();  // (returns at once in the thread that already waited)
+  // the next kernel may be scheduled now; it waits for this grid before it
+  // reads anything this kernel writes
+  griddep_launch_dependents();
+  // the tile's tokens: cache row and position, once each
+  {
+    const int t = t0 + threadIdx.x;
+    long long r = -1;
+    int p = 0;
+    if (t < a.T) {
+      r = append_row(a, s, t);
+      p = a.pos[t];
+    }
+    sm.row[threadIdx.x] = r;
+    sm.pos[threadIdx.x] = p;
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&sm.done, 0, 4 * AT_WAIT);
+  tc_fence_after();
+  if (!ok && threadIdx.x == 0) set_error(a.err, MLA_DEVERR_TIMEOUT);
+  const int pc = mb * 128 + 32 * warp + lane;  // packed column of this lane
+  const bool even = (lane & 1) == 0;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+  for (int c0 = 0; c0 < MM_N && t0 + c0 < a.T; c0 += 16) {
+    float v[16];
+    tmem_ld16(tmem + lane_base + c0, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float partner = __shfl_xor_sync(0xffffffffu, v[i], 1);
+      const long long row = sm.row[c0 + i];
+      if (!ok || row < 0 || pc >= R) continue;
+      float out;
+      const int dst = finish_column(s, a.rope_turns, pc, v[i], even ? v[i] : partner,
+                                    even ? partner : v[i], sm.pos[c0 + i], &out);
+      put_value<__nv_bfloat16>(a, cache, row, R, dst, out);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, MM_N);
+  }
+}
+
+// Launches the GEMM path if it applies (bf16, d_model a multiple of 64,
+// 16-byte aligned x); returns false (nothing launched) otherwise.
+bool launch_append_mm(const Shape& s, const Weights* w, const void* x, const AppendArgs& a,
+                      void* cache, cudaStream_t st, cudaError_t* err) {
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0 || s.d_model % 64 != 0 || s.R() % 2 != 0) return false;
+  TmapSpec ws{};
+  ws.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  ws.rank = 2;
+  ws.base = w->w_dkvr;
+  ws.dims[0] = s.d_model;
+  ws.dims[1] = s.R();
+  ws.strides[0] = static_cast<uint64_t>(s.d_model) * 2;
+  ws.box[0] = 64;
+  ws.box[1] = 128;
+  ws.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  TmapSpec xs{};
+  xs.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  xs.rank = 2;
+  xs.base = x;
+  xs.dims[0] = s.d_model;
+  xs.dims[1] = a.T;
+  xs.strides[0] = static_cast<uint64_t>(s.d_model) * 2;
+  xs.box[0] = 64;
+  xs.box[1] = MM_N;
+  xs.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap tw, tx;
+  if (!get_tmap(ws, &tw) || !get_tmap(xs, &tx)) return false;
+  const size_t smem = sizeof(MmSmem) + 1024;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    if (cudaFuncSetAttribute(append_mm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((s.R() + 127) / 128, (a.T + MM_N - 1) / MM_N, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  // may start while the previous kernel finishes (see the kernel's wait)
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  *err = cudaLaunchKernelEx(&cfg, append_mm_kernel, tw, tx, s, s.d_model / 64,
+                            static_cast<__nv_bfloat16*>(cache), a);
+  return true;
+}
+
 template <typename T>
 cudaError_t append_t(const Shape& s, const Weights* w, const void* x, AppendArgs a, void* cache,
                      cudaStream_t st) {
   const int R = s.R();
   const bool aligned = reinterpret_cast<uintptr_t>(x) % 16 == 0;
   if constexpr (sizeof(T) == 2) {
+    // decode-sized batches: the split-K kernel, whose whole weight slice is
+    // in flight at once; larger ones (or where its staging does not fit):
+    // the tile GEMM
     cudaError_t e = cudaSuccess;
-    if (a.T <= AT_MAX_TOK) {
-      if (launch_append_tc(s, w, x, a, cache, st, &e)) return e;
-    } else {
-      // Bulk fill on the tensor cores: consecutive launches of at most
-      // AT_MAX_TOK tokens each (every launch waits for the one before it,
-      // so the calls write in token order). The weight slice of each launch
-      // is read from L2 after the first.
-      int nkb = 0;
-      size_t smem = 0;
-      const int tail = a.T % AT_MAX_TOK;
-      if (aligned && append_tc_cluster_size(s, AT_MAX_TOK, &nkb, &smem) != 0 &&
-          (tail == 0 || append_tc_cluster_size(s, tail, &nkb, &smem) != 0)) {
-        for (int off = 0; off < a.T; off += AT_MAX_TOK) {
-          AppendArgs c = a;
-          c.seq_idx += off;
-          c.pos += off;
-          if (c.rows_out) c.rows_out += static_cast<size_t>(off) * R;
-          c.T = min(AT_MAX_TOK, a.T - off);
-          const T* xc = static_cast<const T*>(x) + static_cast<size_t>(off) * s.d_model;
-          if (!launch_append_tc(s, w, xc, c, cache, st, &e)) return cudaErrorInvalidValue;
-          if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
-      }
-    }
+    if (a.T <= AT_MAX_TOK && launch_append_tc(s, w, x, a, cache, st, &e)) return e;
+    if (launch_append_mm(s, w, x, a, cache, st, &e)) return e;
   }
   const size_t staged_smem = sizeof(T) * static_cast<size_t>(ST_COLS + ST_TOK) * s.d_model;
   if (a.T <= 256 && aligned && s.d_model % Vec<T>::N == 0 && staged_smem <= 200 * 1024) {

@@ -99,14 +99,16 @@ def test_quantize_rows_bit_exact_and_placed():
     assert np.all(flat_c[untouched] == canary_code) and np.all(flat_s[untouched] == canary_scale)
 
 
-@pytest.mark.parametrize("T", [70, 600])
-def test_append_fp8_rows_within_the_rounding_bound(T):
-    """Rows from hidden states (one chunk; three chunks of at most 256),
-    dequantised, against the oracle's fp64 rows: each element within half
-    an e4m3 step (2^-4 of its magnitude in the normal range, 2^-10 of the
-    row scale below it), plus the fp32 row's own rounding."""
-    w = synth.Workload("fp8_append", n_h=128, d_model=1024, d_c=512, d_r=64, d_nope=128, d_v=128,
-                       batch=3, n_q=1, len_lo=0, len_hi=0, dtype="bf16", seed=53)
+@pytest.mark.parametrize("T,d_model", [(70, 1024), (600, 1024), (300, 5120)])
+def test_append_fp8_rows_within_the_rounding_bound(T, d_model):
+    """Rows from hidden states (one chunk; three chunks of at most 256; at
+    d_model 5120 a 256-token chunk on the tile GEMM and a 44-token one on
+    the split-K kernel), dequantised, against the oracle's fp64 rows: each
+    element within half an e4m3 step (2^-4 of its magnitude in the normal
+    range, 2^-10 of the row scale below it), plus the fp32 row's own
+    rounding."""
+    w = synth.Workload("fp8_append", n_h=128, d_model=d_model, d_c=512, d_r=64, d_nope=128,
+                       d_v=128, batch=3, n_q=1, len_lo=0, len_hi=0, dtype="bf16", seed=53)
     lens = np.array([131072, 900, 64], dtype=np.int32)
     pt, nb = synth.page_table(w, lens)
     g = np.random.default_rng(54)

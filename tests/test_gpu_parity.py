@@ -159,10 +159,14 @@ def test_append_places_rows_exactly(wname, T):
 
 
 @pytest.mark.parametrize("wname,T,d_model", [("dsv2_b16_l4096", 1024, None),
+                                             ("dsv2_b16_l4096", 200, None),
+                                             ("nh16_b256_ragged", 300, None),
                                              ("tiny_fp32", 600, None),
                                              ("tiny_fp32", 20, 4096)])
 def test_append_bulk_and_far_positions(wname, T, d_model):
-    """One call with T > 256 new tokens (the bulk-fill path), or a wide fp32
+    """One call with many new tokens (the tile-GEMM path: 1024 and 300
+    tokens, and 200 at d_model 5120, where the split-K kernel's staging does
+    not fit; the last tile of 128 tokens partly filled), or a wide fp32
     model with few tokens (the direct-load path), at positions up to 131071:
     each row against the oracle's latent_rows (RoPE at the largest
     positions included), placed exactly, every other row untouched."""
@@ -410,6 +414,61 @@ def test_full_size_sampled(wname):
     samples = _samples(w, lens, np.random.default_rng(w.seed))
     ref = r.oracle(samples=samples)
     check_bf16_each([got[s] for s in samples], [ref[s] for s in samples], wname)
+    r.dw.free()
+
+
+# ---------------------------------------------------------------------------
+# The attention core alone (a3 + a4): mla_decode_latent
+# ---------------------------------------------------------------------------
+
+
+def run_latent(r):
+    """mla_decode_latent on Run r's cache with the seeded latent queries:
+    (o_lat on the host, the query values the oracle takes)."""
+    w = r.w
+    qv, qs = synth.latent_queries(w)
+    o = torch.full((w.batch, w.n_q, w.n_h, w.d_c), float("nan"), device="cuda")
+    _lib.mla_decode_latent(r.cfg, to_device(qs, w.dtype), r.cache, r.pt, r.sl, o, r.ws)
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0
+    return o.cpu().numpy(), qv
+
+
+@pytest.mark.parametrize("impl", list(IMPLS))
+@pytest.mark.parametrize("n_q", [1, 2])
+def test_decode_latent_core_small(impl, n_q):
+    """o_lat against the oracle's latent core, every (sequence, query, head)
+    vector on its own; sequences of 2 to 700 tokens (ragged last pages)."""
+    w, lens = small_workload(lens=(2, 64, 65, 200, 700), n_q=n_q, seed=61)
+    r = Run(w, lens, IMPLS[impl])
+    got, qv = run_latent(r)
+    ref = O.decode_latent(qv, r.rows, lens, w.d_c, w.scale)
+    keys = [(b, i, h) for b in range(w.batch) for i in range(n_q) for h in range(w.n_h)]
+    check_bf16_each([got[k] for k in keys], [ref[k] for k in keys], f"latent {impl} n_q={n_q}")
+    r.dw.free()
+
+
+def test_decode_latent_core_fp32():
+    w = synth.WORKLOADS["tiny_fp32"]
+    lens = synth.seq_lens(w)
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO)
+    got, qv = run_latent(r)
+    check_f32(got, O.decode_latent(qv, r.rows, lens, w.d_c, w.scale), "latent fp32")
+    r.dw.free()
+
+
+def test_decode_latent_core_full_size_sampled():
+    """The headline workload (batch 64, 512-32768 cached tokens) on the
+    tensor-core attention: sampled o_lat vectors against the oracle."""
+    w = synth.WORKLOADS["dsv2_b64_ragged"]
+    lens = synth.seq_lens(w)
+    r = Run(w, lens, _lib.MLA_IMPL_AUTO, fill=0.0, spare_blocks=0)
+    got, qv = run_latent(r)
+    assert np.all(np.isfinite(got))
+    samples = _samples(w, lens, np.random.default_rng(w.seed + 7))
+    ref = O.decode_latent(qv, r.rows, lens, w.d_c, w.scale, samples=samples)
+    check_bf16_each([got[s] for s in samples], [ref[s] for s in samples], "latent b64")
     r.dw.free()
 
 
