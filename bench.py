@@ -419,6 +419,29 @@ def measure_workload(args, w, K, warmup, world, rank, local, dist, headline, min
     torch.cuda.synchronize()
     attend_ms = [a0.elapsed_time(a1) / (Ka * R)]
 
+    # the attention core a3 + a4 (mla_decode_latent: latent queries in, the
+    # merged o_lat out), timed the same way
+    q_lat_abs = torch.randn((B, n_q, w.n_h, w.R), generator=gen, device="cuda").to(dt)
+    o_lat = torch.empty((B, n_q, w.n_h, w.d_c), device="cuda")
+    g_core = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_core):
+        for i in range(R):
+            s_ = sets[i % n_sets]
+            _lib.mla_decode_latent(cfg, q_lat_abs, s_["cache"], s_["pt"], seq_lens, o_lat, ws,
+                                   torch.cuda.current_stream())
+    g_core.replay()
+    torch.cuda.synchronize()
+    a0.record()
+    for i in range(Ka):
+        g_core.replay()
+    a1.record()
+    torch.cuda.synchronize()
+    core_ms = a0.elapsed_time(a1) / (Ka * R)
+    st, code = _lib.mla_get_last_device_error(stream)
+    if code:
+        raise RuntimeError(f"{w.name}: device error word {code:#x} in the core timing")
+    del q_lat_abs, o_lat, g_core
+
     # the four stages inside whole-step graph replays (events between them)
     for g in g_prof:
         g.replay()
@@ -444,6 +467,10 @@ def measure_workload(args, w, K, warmup, world, rank, local, dist, headline, min
     att = roofline_entry(cache_bytes, attn_flops, att_ms, hbm, tflops)
     att["kernel"] = "attend_tc_kernel" if impl == 2 else "attend_simt_kernel"
     att["kernel_ms"] = round(att_ms, 5)
+    core = roofline_entry(cache_bytes, attn_flops, core_ms, hbm, tflops)
+    core["kernel_ms"] = round(core_ms, 5)
+    core["what"] = ("attention core a3 + a4 (mla_decode_latent: query copy and plan, "
+                    "attention, log-sum-exp merge into o_lat) against the cache roofline")
     step_roof = roofline_entry(step_bytes, step_flops, ms_per_step, hbm, tflops)
     step_roof["bytes"] = int(step_bytes)
     step_roof["flops"] = float(step_flops)
@@ -454,7 +481,8 @@ def measure_workload(args, w, K, warmup, world, rank, local, dist, headline, min
         "tokens_per_s": round(value, 1),
         "cache_gbs": round(cache_bytes * K / (total_ms_max / 1e3) / 1e9, 1),
         "cache_bytes": int(cache_bytes), "attention_flops": float(attn_flops),
-        "attention_roofline": att, "step_roofline": step_roof, "stage_us": stages,
+        "attention_roofline": att, "core_roofline": core, "step_roofline": step_roof,
+        "stage_us": stages,
         "impl": impl, "peak_source": src, "lens": lens, "n_sets": n_sets,
         "set_bytes": set_bytes, "l2": l2, "clocks": clocks, "host_us": host_us,
     }
@@ -753,6 +781,8 @@ def per_config_row(r):
             "steps": r["steps"], "cache_gbs": r["cache_gbs"],
             "attention": {k: a[k] for k in ("bound", "achieved", "unit", "frac", "kernel_ms",
                                             "roofline_ms", "gbs", "tflops")},
+            "core_a3_a4": {k: r["core_roofline"][k] for k in ("bound", "achieved", "unit", "frac",
+                                                             "kernel_ms", "roofline_ms")},
             "step": {k: s[k] for k in ("bound", "achieved", "unit", "frac", "roofline_ms",
                                        "gbs", "tflops")},
             "stage_us": r["stage_us"]}
@@ -819,6 +849,7 @@ def run_ours(args, world, rank, local):
                    "decode_kernel": "tensor_core" if r["impl"] == 2 else "cuda_core"},
         "cache_gbs": r["cache_gbs"],
         "roofline": roof,
+        "core_roofline": r["core_roofline"],
         "step_roofline": r["step_roofline"],
         "per_config": rows,
         "per_config_fp8": rows_fp8,

@@ -204,6 +204,32 @@ mla_status mla_decode_combine(const mla_config* cfg, mla_weights w, const int32_
                               int32_t B, int32_t n_q, float* out, void* workspace,
                               size_t ws_bytes, cudaStream_t stream);
 
+/* The attention core alone (a3 + a4): split-KV attention of queries that
+ * are already in latent space over the paged cache, and the log-sum-exp
+ * merge of the splits, with neither the W_uk fold nor the W_uv
+ * up-projection.
+ * Source: "Multi-head Latent Attention and KV Cache Compression", section
+ * "The absorption trick and decoupled RoPE" (score = q_lat . c + q_pe .
+ * k_rope; the output side keeps the weighted latent sum); "Multi-head
+ * Latent Attention: the KV cache, compressed", section "RoPE, and why the
+ * explanations stop here" (the position part is a separate product).
+ *   q_abs      [B, n_q, n_h, d_c + d_r] cfg->dtype: per head [q_lat | q_pe],
+ *              q_lat = W_uk[h]^T q_nope and q_pe = RoPE(q_rope, position)
+ *              already applied, not yet scaled
+ *   cache, page_table, seq_lens: as for mla_decode
+ *   o_lat      [B, n_q, n_h, d_c] fp32: sum_j p_j c_j, p = softmax over the
+ *              keys the query sees of scale * (q_lat . c_j + q_pe . k_rope_j);
+ *              16-byte aligned (MLA_ERR_INVALID_ARG otherwise, before any
+ *              work is queued)
+ *   workspace  at least mla_decode_workspace_size() bytes, 256-byte aligned
+ * The queries are copied into the workspace (times scale, in the attention
+ * kernel's operand type), so q_abs has no alignment requirement. Errors as
+ * for mla_decode. Needs no weights handle. */
+mla_status mla_decode_latent(const mla_config* cfg, const void* q_abs, const void* cache,
+                             int32_t num_blocks, const int32_t* page_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t B, int32_t n_q, float* o_lat,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * fp8 latent cache: e4m3 codes with one fp32 scale per cache row.
  *

@@ -28,7 +28,7 @@ EXPORTS = ["mla_absorb_weights", "mla_weights_free", "mla_append_kv",
            "mla_fold_full", "mla_full_weights_free", "mla_decode_full_workspace_size",
            "mla_decode_full", "mla_decode_layer_workspace_size", "mla_decode_layer",
            "mla_quantize_rows_fp8", "mla_append_kv_fp8_workspace_size", "mla_append_kv_fp8",
-           "mla_decode_fp8"]
+           "mla_decode_fp8", "mla_decode_latent"]
 MLA_NO_ALLOC_WORKSPACE_BYTES = 32 << 20
 
 
@@ -62,6 +62,7 @@ def _declare(lib):
         "mla_decode": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_decode_absorb_q": [cfgp, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P],
         "mla_decode_attend": [cfgp, _P, _I, _P, _I, _P, _I, _I, _P, ctypes.c_size_t, _P],
+        "mla_decode_latent": [cfgp, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_decode_combine": [cfgp, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P],
         "mla_decode_impl": [cfgp, ctypes.POINTER(_I)],
         "mla_decode_no_alloc": [cfgp, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P],
@@ -223,6 +224,16 @@ def mla_decode_attend(cfg, cache, page_table, seq_lens, B, n_q, workspace, strea
         ctypes.byref(cfg), ptr(cache), cache.shape[0], ptr(page_table), page_table.shape[1],
         ptr(seq_lens), B, n_q, ptr(workspace), workspace.numel() * workspace.element_size(),
         stream_handle(stream)))
+
+
+def mla_decode_latent(cfg, q_abs, cache, page_table, seq_lens, o_lat, workspace, stream=None):
+    """The attention core alone: q_abs [B, n_q, n_h, d_c + d_r] (absorbed and
+    rotated, unscaled) -> o_lat [B, n_q, n_h, d_c] fp32 (see include/mla.h)."""
+    B, n_q = q_abs.shape[0], q_abs.shape[1]
+    check("mla_decode_latent", load().mla_decode_latent(
+        ctypes.byref(cfg), ptr(q_abs), ptr(cache), cache.shape[0], ptr(page_table),
+        page_table.shape[1], ptr(seq_lens), B, n_q, ptr(o_lat), ptr(workspace),
+        workspace.numel() * workspace.element_size(), stream_handle(stream)))
 
 
 def mla_decode_combine(cfg, w, seq_lens, B, n_q, out, workspace, stream=None):

@@ -518,6 +518,42 @@ mla_status mla_decode(const mla_config* cfg, mla_weights w, const void* q, const
   return mla_decode_combine(&c2, w, seq_lens, B, n_q, out, workspace, ws_bytes, stream);
 }
 
+mla_status mla_decode_latent(const mla_config* cfg, const void* q_abs, const void* cache,
+                             int32_t num_blocks, const int32_t* page_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t B, int32_t n_q, float* o_lat,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (!q_abs || !cache || !page_table || !seq_lens || !o_lat) return MLA_ERR_INVALID_ARG;
+  // both merge kernels write o_lat in 16-byte vectors
+  if (!aligned16(o_lat)) return MLA_ERR_INVALID_ARG;
+  if (num_blocks < 1 || max_blocks < 1) return MLA_ERR_SHAPE;
+  Plan p;
+  const DeviceInfo* di = nullptr;
+  mla_status st = prepare_decode(cfg, B, n_q, cache, workspace, ws_bytes, &p, &di, true);
+  if (st != MLA_OK) return st;
+  if (static_cast<long long>(num_blocks) * cfg->block_size > (1LL << 31) - 1) return MLA_ERR_SHAPE;
+  const WsView v = ws_view(workspace, p.lay);
+  const bool tc = p.impl == MLA_IMPL_TENSOR_CORE;
+  // the tensor-core attention reads queries pre-multiplied by scale * log2(e)
+  const float out_scale = tc ? p.s.scale * 1.4426950408889634f : 1.f;
+  cudaError_t e = launch_latent_q(p.s, cfg->dtype, q_abs, seq_lens, max_blocks, B, n_q, p.part, v,
+                                  out_scale, !tc, di->err, stream);
+  if (e == cudaSuccess) {
+    if (tc)
+      e = launch_attend_tc(p.s, cache, num_blocks, page_table, max_blocks, B, n_q, p.part, v,
+                           seq_lens, di->err, stream);
+    else
+      e = launch_attend_simt(p.s, cfg->dtype, cache, num_blocks, page_table, max_blocks, B, n_q,
+                             p.part, v, seq_lens, di->err, stream);
+  }
+  if (e == cudaSuccess) {
+    if (tc && combine_latent_tc_supported(p.s))
+      e = launch_combine_latent_tc(p.s, B, n_q, p.part, v, o_lat, di->err, stream);
+    else
+      e = launch_combine_latent(p.s, B, n_q, p.part, v, o_lat, stream);
+  }
+  return from_cuda(e);
+}
+
 mla_status mla_quantize_rows_fp8(const mla_config* cfg, const float* rows, const int32_t* seq_idx,
                                  const int32_t* pos, const int32_t* page_table, int32_t B,
                                  int32_t max_blocks, void* cache, float* row_scale,

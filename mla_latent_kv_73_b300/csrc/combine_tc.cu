@@ -23,6 +23,7 @@
 // accuracy. Four warps read the four fp32 accumulators from TMEM, one output
 // column per lane, add them in a fixed order and store the sum.
 #include <cmath>
+#include <cstring>
 
 #include "device_common.cuh"
 #include "plan.cuh"
@@ -40,13 +41,26 @@ constexpr uint32_t CT_WBOX = 128 * 128;      // 128 rows x 64 bf16
 constexpr uint32_t CT_OBOX = CT_TOK * 128;   // 32 token rows x 64 bf16
 constexpr long long CT_WAIT = 2000000000LL;
 
+// Per token of the CTA: the first and last range holding its pieces, and its
+// row offset inside a slot of the partials.
+struct CombPlan {
+  int c_lo[CT_TOK], c_hi[CT_TOK], row_off[CT_TOK];
+};
+
 struct __align__(1024) CombSmem {
   uint8_t w[8][CT_WBOX];          // K-chunk kc of W_uv[h]: 128 output rows x 64 latent dims
   uint8_t o[2][8][CT_OBOX];       // [hi/lo][K-chunk]: token rows x 64 latent dims
   uint64_t wfull, done;
   uint32_t tmem_base;
-  int c_lo[CT_TOK], c_hi[CT_TOK], row_off[CT_TOK];
+  CombPlan plan;
 };
+
+// Shared memory before the range starts and merge weights: the whole
+// CombSmem, or only the plan in the latent mode.
+template <bool LATENT>
+constexpr size_t comb_head_bytes() {
+  return LATENT ? (sizeof(CombPlan) + 15) / 16 * 16 : sizeof(CombSmem);
+}
 
 __device__ __forceinline__ uint64_t kdesc(const void* base, uint32_t byte_off) {
   return smem_desc(smem_u32(base) + byte_off, 16, 1024, kSwizzle128B);
@@ -57,6 +71,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// LATENT: merge only, writing o_lat [B*n_q][n_h][512] fp32 to `out` (no W_uv,
+// no TMEM, no MMA); the attention core alone (mla_decode_latent).
+template <bool LATENT>
 __global__ void __launch_bounds__(CT_THREADS, 1)
 combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
                   const int32_t* __restrict__ tiles, const int32_t* __restrict__ prefix,
@@ -65,35 +82,40 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
                   const float* __restrict__ part_lse, float* __restrict__ out,
                   uint16_t* __restrict__ hilo, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
-  CombSmem& sm = *reinterpret_cast<CombSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~static_cast<uintptr_t>(1023));
-  long long* rb = reinterpret_cast<long long*>(&sm + 1);  // [C + 1] range starts
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  CombSmem& sm = *reinterpret_cast<CombSmem*>(base);  // touched only outside the latent mode
+  CombPlan& pl = LATENT ? *reinterpret_cast<CombPlan*>(base) : sm.plan;
+  long long* rb = reinterpret_cast<long long*>(base + comb_head_bytes<LATENT>());  // [C + 1] range starts
   const int h = blockIdx.x, t0 = blockIdx.y * CT_TOK;
   const int Tq = B * n_q, ntok = min(CT_TOK, Tq - t0);
   const int n_box = ((ntok + 15) / 16) * 16;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-  if (threadIdx.x == 0) {
-    mbar_init(&sm.wfull, 1);
-    mbar_init(&sm.done, 4);  // one commit per K quarter
-    fence_mbarrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, 128);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;
-  // With programmatic dependent launch this CTA may start while the attention
-  // kernel still runs. The packed W_uv is complete and never written once its
-  // handle exists, so its loads start at once; everything the attention
-  // kernel writes is read only after the wait.
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&tmap_w);
-    mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
-    for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
+  uint32_t tmem = 0;
+  if constexpr (!LATENT) {
+    if (threadIdx.x == 0) {
+      mbar_init(&sm.wfull, 1);
+      mbar_init(&sm.done, 4);  // one commit per K quarter
+      fence_mbarrier_init();
+    }
+    if (warp == 1) {
+      tmem_alloc(&sm.tmem_base, 128);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = sm.tmem_base;
+    // With programmatic dependent launch this CTA may start while the
+    // attention kernel still runs. The packed W_uv is complete and never
+    // written once its handle exists, so its loads start at once; everything
+    // the attention kernel writes is read only after the wait.
+    if (threadIdx.x == 0) {
+      prefetch_tmap(&tmap_w);
+      mbar_arrive_expect_tx(&sm.wfull, 8 * CT_WBOX);
+      for (int kc = 0; kc < 8; ++kc) tma_load_2d(sm.w[kc], &tmap_w, 64 * kc, h * 128, &sm.wfull);
+    }
   }
   griddep_wait();
   // the next kernel (its weights are constant) may start its prologue now;
@@ -123,17 +145,17 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
       c0 = range_of_item(rb, p.C, my_first);
       c1 = range_of_item(rb, p.C, my_first + my_tiles - 1);
     }
-    sm.c_lo[threadIdx.x] = c0;
-    sm.c_hi[threadIdx.x] = c1;
-    sm.row_off[threadIdx.x] = my_off;
+    pl.c_lo[threadIdx.x] = c0;
+    pl.c_hi[threadIdx.x] = c1;
+    pl.row_off[threadIdx.x] = my_off;
   }
   __syncthreads();
   float* wts = reinterpret_cast<float*>(rb + p.C + 1);  // [CT_TOK][C + 1] merge weights
   for (int tb = 0; tb < ntok; tb += 2 * (CT_THREADS / 32)) {
     const int t = tb + 2 * warp + (lane >> 4), hl = lane & 15;
     const bool live = t < ntok;
-    const int c0 = live ? sm.c_lo[t] : 0, c1 = live ? sm.c_hi[t] : -1;
-    const int off = live ? sm.row_off[t] : 0;
+    const int c0 = live ? pl.c_lo[t] : 0, c1 = live ? pl.c_hi[t] : -1;
+    const int off = live ? pl.row_off[t] : 0;
     float M = -INFINITY;
     for (int c = c0 + hl; c <= c1; c += 16) {
       const float x = rb[c] != rb[c + 1] ? part_lse[static_cast<size_t>(c) * p.RG + off] : -INFINITY;
@@ -152,7 +174,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
     for (int o = 8; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int c = c0 + hl; c <= c1; c += 16) wts[t * (p.C + 1) + (c - c0)] *= inv;
-    if (live && hl == 0 && M == -INFINITY) sm.c_hi[t] = -1;  // no piece holds a visible token
+    if (live && hl == 0 && M == -INFINITY) pl.c_hi[t] = -1;  // no piece holds a visible token
   }
   __syncthreads();
 
@@ -177,9 +199,9 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
         hi[j] = -1;
         off[j] = 0;
         if (tt < ntok) {
-          lo[j] = sm.c_lo[tt];
-          hi[j] = sm.c_hi[tt];
-          off[j] = sm.row_off[tt];
+          lo[j] = pl.c_lo[tt];
+          hi[j] = pl.c_hi[tt];
+          off[j] = pl.row_off[tt];
           nb = max(nb, (hi[j] - lo[j] + 4) / 4);
         }
       }
@@ -216,6 +238,18 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
             acc[j][7] = fmaf(wg[j][q], vb[j][q].w, acc[j][7]);
           }
       }
+      if constexpr (LATENT) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int tt = tb + g + 4 * j;
+          if (tt >= ntok) continue;
+          float4* dst = reinterpret_cast<float4*>(
+              out + (static_cast<size_t>(t0 + tt) * n_h + h) * 512 + 8 * u);
+          dst[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+          dst[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+        }
+        continue;
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tt = tb + g + 4 * j;
@@ -232,6 +266,7 @@ combine_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, int n_h,
       }
     }
   }
+  if constexpr (LATENT) return;
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -314,30 +349,21 @@ bool combine_tc_supported(const Shape& s, mla_dtype dt) {
   return dt == MLA_BF16 && s.d_c == 512 && s.d_v == 128;
 }
 
-cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
-                              const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
-                              uint32_t* err, cudaStream_t st) {
+namespace {
+
+template <bool LATENT>
+cudaError_t combine_tc_t(const Shape& s, const CUtensorMap& tw, int B, int n_q,
+                         const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
+                         uint32_t* err, cudaStream_t st) {
   const int Tq = B * n_q;
-  TmapSpec spec{};
-  spec.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  spec.rank = 2;
-  spec.base = w->w_uv;
-  spec.dims[0] = 512;
-  spec.dims[1] = static_cast<uint64_t>(s.n_h) * 128;
-  spec.strides[0] = 1024;
-  spec.box[0] = 64;
-  spec.box[1] = 128;
-  spec.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
-  CUtensorMap tw;
-  if (!get_tmap(spec, &tw)) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(CombSmem) + 1024 + sizeof(long long) * (p.C + 1) +
+  const size_t smem = comb_head_bytes<LATENT>() + 1024 + sizeof(long long) * (p.C + 1) +
                       sizeof(float) * CT_TOK * (p.C + 1);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   static int attr_bytes[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || attr_bytes[dev] < static_cast<int>(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(combine_tc_kernel<LATENT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -354,12 +380,42 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_tc_kernel, tw, s.n_h,
+  return cudaLaunchKernelEx(&cfg, combine_tc_kernel<LATENT>, tw, s.n_h,
                             static_cast<const int32_t*>(ws.tiles),
                             static_cast<const int32_t*>(ws.prefix),
                             static_cast<const long long*>(ws.bounds), B, n_q, p,
                             static_cast<const float*>(ws.part_o),
                             static_cast<const float*>(ws.part_lse), out, hilo, err);
+}
+
+}  // namespace
+
+cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
+                              const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
+                              uint32_t* err, cudaStream_t st) {
+  TmapSpec spec{};
+  spec.dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  spec.rank = 2;
+  spec.base = w->w_uv;
+  spec.dims[0] = 512;
+  spec.dims[1] = static_cast<uint64_t>(s.n_h) * 128;
+  spec.strides[0] = 1024;
+  spec.box[0] = 64;
+  spec.box[1] = 128;
+  spec.swizzle = CU_TENSOR_MAP_SWIZZLE_128B;
+  CUtensorMap tw;
+  if (!get_tmap(spec, &tw)) return cudaErrorInvalidValue;
+  return combine_tc_t<false>(s, tw, B, n_q, p, ws, out, hilo, err, st);
+}
+
+bool combine_latent_tc_supported(const Shape& s) { return s.d_c == 512; }
+
+cudaError_t launch_combine_latent_tc(const Shape& s, int B, int n_q, const Partition& p,
+                                     const WsView& ws, float* olat, uint32_t* err,
+                                     cudaStream_t st) {
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  return combine_tc_t<true>(s, unused, B, n_q, p, ws, olat, nullptr, err, st);
 }
 
 }  // namespace mla

@@ -436,6 +436,51 @@ cudaError_t q_finish_t(const Shape& s, const uint64_t* rope_turns, const float* 
   return cudaGetLastError();
 }
 
+// qabs = out_scale * q_abs, element by element, in T (the attention kernel's
+// query type), from queries the caller has already absorbed and rotated
+// (mla_decode_latent). Block 0 also writes the split-KV plan.
+template <typename TI, typename T>
+__global__ void __launch_bounds__(QF_THREADS)
+latent_q_kernel(Shape s, const TI* __restrict__ q_abs, size_t n, const int32_t* __restrict__ seq_lens,
+                int B, int n_q, int max_blocks, int TS, int G, int C, int K, float out_scale,
+                T* __restrict__ qabs, int32_t* tiles, int32_t* prefix, long long* bounds,
+                int32_t* first_b, uint32_t* err) {
+  if (blockIdx.x == 0)
+    write_plan<QF_THREADS>(seq_lens, B, n_q, max_blocks, s.bs, TS, G, C, K, tiles, prefix, bounds,
+                           first_b, err);
+  const size_t stride = static_cast<size_t>(gridDim.x) * QF_THREADS;
+  const size_t first = static_cast<size_t>(blockIdx.x) * QF_THREADS + threadIdx.x;
+  if constexpr (sizeof(TI) == 2 && sizeof(T) == 2) {
+    // eight elements per 16-byte access where the caller's buffer allows it
+    if (reinterpret_cast<uintptr_t>(q_abs) % 16 == 0 && n % 8 == 0) {
+      for (size_t i = first; i < n / 8; i += stride) {
+        uint4 v = reinterpret_cast<const uint4*>(q_abs)[i];
+        TI* x = reinterpret_cast<TI*>(&v);
+        uint4 o;
+        T* y = reinterpret_cast<T*>(&o);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = from_f32<T>(to_f32<TI>(x[k]) * out_scale);
+        reinterpret_cast<uint4*>(qabs)[i] = o;
+      }
+      return;
+    }
+  }
+  for (size_t i = first; i < n; i += stride) qabs[i] = from_f32<T>(to_f32<TI>(q_abs[i]) * out_scale);
+}
+
+template <typename TI, typename T>
+cudaError_t latent_q_t(const Shape& s, const void* q_abs, const int32_t* seq_lens, int max_blocks,
+                       int B, int n_q, const Partition& p, const WsView& ws, float out_scale,
+                       uint32_t* err, cudaStream_t st) {
+  const size_t n = static_cast<size_t>(B) * n_q * s.n_h * s.R();
+  const size_t blocks = (n / 8 + QF_THREADS) / QF_THREADS;
+  latent_q_kernel<TI, T><<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), QF_THREADS, 0,
+                           st>>>(s, static_cast<const TI*>(q_abs), n, seq_lens, B, n_q, max_blocks,
+                                 p.TS, p.G, p.C, p.K, out_scale, static_cast<T*>(ws.qabs),
+                                 ws.tiles, ws.prefix, ws.bounds, ws.first_b, err);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // K is split so that the grid fills the two CTAs per SM that the ring kernel
@@ -554,6 +599,20 @@ cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const uint64_t* rope_t
                              err, st);
   return q_finish_t<__nv_bfloat16>(s, rope_turns, qpre, seq_lens, max_blocks, B, n_q, p, ws,
                                    out_scale, err, st);
+}
+
+cudaError_t launch_latent_q(const Shape& s, mla_dtype dt, const void* q_abs,
+                            const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                            const Partition& p, const WsView& ws, float out_scale, bool q_f32,
+                            uint32_t* err, cudaStream_t st) {
+  if (dt == MLA_F32)
+    return latent_q_t<float, float>(s, q_abs, seq_lens, max_blocks, B, n_q, p, ws, out_scale, err,
+                                    st);
+  if (q_f32)
+    return latent_q_t<__nv_bfloat16, float>(s, q_abs, seq_lens, max_blocks, B, n_q, p, ws,
+                                            out_scale, err, st);
+  return latent_q_t<__nv_bfloat16, __nv_bfloat16>(s, q_abs, seq_lens, max_blocks, B, n_q, p, ws,
+                                                  out_scale, err, st);
 }
 
 }  // namespace mla

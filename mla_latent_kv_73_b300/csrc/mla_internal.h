@@ -151,6 +151,13 @@ cudaError_t launch_combine_tc(const Shape& s, const Weights* w, int B, int n_q,
                               const Partition& p, const WsView& ws, float* out, uint16_t* hilo,
                               uint32_t* err, cudaStream_t st);
 
+// The merge alone on the tensor-core partition (d_c = 512): o_lat
+// [B*n_q][n_h][512] fp32, without the up-projection.
+bool combine_latent_tc_supported(const Shape& s);
+cudaError_t launch_combine_latent_tc(const Shape& s, int B, int n_q, const Partition& p,
+                                     const WsView& ws, float* olat, uint32_t* err,
+                                     cudaStream_t st);
+
 cudaError_t launch_combine(const Shape& s, mla_dtype dt, const Weights* w,
                            const int32_t* seq_lens, int B, int n_q, const Partition& p,
                            const WsView& ws, float* out, cudaStream_t st);
@@ -179,6 +186,12 @@ cudaError_t launch_q_finish(const Shape& s, mla_dtype dt, const uint64_t* rope_t
                             bool q_f32, uint32_t* err, cudaStream_t st);
 cudaError_t launch_combine_latent(const Shape& s, int B, int n_q, const Partition& p,
                                   const WsView& ws, float* olat, cudaStream_t st);
+// The workspace's qabs = out_scale * q_abs (caller-absorbed queries in dt;
+// fp32 when q_f32, else dt) and the split-KV plan, for mla_decode_latent.
+cudaError_t launch_latent_q(const Shape& s, mla_dtype dt, const void* q_abs,
+                            const int32_t* seq_lens, int max_blocks, int B, int n_q,
+                            const Partition& p, const WsView& ws, float out_scale, bool q_f32,
+                            uint32_t* err, cudaStream_t st);
 // out[i] = sum_z part[z][i] over the S splits, in increasing z.
 cudaError_t launch_sum_splits(const float* part, int S, size_t n, float* out, cudaStream_t st);
 

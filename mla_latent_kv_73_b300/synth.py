@@ -26,7 +26,7 @@ import math
 import numpy as np
 
 # Sub-stream ids
-_S_WEIGHTS, _S_LENS, _S_PAGES, _S_CACHE, _S_Q, _S_X, _S_FP8 = 1, 2, 3, 4, 5, 6, 7
+_S_WEIGHTS, _S_LENS, _S_PAGES, _S_CACHE, _S_Q, _S_X, _S_FP8, _S_QLAT = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 @dataclasses.dataclass(frozen=True)
@@ -215,6 +215,18 @@ def fill_paged_cache(w: Workload, lens, pt, num_blocks, fill_value=0.0,
 def queries(w: Workload):
     """q [B, n_q, n_h, d_nope + d_r] before RoPE: (values float32, storage)."""
     a = normal(rng(w.seed, _S_Q), (w.batch, w.n_q, w.n_h, w.d_nope + w.d_r))
+    return to_dtype(a, w.dtype)
+
+
+def latent_queries(w: Workload):
+    """Queries already in latent space, [B, n_q, n_h, d_c + d_r] per head
+    [q_lat | q_pe], for the attention core alone: (values float32, storage).
+    q_lat ~ N(0, d_nope / d_c), the spread that W_uk^T q_nope has for the
+    workloads' weights and queries, and q_pe ~ N(0, 1)."""
+    g = rng(w.seed, _S_QLAT)
+    shape = (w.batch, w.n_q, w.n_h)
+    a = np.concatenate([normal(g, shape + (w.d_c,), math.sqrt(w.d_nope / w.d_c)),
+                        normal(g, shape + (w.d_r,))], axis=-1)
     return to_dtype(a, w.dtype)
 
 

@@ -343,6 +343,50 @@ def decode_head_absorbed(q_head, rows, pos_q, W_uk_h, W_uv_h, d_c, scale, base):
     return o_lat @ W_uv_h
 
 
+def latent_attention_head(q_lat, q_pe, rows, pos_q, d_c, scale):
+    """The latent output of one head for one query, before the value
+    up-projection: o_lat = sum_j p_j c_j with p = softmax over the visible
+    keys (j <= pos_q) of scale * (q_lat . c_j + q_pe . k_rope_j).
+
+    [P5] "The absorption trick and decoupled RoPE" (the content score is
+    q_lat . c with q_lat = W_uk^T q_nope, the position score q_pe . k_rope
+    is added, and the output side keeps the weighted latent sum, W_uv being
+    applied once afterwards); [P1] "RoPE, and why the explanations stop
+    here" (the position part is its own inner product). q_pe is already
+    rotated; rows: [L, d_c + d_r] logical cache rows.
+    """
+    q_lat = np.asarray(q_lat, dtype=np.float64)
+    q_pe = np.asarray(q_pe, dtype=np.float64)
+    rows = np.asarray(rows, dtype=np.float64)
+    C, KR = rows[:, :d_c], rows[:, d_c:]
+    s = (C @ q_lat + KR @ q_pe) * scale
+    s = np.where(np.arange(rows.shape[0]) <= pos_q, s, -np.inf)
+    return softmax(s) @ C
+
+
+def decode_latent(q_abs, seq_rows, seq_lens, d_c, scale, samples=None):
+    """latent_attention_head over a batch: q_abs [B, n_q, n_h, d_c + d_r]
+    holds per head [q_lat | q_pe]; query i of sequence b sits at position
+    seq_lens[b] - n_q + i. Returns [B, n_q, n_h, d_c] (NaN where not
+    sampled) when samples is None, else a dict keyed by (b, i, h)."""
+    q_abs = np.asarray(q_abs, dtype=np.float64)
+    B, n_q, n_h, _ = q_abs.shape
+    want = samples
+    if want is None:
+        want = [(b, i, h) for b in range(B) for i in range(n_q) for h in range(n_h)]
+    res = {}
+    for (b, i, h) in want:
+        L = int(seq_lens[b])
+        res[(b, i, h)] = latent_attention_head(q_abs[b, i, h, :d_c], q_abs[b, i, h, d_c:],
+                                               seq_rows[b][:L], L - n_q + i, d_c, scale)
+    if samples is not None:
+        return res
+    out = np.full((B, n_q, n_h, d_c), np.nan)
+    for (b, i, h), v in res.items():
+        out[b, i, h] = v
+    return out
+
+
 def default_scale(d_nope, d_r):
     """Score scale 1/sqrt(d_nope + d_r). A head's query/key width is d_nope + d_r."""
     return 1.0 / math.sqrt(d_nope + d_r)

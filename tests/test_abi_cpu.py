@@ -98,6 +98,13 @@ def test_null_and_count_checks(lib):
     assert lib.mla_decode_layer(ctypes.byref(cfg), None, None, None, None, None, None, None, 1,
                                 None, 1, None, 1, 1, None, None, None, 0, None) == 1
     assert lib.mla_get_last_device_error(None, None) == 1
+    # the attention core alone: null pointers, and an o_lat off its 16-byte
+    # alignment (never dereferenced: refused before any device work)
+    assert lib.mla_decode_latent(ctypes.byref(cfg), None, None, 1, None, 1, None, 1, 1, None,
+                                 None, 0, None) == 1
+    fake = ctypes.c_void_p(256)
+    assert lib.mla_decode_latent(ctypes.byref(cfg), fake, fake, 1, fake, 1, fake, 1, 1,
+                                 ctypes.c_void_p(256 + 4), fake, 1 << 20, None) == 1
 
 
 def test_no_gpu_means_a_loud_cuda_error(lib):

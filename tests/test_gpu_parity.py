@@ -449,6 +449,38 @@ def test_decode_latent_core_small(impl, n_q):
     r.dw.free()
 
 
+def test_decode_latent_core_unaligned_buffers():
+    """q_abs one element off its 16-byte alignment: the query copy takes
+    scalar loads and the result matches the oracle as the aligned call does.
+    An o_lat off its 16-byte alignment is refused on the host (both merge
+    kernels store 16-byte vectors), with nothing queued."""
+    w, lens = small_workload(lens=(3, 100, 129), n_q=2, seed=62)
+    r = Run(w, lens, _lib.MLA_IMPL_TENSOR_CORE)
+    qv, qs = synth.latent_queries(w)
+    qd = to_device(qs, w.dtype)
+    qbuf = torch.empty(qd.numel() + 1, dtype=qd.dtype, device="cuda")
+    qbuf[1:].copy_(qd.reshape(-1))
+    q_off = qbuf[1:].view(qd.shape)
+    assert q_off.data_ptr() % 16 != 0
+    o = torch.full((w.batch, w.n_q, w.n_h, w.d_c), float("nan"), device="cuda")
+    _lib.mla_decode_latent(r.cfg, q_off, r.cache, r.pt, r.sl, o, r.ws)
+    torch.cuda.synchronize()
+    st, code = _lib.mla_get_last_device_error()
+    assert code == 0
+    got = o.cpu().numpy()
+    ref = O.decode_latent(qv, r.rows, lens, w.d_c, w.scale)
+    keys = [(b, i, h) for b in range(w.batch) for i in range(w.n_q) for h in range(w.n_h)]
+    check_bf16_each([got[k] for k in keys], [ref[k] for k in keys], "latent unaligned q")
+    obuf = torch.zeros(o.numel() + 1, device="cuda")
+    o_off = obuf[1:].view(o.shape)
+    with pytest.raises(_lib.MlaError) as ei:
+        _lib.mla_decode_latent(r.cfg, q_off, r.cache, r.pt, r.sl, o_off, r.ws)
+    assert ei.value.status == 1  # MLA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.all(obuf == 0)
+    r.dw.free()
+
+
 def test_decode_latent_core_fp32():
     w = synth.WORKLOADS["tiny_fp32"]
     lens = synth.seq_lens(w)

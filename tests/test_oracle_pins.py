@@ -360,6 +360,71 @@ def test_two_queries_are_causal():
     assert np.max(np.abs(both2[1] - both[1])) > 1e-6
 
 
+def _latent_queries(t, n_q):
+    """q_abs [1, n_q, n_h, d_c + d_r]: per head [W_uk[h]^T q_nope | RoPE(q_rope,
+    position)], the absorbed form of the tiny case's queries."""
+    d_c, d_nope, n_h, L = t["d_c"], t["d_nope"], t["n_h"], t["L"]
+    q_abs = np.zeros((1, n_q, n_h, d_c + t["d_r"]))
+    for i in range(n_q):
+        for h in range(n_h):
+            q = t["q"][0, i, h]
+            q_abs[0, i, h, :d_c] = O.head_slice(t["W_uk"], h, d_nope) @ q[:d_nope]
+            q_abs[0, i, h, d_c:] = O.apply_rope(q[d_nope:], L - n_q + i, 10000.0)
+    return q_abs
+
+
+@pytest.mark.parametrize("n_q", [1, 2])
+def test_latent_core_up_projected_is_library_attention(n_q):
+    """The attention core on absorbed queries, up-projected through W_uv[h]
+    afterwards, equals torch's scaled_dot_product_attention over the
+    explicitly built keys and values (causal for n_q = 2)."""
+    t = _tiny(seed=11)
+    scale = O.default_scale(t["d_nope"], t["d_r"])
+    o_lat = O.decode_latent(_latent_queries(t, n_q), [t["rows"]], [t["L"]], t["d_c"], scale)[0]
+    ref = _sdpa_reference(t, n_q)
+    for h in range(t["n_h"]):
+        got = o_lat[:, h] @ O.head_slice(t["W_uv"], h, t["d_v"])
+        assert np.max(np.abs(got - ref[:, h])) < 1e-10
+
+
+def test_latent_core_closed_forms():
+    """One visible key: o_lat is that key's latent row. Equal latent rows and
+    zero rope parts: every score is equal and o_lat is the shared row."""
+    t = _tiny(seed=12, L=30)
+    d_c = t["d_c"]
+    q_abs = _latent_queries(t, 1)[0, 0]
+    for h in range(t["n_h"]):
+        o = O.latent_attention_head(q_abs[h, :d_c], q_abs[h, d_c:], t["rows"], 0, d_c, 0.3)
+        assert np.array_equal(o, t["rows"][0, :d_c])
+    rows = np.repeat(t["rows"][3:4], 30, axis=0)
+    rows[:, d_c:] = 0.0
+    o = O.latent_attention_head(q_abs[1, :d_c], q_abs[1, d_c:], rows, 29, d_c, 0.3)
+    assert np.max(np.abs(o - rows[0, :d_c])) < 1e-14
+
+
+ORIG_LATENT_HEAD = O.latent_attention_head
+
+
+def _latent_mutants():
+    def without_position_term(q_lat, q_pe, rows, pos_q, d_c, scale):
+        return ORIG_LATENT_HEAD(q_lat, np.zeros_like(q_pe), rows, pos_q, d_c, scale)
+
+    def unscaled(q_lat, q_pe, rows, pos_q, d_c, scale):
+        return ORIG_LATENT_HEAD(q_lat, q_pe, rows, pos_q, d_c, 1.0)
+
+    def mask_one_short(q_lat, q_pe, rows, pos_q, d_c, scale):
+        return ORIG_LATENT_HEAD(q_lat, q_pe, rows, pos_q - 1, d_c, scale)
+
+    return [without_position_term, unscaled, mask_one_short]
+
+
+@pytest.mark.parametrize("idx", range(3))
+def test_planted_latent_core_mistakes_are_caught(monkeypatch, idx):
+    monkeypatch.setattr(O, "latent_attention_head", _latent_mutants()[idx])
+    with pytest.raises(AssertionError):
+        test_latent_core_up_projected_is_library_attention(2)
+
+
 def test_default_scale_is_torch_attention_default():
     """The score scale over the full query/key width d_nope + d_r.
 
