@@ -39,9 +39,9 @@ __device__ __forceinline__ __half from_f32<__half>(float v) {
 // fp64 rate is low). Its top 32 bits, read as a signed number, are the angle
 // in [-1/2, 1/2) turns; sincospif evaluates sin/cos of pi times twice that.
 // The representation error of theta_i / (2 pi) is at most 2^-65 turns, so
-// the angle is good to about 2^-48 turns at positions up to 2^17; the fp32
-// argument of sincospif adds at most 2^-25 (relative to pi), as a directly
-// reduced fp32 angle would.
+// the product is good to about 2^-48 turns at positions up to 2^17; the fp32
+// argument of sincospif then keeps 24 bits of it, as a directly reduced fp32
+// angle would.
 __device__ __forceinline__ void rope_cos_sin(int pos, uint64_t rope_turns, float* c, float* s) {
   const uint64_t f = static_cast<uint64_t>(static_cast<uint32_t>(pos)) * rope_turns;
   const int32_t hi = static_cast<int32_t>(static_cast<uint32_t>(f >> 32));
