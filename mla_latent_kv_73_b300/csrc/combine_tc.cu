@@ -21,7 +21,13 @@
 // its own TMEM accumulator. The hi + lo split keeps about 16 bits of o_lat's
 // mantissa, so rounding o_lat for the tensor core costs no measurable
 // accuracy. Four warps read the four fp32 accumulators from TMEM, one output
-// column per lane, add them in a fixed order and store the sum.
+// column per lane, add them in a fixed order and store the sum. For the
+// layer step they also store the sum as a bf16 hi + lo pair, the operand of
+// the tensor-core W_o projection.
+//
+// The latent mode (mla_decode_latent, the attention core alone) keeps only
+// the merge: each thread writes its 8 merged o_lat values straight to
+// global memory, with no W_uv, TMEM or MMA.
 #include <cmath>
 #include <cstring>
 
