@@ -128,6 +128,7 @@ def test_layer_dsv2_widths():
 
 @pytest.mark.parametrize("lens,n_q,d_model", [
     ((3, 64, 65, 130, 200, 257) * 4, 2, 200),  # 48 tokens; outputs 128..199 fill a tile partly
+    ((7, 64, 129, 300) * 8, 2, 384),            # 64 tokens: the projection's widest token tile
     ((5, 90) * 20, 2, 256),                     # 80 tokens: past the tensor-core projection's 64
 ])
 def test_layer_token_counts_and_ragged_outputs(lens, n_q, d_model):
