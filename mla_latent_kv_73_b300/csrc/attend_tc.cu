@@ -574,7 +574,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qc,
       prefetch_tmap(&tmap_qr);
       prefetch_tmap(&tmap_kc);
       prefetch_tmap(&tmap_kr);
-      const uint64_t pol = policy_evict_first();
+      // With one 128-row group per sequence every page is read once: stream
+      // it past L2. With several (two query tokens, prefill chunks) each group
+      // reads the page again, and the pairs walking the other groups read it
+      // at about the same time: keep it in L2.
+      const uint64_t pol = a.G > 1 ? policy_evict_normal() : policy_evict_first();
       const int xr = 512 + 32 * static_cast<int>(rank);
       uint32_t kv_it = 0;
       int piece_idx = 0;
