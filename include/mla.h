@@ -401,9 +401,10 @@ mla_status mla_decode_full(const mla_config* cfg, mla_full_weights fw, const voi
  * plainly" (W_o [n_h*head_dim -> d_model] among the layer's weights).
  * ------------------------------------------------------------------------ */
 
-/* Bytes of device workspace that mla_decode_layer needs (the decode's plus
- * the projection's split partials). Writes the size to *bytes (a host
- * pointer). */
+/* Bytes of device workspace that mla_decode_layer needs (the decode's, the
+ * bf16 hi/lo copy of out that the tensor-core projection reads for up to 64
+ * new tokens, and the projection's split partials). Writes the size to
+ * *bytes (a host pointer). */
 mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int32_t n_q,
                                            size_t* bytes);
 
@@ -419,8 +420,11 @@ mla_status mla_decode_layer_workspace_size(const mla_config* cfg, int32_t B, int
  *   y          [B, n_q, d_model] fp32: the layer output
  *   workspace  at least mla_decode_layer_workspace_size() bytes, 256-byte
  *              aligned
- * The projection accumulates in fp32. Errors as in mla_append_kv and
- * mla_decode. */
+ * The projection accumulates in fp32. With the tensor-core decode, up to 64
+ * new tokens, d_model and n_h*d_v multiples of 8, a 16-byte aligned W_o and
+ * a 16-byte aligned out, it runs on the tensor cores: out enters as a bf16
+ * hi + lo pair (about 16 bits of its mantissa). Otherwise it runs on the
+ * CUDA cores from out in fp32. Errors as in mla_append_kv and mla_decode. */
 mla_status mla_decode_layer(const mla_config* cfg, mla_weights w, const void* W_o, const void* x,
                             const int32_t* seq_idx, const int32_t* pos, const void* q,
                             void* cache, int32_t num_blocks, const int32_t* page_table,
