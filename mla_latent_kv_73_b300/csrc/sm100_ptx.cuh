@@ -88,16 +88,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// Pulls a tile of a tensor into L2 (no shared-memory destination, no
-// completion signal). L2 is coherent, so this is safe before the data's
-// producer has finished; only the later load must wait.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m, int32_t x,
                                             int32_t y, int32_t z, uint64_t* bar) {
   asm volatile(
